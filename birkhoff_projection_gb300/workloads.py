@@ -1,0 +1,112 @@
+"""Seeded synthetic inputs for the 4x4 Birkhoff projection.
+
+Shared by the tests, the benchmark and the oracle checks.  This module only
+draws random numbers in the shapes and distributions of the workloads; it
+holds none of the projection's arithmetic and imports neither the CUDA
+library nor the oracle.
+
+Workloads (all tokens are [4,4] row-major; T = number of tokens):
+  small_normal     T = 4096, X fp32 iid N(0,1), seed 0 (forward only)
+  normal_1m        T = 2^20, X and upstream dP fp32 iid N(0,1), seed 1
+  large_magnitude  T = 2^20, X_ij = 20 Z_ij + r_i + c_j, Z ~ N(0,1),
+                   r_i, c_j ~ U[-50,50] per token, fp32, seed 2
+  mhc_batch        X bf16 [64, 32, 8192, 4, 4] (2^24 tokens),
+                   X = Z + 0.5 s I with Z ~ N(0,1) per entry and one
+                   s ~ N(0,1) per token (diagonal bias); dP bf16 N(0,1), seed 3
+  sweep            T = 2^12 ... 2^26, X fp32 iid N(0, sigma^2),
+                   sigma in {1, 10}, seed 4
+"""
+from __future__ import annotations
+
+import torch
+
+SWEEP_LOG2_T = list(range(12, 27))
+SWEEP_SIGMAS = (1.0, 10.0)
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    return torch.Generator(device=torch.device(device)).manual_seed(seed)
+
+
+def normal(T: int, sigma: float = 1.0, seed: int = 0, device="cpu",
+           dtype=torch.float32) -> torch.Tensor:
+    """X [T,4,4] iid N(0, sigma^2), drawn in fp32 then cast to ``dtype``."""
+    g = _gen(seed, device)
+    x = torch.randn(T, 4, 4, generator=g, device=device, dtype=torch.float32)
+    if sigma != 1.0:
+        x.mul_(sigma)
+    return x.to(dtype)
+
+
+def small_normal(device="cpu") -> torch.Tensor:
+    return normal(4096, 1.0, seed=0, device=device)
+
+
+def normal_1m(T: int = 1 << 20, device="cpu"):
+    """(X, dP), both [T,4,4] fp32 iid N(0,1) from one stream, seed 1."""
+    g = _gen(1, device)
+    x = torch.randn(T, 4, 4, generator=g, device=device, dtype=torch.float32)
+    dp = torch.randn(T, 4, 4, generator=g, device=device, dtype=torch.float32)
+    return x, dp
+
+
+def large_magnitude(T: int = 1 << 20, device="cpu"):
+    """(X, dP): X_ij = 20 Z_ij + r_i + c_j with r, c ~ U[-50, 50] per token
+    (|X| up to about 200); dP iid N(0,1).  Seed 2."""
+    g = _gen(2, device)
+    z = torch.randn(T, 4, 4, generator=g, device=device, dtype=torch.float32)
+    r = torch.rand(T, 4, 1, generator=g, device=device, dtype=torch.float32) * 100.0 - 50.0
+    c = torch.rand(T, 1, 4, generator=g, device=device, dtype=torch.float32) * 100.0 - 50.0
+    x = 20.0 * z + r + c
+    dp = torch.randn(T, 4, 4, generator=g, device=device, dtype=torch.float32)
+    return x, dp
+
+
+MHC_SHAPE = (64, 32, 8192)
+
+
+def mhc_batch(shape=MHC_SHAPE, device="cpu"):
+    """(X, dP) bf16 [*shape, 4, 4]: X = Z + 0.5 s I (one s per token), seed 3."""
+    g = _gen(3, device)
+    z = torch.randn(*shape, 4, 4, generator=g, device=device, dtype=torch.float32)
+    s = torch.randn(*shape, 1, 1, generator=g, device=device, dtype=torch.float32)
+    eye = torch.eye(4, device=device, dtype=torch.float32)
+    x = (z + 0.5 * s * eye).to(torch.bfloat16)
+    dp = torch.randn(*shape, 4, 4, generator=g, device=device,
+                     dtype=torch.float32).to(torch.bfloat16)
+    return x, dp
+
+
+def sweep(log2_T: int, sigma: float, device="cpu"):
+    """(X, dP) for the throughput sweep: X fp32 iid N(0, sigma^2), dP N(0,1)."""
+    T = 1 << log2_T
+    g = _gen(4, device)
+    x = torch.randn(T, 4, 4, generator=g, device=device, dtype=torch.float32)
+    if sigma != 1.0:
+        x.mul_(sigma)
+    dp = torch.randn(T, 4, 4, generator=g, device=device, dtype=torch.float32)
+    return x, dp
+
+
+def fixed_point_family(T: int, seed: int, spread: float = 5.0, floor: float = 1e-3,
+                       device="cpu", dtype=torch.float64):
+    """(X, Q) with Q strictly positive and doubly stochastic and
+    X = log Q + u 1^T + 1 v^T (u, v ~ U[-spread, spread] per token).
+
+    Q mixes the 24 permutation matrices with Dirichlet(1) weights plus
+    ``floor`` times the uniform matrix, renormalised; the projection of X is Q
+    exactly, whatever the offsets.  Built in float64."""
+    import itertools
+
+    g = _gen(seed, device)
+    perms = torch.tensor(list(itertools.permutations(range(4))), device=device)
+    pm = torch.zeros(24, 4, 4, dtype=torch.float64, device=device)
+    pm[torch.arange(24).repeat_interleave(4), torch.arange(4).repeat(24), perms.reshape(-1)] = 1.0
+    w = -torch.log(torch.rand(T, 24, generator=g, device=device, dtype=torch.float64))
+    w = w / w.sum(dim=1, keepdim=True)
+    q = torch.einsum("tk,kij->tij", w, pm)
+    q = (q + floor / 4.0) / (1.0 + floor)
+    u = (torch.rand(T, 4, 1, generator=g, device=device, dtype=torch.float64) * 2 - 1) * spread
+    v = (torch.rand(T, 1, 4, generator=g, device=device, dtype=torch.float64) * 2 - 1) * spread
+    x = torch.log(q) + u + v
+    return x.to(dtype), q

@@ -1,0 +1,419 @@
+/*
+ * birkhoff4_oracle.c -- float64 CPU oracle for the per-token 4x4 Birkhoff
+ * projection.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain checker that the
+ * CUDA path is compared against.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference leg of bench.py may load it.  It shares no code,
+ * header, table or constant with the CUDA library, and nothing in the product
+ * path may call it.
+ *
+ * Sources (page titles and sections):
+ *   [mHC] "Accelerating the Birkhoff Projection for Manifold-Constrained
+ *         Hyper-Connections" (technical summary, arXiv 2606.07574), in its
+ *         Spanish and French renderings.
+ *     s1   : the projection maps each residual mixing matrix onto the Birkhoff
+ *            polytope (doubly stochastic matrices); current mHC runs
+ *            Sinkhorn-Knopp for it, often with a small fixed iteration count.
+ *     s2   : the projection is entropic optimal transport.
+ *     s2.1 : the dual is reduced to m-1 = 3 free variables (the duals are only
+ *            defined up to a common scalar shift); closed-form gradient and
+ *            Hessian; Newton's method; rows shifted by their maximum before the
+ *            softmax.
+ *     s2.2 : the backward pass uses the implicit function theorem on that
+ *            dual; the last Newton Hessian is the matrix of the linear system.
+ *
+ * Every token is one X in R^{4x4}, row-major: element (t,i,j) sits at offset
+ * 16*t + 4*i + j.  The projection is P = diag(e^a) exp(X) diag(e^b) with unit
+ * row and column sums (entropic OT with epsilon = 1 and uniform unit
+ * marginals); P is unique by Sinkhorn's theorem.  The gauge is b[3] = 0.
+ *
+ * Functions (all batched over T tokens, OpenMP over tokens):
+ *   oracle_sinkhorn64   : log-domain Sinkhorn-Knopp.  With tol > 0 it runs to
+ *                         max(row, column residual) < tol or max_iters; with
+ *                         tol <= 0 it runs exactly max_iters iterations (the
+ *                         fixed-iteration scheme of [mHC s1]).
+ *   oracle_newton64     : Newton's method on the reduced 3-variable dual
+ *                         [mHC s2.1] with an Armijo backtracking line search.
+ *   oracle_backward64   : vector-Jacobian product dX = (dP/dX)^T G through the
+ *                         implicit function theorem on the reduced dual
+ *                         [mHC s2.2].
+ *
+ * Build: gcc -O2 -fopenmp -fPIC -shared (no fast-math).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_VERSION 1
+
+int oracle_version(void) { return ORACLE_VERSION; }
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* log(sum_k exp(v[k])) for four values, shifted by the maximum. */
+static double lse4(double v0, double v1, double v2, double v3)
+{
+    double m = v0;
+    if (v1 > m) m = v1;
+    if (v2 > m) m = v2;
+    if (v3 > m) m = v3;
+    if (isinf(m) && m < 0) return m;
+    return m + log(exp(v0 - m) + exp(v1 - m) + exp(v2 - m) + exp(v3 - m));
+}
+
+/* max over rows of |row sum - 1| and over columns of |column sum - 1|. */
+static double marginal_residual(const double p[16])
+{
+    double res = 0.0;
+    for (int i = 0; i < 4; ++i) {
+        double s = p[4 * i] + p[4 * i + 1] + p[4 * i + 2] + p[4 * i + 3];
+        double d = fabs(s - 1.0);
+        if (d > res || isnan(d)) res = d;
+    }
+    for (int j = 0; j < 4; ++j) {
+        double s = p[j] + p[4 + j] + p[8 + j] + p[12 + j];
+        double d = fabs(s - 1.0);
+        if (d > res || isnan(d)) res = d;
+    }
+    return res;
+}
+
+/* A token with a NaN or infinite logit has no projection (exp(X) is not a
+ * strictly positive finite matrix); its outputs are all NaN. */
+static int nonfinite_token(const double x[16], double p[16], double *b)
+{
+    for (int k = 0; k < 16; ++k) {
+        if (!isfinite(x[k])) {
+            for (int q = 0; q < 16; ++q) p[q] = NAN;
+            if (b)
+                for (int q = 0; q < 4; ++q) b[q] = NAN;
+            return 1;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sinkhorn-Knopp in the log domain [mHC s1, s2].                            */
+/* One iteration: a_i = -LSE_j(X_ij + b_j) (rows), then                      */
+/*                b_j = -LSE_i(X_ij + a_i) (columns).                        */
+/* The output is P = exp(X_ij + a_i + b_j) after the last column step.       */
+/* ------------------------------------------------------------------------ */
+static int sinkhorn_token(const double x[16], double p[16], double bout[4],
+                          double tol, int32_t max_iters, int32_t *iters)
+{
+    double a[4] = {0, 0, 0, 0}, b[4] = {0, 0, 0, 0};
+    int converged = 0;
+    if (nonfinite_token(x, p, bout)) {
+        if (iters) *iters = 0;
+        return 0;
+    }
+    int32_t it = 0;
+    while (it < max_iters) {
+        for (int i = 0; i < 4; ++i)
+            a[i] = -lse4(x[4 * i] + b[0], x[4 * i + 1] + b[1], x[4 * i + 2] + b[2],
+                         x[4 * i + 3] + b[3]);
+        for (int j = 0; j < 4; ++j)
+            b[j] = -lse4(x[j] + a[0], x[4 + j] + a[1], x[8 + j] + a[2], x[12 + j] + a[3]);
+        ++it;
+        if (tol > 0.0) {
+            double q[16];
+            for (int i = 0; i < 4; ++i)
+                for (int j = 0; j < 4; ++j) q[4 * i + j] = exp(x[4 * i + j] + a[i] + b[j]);
+            if (marginal_residual(q) < tol) {
+                converged = 1;
+                break;
+            }
+        }
+    }
+    for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 4; ++j) p[4 * i + j] = exp(x[4 * i + j] + a[i] + b[j]);
+    if (bout) {
+        /* gauge b[3] = 0; a absorbs the shift (P is unchanged) */
+        double s = b[3];
+        for (int j = 0; j < 4; ++j) bout[j] = b[j] - s;
+    }
+    if (iters) *iters = it;
+    if (tol <= 0.0) converged = 1;
+    return converged;
+}
+
+/* Returns the number of tokens that did not reach tol (0 when tol <= 0). */
+int64_t oracle_sinkhorn64(const double *X, double *P, double *b, int64_t T, double tol,
+                          int32_t max_iters, int32_t *iters_out)
+{
+    int64_t nonconv = 0;
+    if (T <= 0) return 0;
+#pragma omp parallel for schedule(dynamic, 64) reduction(+ : nonconv)
+    for (int64_t t = 0; t < T; ++t) {
+        int32_t it = 0;
+        int ok = sinkhorn_token(X + 16 * t, P + 16 * t, b ? b + 4 * t : NULL, tol, max_iters, &it);
+        if (!ok) ++nonconv;
+        if (iters_out) iters_out[t] = it;
+    }
+    return nonconv;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Newton's method on the reduced dual [mHC s2.1].                           */
+/*                                                                           */
+/*   phi(b) = sum_i LSE_j(X_ij + b_j) - sum_j b_j,   b_3 = 0                 */
+/*   p_ij(b) = softmax_j(X_ij + b_j)        (row softmax, rows shifted by     */
+/*                                           their maximum)                  */
+/*   grad_j  = sum_i p_ij - 1                                   (j = 0..2)   */
+/*   Hess_jk = sum_i p_ij (delta_jk - p_ik)                     (j,k = 0..2) */
+/*                                                                           */
+/* The diagonal term p_ij (1 - p_ij) is evaluated as p_ij * sum_{l!=j} p_il  */
+/* (equal because every row of p sums to one) so that it does not cancel     */
+/* when p_ij is close to 1.  The 3x3 system is solved by Cholesky after a    */
+/* symmetric diagonal (Jacobi) scaling.  A Newton step longer than 32 in    */
+/* the max norm is scaled down to 32 (far from the solution the dual is      */
+/* nearly flat along some directions and the raw step is unbounded); the     */
+/* step length then comes from Armijo backtracking on phi (on the marginal  */
+/* residual once the predicted decrease of phi is below its rounding error). */
+/* The iteration stops at residual <= tol, after                             */
+/* max_iters steps, or when the residual is below 1e-10 and has not improved */
+/* for 8 steps (rounding regime); the                                        */
+/* best iterate seen is returned.                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Evaluate the row softmax p(b), phi(b) and the gradient (all four columns). */
+static double dual_eval(const double x[16], const double b[4], double p[16], double g[4])
+{
+    double phi = -(b[0] + b[1] + b[2] + b[3]);
+    for (int i = 0; i < 4; ++i) {
+        double z[4];
+        double m = -INFINITY;
+        for (int j = 0; j < 4; ++j) {
+            z[j] = x[4 * i + j] + b[j];
+            if (z[j] > m) m = z[j];
+        }
+        double e[4], s = 0.0;
+        for (int j = 0; j < 4; ++j) {
+            e[j] = exp(z[j] - m);
+            s += e[j];
+        }
+        for (int j = 0; j < 4; ++j) p[4 * i + j] = e[j] / s;
+        phi += m + log(s);
+    }
+    for (int j = 0; j < 4; ++j) g[j] = p[j] + p[4 + j] + p[8 + j] + p[12 + j] - 1.0;
+    return phi;
+}
+
+/* Hessian of phi with respect to b_0..b_2, from a row-normalised p. */
+static void dual_hessian(const double p[16], double H[3][3])
+{
+    for (int j = 0; j < 3; ++j) {
+        for (int k = 0; k < 3; ++k) {
+            double h = 0.0;
+            for (int i = 0; i < 4; ++i) {
+                const double *pi = p + 4 * i;
+                if (j == k) {
+                    double rest = 0.0;
+                    for (int l = 0; l < 4; ++l)
+                        if (l != j) rest += pi[l];
+                    h += pi[j] * rest;
+                } else {
+                    h -= pi[j] * pi[k];
+                }
+            }
+            H[j][k] = h;
+        }
+    }
+}
+
+/* Solve H x = r for a symmetric positive definite 3x3 H: Jacobi scaling then
+ * Cholesky.  Returns 0 on success, -1 if H is not numerically positive
+ * definite. */
+static int spd3_solve(const double H[3][3], const double r[3], double x[3])
+{
+    double d[3];
+    for (int j = 0; j < 3; ++j) {
+        if (!(H[j][j] > 0.0)) return -1;
+        d[j] = 1.0 / sqrt(H[j][j]);
+    }
+    double A[3][3];
+    for (int j = 0; j < 3; ++j)
+        for (int k = 0; k < 3; ++k) A[j][k] = d[j] * H[j][k] * d[k];
+    double L[3][3] = {{0}};
+    for (int j = 0; j < 3; ++j) {
+        double s = A[j][j];
+        for (int k = 0; k < j; ++k) s -= L[j][k] * L[j][k];
+        if (!(s > 0.0)) return -1;
+        L[j][j] = sqrt(s);
+        for (int i = j + 1; i < 3; ++i) {
+            double t = A[i][j];
+            for (int k = 0; k < j; ++k) t -= L[i][k] * L[j][k];
+            L[i][j] = t / L[j][j];
+        }
+    }
+    double y[3], z[3];
+    for (int j = 0; j < 3; ++j) {
+        double s = d[j] * r[j];
+        for (int k = 0; k < j; ++k) s -= L[j][k] * y[k];
+        y[j] = s / L[j][j];
+    }
+    for (int j = 2; j >= 0; --j) {
+        double s = y[j];
+        for (int k = j + 1; k < 3; ++k) s -= L[k][j] * z[k];
+        z[j] = s / L[j][j];
+    }
+    for (int j = 0; j < 3; ++j) x[j] = d[j] * z[j];
+    return 0;
+}
+
+static int newton_token(const double x[16], double pout[16], double bout[4], double tol,
+                        int32_t max_iters, int32_t *iters, double *trace, int32_t trace_len)
+{
+    double b[4] = {0, 0, 0, 0};
+    double p[16], g[4];
+    if (nonfinite_token(x, pout, bout)) {
+        if (iters) *iters = 0;
+        if (trace)
+            for (int32_t q = 0; q < trace_len; ++q) trace[q] = NAN;
+        return 0;
+    }
+    double best_p[16], best_b[4], best_res = INFINITY;
+    int32_t best_k = 0, since_best = 0;
+    double phi = dual_eval(x, b, p, g);
+    int32_t k = 0;
+    if (trace)
+        for (int32_t q = 0; q < trace_len; ++q) trace[q] = NAN;
+    for (;;) {
+        double res = marginal_residual(p);
+        if (trace && k < trace_len) trace[k] = res;
+        if (k == 0 || res < best_res) { /* k == 0: a NaN token keeps its NaN P */
+            best_res = res;
+            memcpy(best_p, p, sizeof best_p);
+            memcpy(best_b, b, sizeof best_b);
+            best_k = k;
+            since_best = 0;
+        } else {
+            ++since_best;
+        }
+        if (res <= tol || k >= max_iters || isnan(res)) break;
+        /* stalled in the rounding regime: more steps cannot help */
+        if (since_best >= 8 && best_res < 1e-10) break;
+
+        double H[3][3], step[3];
+        dual_hessian(p, H);
+        if (spd3_solve(H, g, step) != 0) {
+            /* not numerically positive definite: fall back to a gradient step */
+            for (int j = 0; j < 3; ++j) step[j] = g[j];
+        }
+        double smax = fmax(fabs(step[0]), fmax(fabs(step[1]), fabs(step[2])));
+        if (smax > 32.0)
+            for (int j = 0; j < 3; ++j) step[j] *= 32.0 / smax;
+        double slope = g[0] * step[0] + g[1] * step[1] + g[2] * step[2];
+        double t = 1.0;
+        double bn[4], pn[16], gn[4], phin = phi;
+        int accepted = 0;
+        for (int ls = 0; ls < 60; ++ls) {
+            bn[0] = b[0] - t * step[0];
+            bn[1] = b[1] - t * step[1];
+            bn[2] = b[2] - t * step[2];
+            bn[3] = 0.0;
+            phin = dual_eval(x, bn, pn, gn);
+            /* Armijo sufficient decrease on phi */
+            if (phin <= phi - 1e-4 * t * slope) {
+                accepted = 1;
+                break;
+            }
+            /* Near the solution the predicted decrease t*slope falls below the
+             * rounding error of phi itself and the Armijo test is noise; there
+             * the step is judged by the marginal residual instead. */
+            if (t * slope <= 1e-12 * (fabs(phi) + 1.0) && marginal_residual(pn) < res) {
+                accepted = 1;
+                break;
+            }
+            t *= 0.5;
+        }
+        ++k;
+        if (!accepted) {
+            /* no decrease possible in floating point: stop at the best iterate */
+            break;
+        }
+        memcpy(b, bn, sizeof b);
+        memcpy(p, pn, sizeof p);
+        memcpy(g, gn, sizeof g);
+        phi = phin;
+    }
+    memcpy(pout, best_p, sizeof best_p);
+    if (bout) memcpy(bout, best_b, sizeof best_b);
+    if (iters) *iters = best_k;
+    return best_res <= tol;
+}
+
+/* Returns the number of tokens whose best residual stayed above tol.
+ * trace (optional) is [T, trace_len]: residual after each Newton step
+ * (index 0 = at b = 0), NaN past the end. */
+int64_t oracle_newton64(const double *X, double *P, double *b, int64_t T, double tol,
+                        int32_t max_iters, int32_t *iters_out, double *trace, int32_t trace_len)
+{
+    int64_t nonconv = 0;
+    if (T <= 0) return 0;
+#pragma omp parallel for schedule(dynamic, 64) reduction(+ : nonconv)
+    for (int64_t t = 0; t < T; ++t) {
+        int32_t it = 0;
+        int ok = newton_token(X + 16 * t, P + 16 * t, b ? b + 4 * t : NULL, tol, max_iters, &it,
+                              trace ? trace + (int64_t)trace_len * t : NULL, trace_len);
+        if (!ok) ++nonconv;
+        if (iters_out) iters_out[t] = it;
+    }
+    return nonconv;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass by the implicit function theorem [mHC s2.2].                */
+/*                                                                           */
+/* P(X) = p(X, b*(X)) with p the row softmax of X + b and b* defined by      */
+/* F(X, b) = grad_b phi = colsum(p) - 1 = 0 (components 0..2, b_3 = 0).      */
+/* For a loss L with G = dL/dP:                                              */
+/*   dL/dX = dL/dX|_b  -  lambda^T dF/dX,   Hess lambda = dL/db|_X            */
+/* where, with r_k = sum_j G_kj p_kj,                                        */
+/*   dL/dX_kl |_b = p_kl (G_kl - r_k)                                         */
+/*   dL/db_l  |_X = sum_k p_kl (G_kl - r_k)                    (l = 0..2)    */
+/*   dF_l/dX_kq   = p_kl (delta_lq - p_kq)                                    */
+/* Hess is the dual Hessian at P (the matrix of the last Newton step).       */
+/* ------------------------------------------------------------------------ */
+static void backward_token(const double p[16], const double G[16], double dX[16])
+{
+    double direct[16], r[4];
+    for (int k = 0; k < 4; ++k) {
+        r[k] = 0.0;
+        for (int j = 0; j < 4; ++j) r[k] += G[4 * k + j] * p[4 * k + j];
+        for (int j = 0; j < 4; ++j) direct[4 * k + j] = p[4 * k + j] * (G[4 * k + j] - r[k]);
+    }
+    double v[3];
+    for (int l = 0; l < 3; ++l) v[l] = direct[l] + direct[4 + l] + direct[8 + l] + direct[12 + l];
+    double H[3][3], lam[3] = {0, 0, 0};
+    dual_hessian(p, H);
+    if (spd3_solve(H, v, lam) != 0) lam[0] = lam[1] = lam[2] = NAN;
+    for (int k = 0; k < 4; ++k) {
+        double s = 0.0; /* sum_l lambda_l p_kl */
+        for (int l = 0; l < 3; ++l) s += lam[l] * p[4 * k + l];
+        for (int q = 0; q < 4; ++q) {
+            double dF = -s * p[4 * k + q];
+            if (q < 3) dF += lam[q] * p[4 * k + q];
+            dX[4 * k + q] = direct[4 * k + q] - dF;
+        }
+    }
+}
+
+void oracle_backward64(const double *P, const double *G, double *dX, int64_t T)
+{
+    if (T <= 0) return;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) backward_token(P + 16 * t, G + 16 * t, dX + 16 * t);
+}
