@@ -74,6 +74,8 @@ def _load():
         lib.oracle_newton64.restype = i64
         lib.oracle_backward64.argtypes = [dp, dp, dp, i64]
         lib.oracle_backward64.restype = None
+        lib.oracle_laplacian_solve64.argtypes = [dp, dp, dp, i64]
+        lib.oracle_laplacian_solve64.restype = i64
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_version.restype = ctypes.c_int
         _lib = lib
@@ -197,6 +199,18 @@ def unrolled_sinkhorn_backward64(X, G, iters: int = 2000):
     P = torch.exp(x + a + b)
     (P * g).sum().backward()
     return P.detach().numpy(), x.grad.detach().numpy()
+
+
+def laplacian_solve64(w, r):
+    """Solve H x = r where H is the Laplacian of the complete graph on four
+    nodes with edge weights w [n,6] (edges (0,1),(0,2),(0,3),(1,2),(1,3),(2,3)),
+    restricted to nodes 0..2; closed form by the matrix-tree theorem."""
+    lib = _load()
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.float64).reshape(-1, 6))
+    r = np.ascontiguousarray(np.asarray(r, dtype=np.float64).reshape(-1, 3))
+    x = np.empty_like(r)
+    lib.oracle_laplacian_solve64(_ptr(w), _ptr(r), _ptr(x), w.shape[0])
+    return x
 
 
 def marginal_residual(P) -> np.ndarray:

@@ -176,8 +176,8 @@ int64_t oracle_sinkhorn64(const double *X, double *P, double *b, int64_t T, doub
 /*                                                                           */
 /* The diagonal term p_ij (1 - p_ij) is evaluated as p_ij * sum_{l!=j} p_il  */
 /* (equal because every row of p sums to one) so that it does not cancel     */
-/* when p_ij is close to 1.  The 3x3 system is solved by Cholesky after a    */
-/* symmetric diagonal (Jacobi) scaling.  A Newton step longer than 32 in    */
+/* when p_ij is close to 1.  The 3x3 system is solved in closed form by the */
+/* matrix-tree theorem (hessian_solve).  A Newton step longer than 32 in     */
 /* the max norm is scaled down to 32 (far from the solution the dual is      */
 /* nearly flat along some directions and the raw step is unbounded); the     */
 /* step length then comes from Armijo backtracking on phi (on the marginal  */
@@ -211,66 +211,125 @@ static double dual_eval(const double x[16], const double b[4], double p[16], dou
     return phi;
 }
 
-/* Hessian of phi with respect to b_0..b_2, from a row-normalised p. */
-static void dual_hessian(const double p[16], double H[3][3])
+/* The reduced Hessian as a graph Laplacian.  Because every row of p sums to
+ * one, p_ij (1 - p_ij) = p_ij sum_{l!=j} p_il, so
+ *   Hess_jk = -w_jk (j != k),   Hess_jj = sum_{l != j} w_jl,
+ *   w_jk = sum_i p_ij p_ik      (j, k = 0..3, j != k),
+ * i.e. Hess is the Laplacian of the complete graph on the four columns with
+ * edge weights w, restricted to columns 0..2 (column 3 is grounded by the
+ * gauge b_3 = 0).  Edge e joins columns EDGE[e][0] and EDGE[e][1]. */
+static const int EDGE[6][2] = {{0, 1}, {0, 2}, {0, 3}, {1, 2}, {1, 3}, {2, 3}};
+
+static void hessian_weights(const double p[16], double w[6])
 {
-    for (int j = 0; j < 3; ++j) {
-        for (int k = 0; k < 3; ++k) {
-            double h = 0.0;
-            for (int i = 0; i < 4; ++i) {
-                const double *pi = p + 4 * i;
-                if (j == k) {
-                    double rest = 0.0;
-                    for (int l = 0; l < 4; ++l)
-                        if (l != j) rest += pi[l];
-                    h += pi[j] * rest;
-                } else {
-                    h -= pi[j] * pi[k];
-                }
-            }
-            H[j][k] = h;
-        }
+    for (int e = 0; e < 6; ++e) {
+        int j = EDGE[e][0], k = EDGE[e][1];
+        double s = 0.0;
+        for (int i = 0; i < 4; ++i) s += p[4 * i + j] * p[4 * i + k];
+        w[e] = s;
     }
 }
 
-/* Solve H x = r for a symmetric positive definite 3x3 H: Jacobi scaling then
- * Cholesky.  Returns 0 on success, -1 if H is not numerically positive
- * definite. */
-static int spd3_solve(const double H[3][3], const double r[3], double x[3])
+/* Connected components of the graph on columns 0..3 with the edges in mask;
+ * comp[v] is a representative of v's component.  Returns the count. */
+static int edge_components(unsigned mask, int comp[4])
 {
-    double d[3];
-    for (int j = 0; j < 3; ++j) {
-        if (!(H[j][j] > 0.0)) return -1;
-        d[j] = 1.0 / sqrt(H[j][j]);
+    int par[4] = {0, 1, 2, 3};
+    for (int e = 0; e < 6; ++e) {
+        if (!(mask & (1u << e))) continue;
+        int a = EDGE[e][0], b = EDGE[e][1];
+        while (par[a] != a) a = par[a];
+        while (par[b] != b) b = par[b];
+        if (a != b) par[a] = b;
     }
-    double A[3][3];
-    for (int j = 0; j < 3; ++j)
-        for (int k = 0; k < 3; ++k) A[j][k] = d[j] * H[j][k] * d[k];
-    double L[3][3] = {{0}};
-    for (int j = 0; j < 3; ++j) {
-        double s = A[j][j];
-        for (int k = 0; k < j; ++k) s -= L[j][k] * L[j][k];
-        if (!(s > 0.0)) return -1;
-        L[j][j] = sqrt(s);
-        for (int i = j + 1; i < 3; ++i) {
-            double t = A[i][j];
-            for (int k = 0; k < j; ++k) t -= L[i][k] * L[j][k];
-            L[i][j] = t / L[j][j];
+    int n = 0;
+    for (int v = 0; v < 4; ++v) {
+        int a = v;
+        while (par[a] != a) a = par[a];
+        comp[v] = a;
+        if (a == v) ++n;
+    }
+    return n;
+}
+
+/* Solve Hess x = r through the matrix-tree theorem (the inverse of a grounded
+ * Laplacian in closed form):
+ *   det Hess       = sum over spanning trees T of the four columns of w(T),
+ *   (Hess^-1)_jk   = sum over spanning forests F with two trees, column 3 in
+ *                    one and columns j and k in the other, of w(F), / det,
+ * where w(.) is the product of the edge weights.  Every term is positive, so
+ * nothing cancels however small the weights are; the sums run in long double
+ * to keep products of tiny weights off the underflow threshold.  The four
+ * columns have 16 spanning trees and 15 two-tree forests (every pair of
+ * edges); which edge subsets they are, and which (j,k) each forest serves, is
+ * enumerated once by brute force over the 2^6 edge subsets.
+ * Returns -1 if the determinant is not positive (a zero weight pattern that
+ * disconnects the graph). */
+static struct {
+    int ntree, nforest;
+    unsigned tree[16];
+    unsigned forest[15];
+    unsigned char serves[15][3][3]; /* forest f contributes to (j,k) */
+} MT;
+
+static void matrix_tree_tables(void)
+{
+    int nt = 0, nf = 0;
+    for (unsigned mask = 0; mask < 64; ++mask) {
+        int ne = __builtin_popcount(mask);
+        if (ne != 2 && ne != 3) continue;
+        int comp[4];
+        int nc = edge_components(mask, comp);
+        if (ne == 3 && nc == 1) MT.tree[nt++] = mask;
+        if (ne == 2 && nc == 2) {
+            for (int j = 0; j < 3; ++j)
+                for (int k = 0; k < 3; ++k)
+                    MT.serves[nf][j][k] = (comp[j] == comp[k] && comp[j] != comp[3]);
+            MT.forest[nf++] = mask;
         }
     }
-    double y[3], z[3];
-    for (int j = 0; j < 3; ++j) {
-        double s = d[j] * r[j];
-        for (int k = 0; k < j; ++k) s -= L[j][k] * y[k];
-        y[j] = s / L[j][j];
+    MT.ntree = nt;
+    MT.nforest = nf;
+}
+
+static long double edge_product(const double w[6], unsigned mask)
+{
+    long double prod = 1.0L;
+    for (int e = 0; e < 6; ++e)
+        if (mask & (1u << e)) prod *= (long double)w[e];
+    return prod;
+}
+
+static int hessian_solve(const double w[6], const double r[3], double x[3])
+{
+    long double det = 0.0L, F[3][3] = {{0.0L}};
+    for (int t = 0; t < MT.ntree; ++t) det += edge_product(w, MT.tree[t]);
+    for (int f = 0; f < MT.nforest; ++f) {
+        long double prod = edge_product(w, MT.forest[f]);
+        for (int j = 0; j < 3; ++j)
+            for (int k = 0; k < 3; ++k)
+                if (MT.serves[f][j][k]) F[j][k] += prod;
     }
-    for (int j = 2; j >= 0; --j) {
-        double s = y[j];
-        for (int k = j + 1; k < 3; ++k) s -= L[k][j] * z[k];
-        z[j] = s / L[j][j];
-    }
-    for (int j = 0; j < 3; ++j) x[j] = d[j] * z[j];
+    if (!(det > 0.0L)) return -1;
+    for (int j = 0; j < 3; ++j)
+        x[j] = (double)((F[j][0] * r[0] + F[j][1] * r[1] + F[j][2] * r[2]) / det);
     return 0;
+}
+
+/* Batched form of hessian_solve for the tests: w [n,6] (edge order
+ * (0,1),(0,2),(0,3),(1,2),(1,3),(2,3)), r and x [n,3].  Returns the number of
+ * systems with a non-positive determinant (their x is NaN). */
+int64_t oracle_laplacian_solve64(const double *w, const double *r, double *x, int64_t n)
+{
+    int64_t bad = 0;
+    matrix_tree_tables();
+    for (int64_t t = 0; t < n; ++t) {
+        if (hessian_solve(w + 6 * t, r + 3 * t, x + 3 * t) != 0) {
+            x[3 * t] = x[3 * t + 1] = x[3 * t + 2] = NAN;
+            ++bad;
+        }
+    }
+    return bad;
 }
 
 static int newton_token(const double x[16], double pout[16], double bout[4], double tol,
@@ -306,9 +365,9 @@ static int newton_token(const double x[16], double pout[16], double bout[4], dou
         /* stalled in the rounding regime: more steps cannot help */
         if (since_best >= 8 && best_res < 1e-10) break;
 
-        double H[3][3], step[3];
-        dual_hessian(p, H);
-        if (spd3_solve(H, g, step) != 0) {
+        double w[6], step[3];
+        hessian_weights(p, w);
+        if (hessian_solve(w, g, step) != 0) {
             /* not numerically positive definite: fall back to a gradient step */
             for (int j = 0; j < 3; ++j) step[j] = g[j];
         }
@@ -363,6 +422,7 @@ int64_t oracle_newton64(const double *X, double *P, double *b, int64_t T, double
 {
     int64_t nonconv = 0;
     if (T <= 0) return 0;
+    matrix_tree_tables();
 #pragma omp parallel for schedule(dynamic, 64) reduction(+ : nonconv)
     for (int64_t t = 0; t < T; ++t) {
         int32_t it = 0;
@@ -381,39 +441,54 @@ int64_t oracle_newton64(const double *X, double *P, double *b, int64_t T, double
 /* F(X, b) = grad_b phi = colsum(p) - 1 = 0 (components 0..2, b_3 = 0).      */
 /* For a loss L with G = dL/dP:                                              */
 /*   dL/dX = dL/dX|_b  -  lambda^T dF/dX,   Hess lambda = dL/db|_X            */
-/* where, with r_k = sum_j G_kj p_kj,                                        */
-/*   dL/dX_kl |_b = p_kl (G_kl - r_k)                                         */
-/*   dL/db_l  |_X = sum_k p_kl (G_kl - r_k)                    (l = 0..2)    */
+/* where, with r_k = sum_j G_kj p_kj and D_kl = G_kl - r_k,                  */
+/*   dL/dX_kl |_b = p_kl D_kl                                                 */
+/*   dL/db_l  |_X = v_l = sum_k p_kl D_kl                       (l = 0..2)   */
 /*   dF_l/dX_kq   = p_kl (delta_lq - p_kq)                                    */
-/* Hess is the dual Hessian at P (the matrix of the last Newton step).       */
+/* so that  dX_kq = p_kq (D_kq - sum_l p_kl (lambda_q - lambda_l)),           */
+/* lambda_3 = 0.  Hess is the dual Hessian at P (the matrix of the last      */
+/* Newton step), solved in closed form by hessian_solve.                     */
+/*                                                                           */
+/* P is first rescaled to unit row sums (P from the forward pass has them up */
+/* to rounding; storing P in a narrower type perturbs them).  With unit row  */
+/* sums two identities hold exactly and are used to avoid cancellation when  */
+/* a row of P is close to one-hot:                                           */
+/*   D_kl = sum_j p_kj (G_kl - G_kj),                                         */
+/*   lambda_q - sum_l p_kl lambda_l = sum_l p_kl (lambda_q - lambda_l).       */
 /* ------------------------------------------------------------------------ */
-static void backward_token(const double p[16], const double G[16], double dX[16])
+static void backward_token(const double pin[16], const double G[16], double dX[16])
 {
-    double direct[16], r[4];
+    double p[16], D[16];
     for (int k = 0; k < 4; ++k) {
-        r[k] = 0.0;
-        for (int j = 0; j < 4; ++j) r[k] += G[4 * k + j] * p[4 * k + j];
-        for (int j = 0; j < 4; ++j) direct[4 * k + j] = p[4 * k + j] * (G[4 * k + j] - r[k]);
+        double s = pin[4 * k] + pin[4 * k + 1] + pin[4 * k + 2] + pin[4 * k + 3];
+        for (int j = 0; j < 4; ++j) p[4 * k + j] = pin[4 * k + j] / s;
     }
-    double v[3];
-    for (int l = 0; l < 3; ++l) v[l] = direct[l] + direct[4 + l] + direct[8 + l] + direct[12 + l];
-    double H[3][3], lam[3] = {0, 0, 0};
-    dual_hessian(p, H);
-    if (spd3_solve(H, v, lam) != 0) lam[0] = lam[1] = lam[2] = NAN;
-    for (int k = 0; k < 4; ++k) {
-        double s = 0.0; /* sum_l lambda_l p_kl */
-        for (int l = 0; l < 3; ++l) s += lam[l] * p[4 * k + l];
-        for (int q = 0; q < 4; ++q) {
-            double dF = -s * p[4 * k + q];
-            if (q < 3) dF += lam[q] * p[4 * k + q];
-            dX[4 * k + q] = direct[4 * k + q] - dF;
+    for (int k = 0; k < 4; ++k)
+        for (int l = 0; l < 4; ++l) {
+            double d = 0.0;
+            for (int j = 0; j < 4; ++j)
+                if (j != l) d += p[4 * k + j] * (G[4 * k + l] - G[4 * k + j]);
+            D[4 * k + l] = d;
         }
-    }
+    double v[3];
+    for (int l = 0; l < 3; ++l)
+        v[l] = p[l] * D[l] + p[4 + l] * D[4 + l] + p[8 + l] * D[8 + l] + p[12 + l] * D[12 + l];
+    double w[6], lam[4] = {0, 0, 0, 0};
+    hessian_weights(p, w);
+    if (hessian_solve(w, v, lam) != 0) lam[0] = lam[1] = lam[2] = NAN;
+    for (int k = 0; k < 4; ++k)
+        for (int q = 0; q < 4; ++q) {
+            double c = 0.0;
+            for (int l = 0; l < 4; ++l)
+                if (l != q) c += p[4 * k + l] * (lam[q] - lam[l]);
+            dX[4 * k + q] = p[4 * k + q] * (D[4 * k + q] - c);
+        }
 }
 
 void oracle_backward64(const double *P, const double *G, double *dX, int64_t T)
 {
     if (T <= 0) return;
+    matrix_tree_tables();
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) backward_token(P + 16 * t, G + 16 * t, dX + 16 * t);
 }

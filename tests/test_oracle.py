@@ -209,23 +209,62 @@ def test_backward_matches_unrolled_sinkhorn_autodiff():
     assert np.abs(dXu - dX).max() <= 1e-11
 
 
-def test_backward_structure():
+@pytest.mark.parametrize("name,tol", [("n01", 1e-12), ("large_magnitude", 1e-7)])
+def test_backward_structure(name, tol):
+    """tol: float64 rounding amplified by the conditioning of the dual Hessian.
+    On nearly one-hot tokens of the large-magnitude family the dual potentials
+    reach ~1e8, so solving for them in float64 leaves residuals ~1e-8 (the
+    60-digit comparison below bounds the same effect)."""
     r = rng(13)
-    X = np.concatenate([r.standard_normal((500, 4, 4)), large_mag(500, 2)])
+    X = r.standard_normal((1000, 4, 4)) if name == "n01" else large_mag(1000, 2)
     G = r.standard_normal(X.shape)
     P = oracle.newton64(X)[0]
     dX = oracle.backward64(P, G)
     g = np.abs(G).max()
     # the projection is invariant to row/column offsets of X: dX has zero
     # row and column sums
-    assert np.abs(dX.sum(axis=1)).max() <= 1e-12 * g
-    assert np.abs(dX.sum(axis=2)).max() <= 1e-12 * g
+    assert np.abs(dX.sum(axis=1)).max() <= tol * g
+    assert np.abs(dX.sum(axis=2)).max() <= tol * g
     # and an upstream gradient of the form u_i + v_j changes nothing (the
     # marginals are fixed), so dX = 0
     U = r.standard_normal((len(X), 4, 1)) + r.standard_normal((len(X), 1, 4))
-    assert np.abs(oracle.backward64(P, U)).max() <= 1e-12
+    assert np.abs(oracle.backward64(P, U)).max() <= tol * 100
     # the Jacobian is positive semidefinite (Hessian of a convex function)
-    assert (np.einsum("tij,tij->t", G, dX) >= -1e-12).all()
+    assert (np.einsum("tij,tij->t", G, dX) >= -tol).all()
+
+
+def test_backward_against_60_digit_arithmetic():
+    """The float64 backward against the same formula evaluated with 60
+    significant digits (mpmath), on the same P rescaled to unit row sums."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 60
+
+    def exact(P, G):
+        p = [[mpmath.mpf(float(v)) for v in row] for row in P]
+        p = [[v / sum(row) for v in row] for row in p]
+        g = [[mpmath.mpf(float(v)) for v in row] for row in G]
+        r = [sum(p[k][j] * g[k][j] for j in range(4)) for k in range(4)]
+        v = [sum(p[k][l] * (g[k][l] - r[k]) for k in range(4)) for l in range(3)]
+        H = mpmath.matrix(3, 3)
+        for j in range(3):
+            for k in range(3):
+                H[j, k] = (sum(p[i][j] * (1 - p[i][j]) for i in range(4)) if j == k
+                           else -sum(p[i][j] * p[i][k] for i in range(4)))
+        lam = list(mpmath.lu_solve(H, mpmath.matrix(v))) + [mpmath.mpf(0)]
+        out = np.zeros((4, 4))
+        for k in range(4):
+            s = sum(lam[l] * p[k][l] for l in range(4))
+            for q in range(4):
+                out[k, q] = float(p[k][q] * (g[k][q] - r[k] - lam[q] + s))
+        return out
+
+    r = rng(19)
+    for X, tol in ((r.standard_normal((60, 4, 4)), 1e-14), (large_mag(200, 2), 1e-8)):
+        G = r.standard_normal(X.shape)
+        P = oracle.newton64(X)[0]
+        dX = oracle.backward64(P, G)
+        err = max(np.abs(exact(P[t], G[t]) - dX[t]).max() for t in range(len(X)))
+        assert err <= tol
 
 
 def test_backward_is_symmetric_jacobian():
