@@ -1,0 +1,152 @@
+"""GB300-native per-token 4x4 Birkhoff projection (mHC, expansion rate n = 4).
+
+Each token's logit matrix X is mapped to the doubly stochastic
+P = diag(e^a) exp(X) diag(e^b) by Newton's method on the 3-variable reduced
+dual, and the backward pass maps dP to dX by implicit differentiation
+("Accelerating the Birkhoff Projection for Manifold-Constrained
+Hyper-Connections", s2.1-s2.3).  Every step runs in the sm_103a kernels of
+libbirkhoff4.so (C ABI: include/birkhoff4.h); this module only marshals
+torch CUDA tensors and the current stream into those calls.
+
+    P = project(X)              # autograd: backward uses the implicit formula
+    P, b = forward(X, return_dual=True)
+    dX = backward(dP, P=P)      # or backward(dP, X=X): P recomputed, not stored
+    P, dX = forward_backward(X, dP)
+    P20 = sinkhorn(X, iters=20) # fixed-iteration Sinkhorn-Knopp reference
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import B4_BF16, B4_F32, Birkhoff4Error, Opts, check, lib
+
+__all__ = ["project", "forward", "backward", "forward_backward", "sinkhorn", "Birkhoff4Error",
+           "lib", "Projection"]
+
+_DT = {torch.float32: B4_F32, torch.bfloat16: B4_BF16}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_tokens(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype not in _DT:
+        raise TypeError("%s must be float32 or bfloat16, got %s" % (name, t.dtype))
+    if t.dim() < 2 or tuple(t.shape[-2:]) != (4, 4):
+        raise ValueError("%s must have shape [..., 4, 4], got %s" % (name, tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.numel() // 16
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def forward(X: torch.Tensor, *, out: torch.Tensor = None, out_dtype=None, return_dual: bool = False,
+            tol: float = 0.0, max_evals: int = 0, return_stats: bool = False):
+    """Projection of every token of X ([..., 4, 4], fp32 or bf16).
+
+    Returns P (dtype out_dtype, default X.dtype), plus b ([..., 4] fp32,
+    natural-log column dual, b[..., 3] = 0) if return_dual, plus
+    (evals [...] int32, nonconverged count) if return_stats."""
+    T = _check_tokens(X, "X")
+    odt = out_dtype or X.dtype
+    if out is None:
+        out = torch.empty(X.shape, dtype=odt, device=X.device)
+    else:
+        _check_tokens(out, "out")
+        if out.shape != X.shape or out.dtype != odt or out.device != X.device:
+            raise ValueError("out does not match X")
+    b = torch.empty(X.shape[:-1], dtype=torch.float32, device=X.device) if return_dual else None
+    opts = Opts(in_dtype=_DT[X.dtype], out_dtype=_DT[odt], max_evals=int(max_evals), tol=float(tol))
+    evals = nonconv = None
+    if return_stats:
+        evals = torch.empty(X.shape[:-2], dtype=torch.int32, device=X.device)
+        nonconv = torch.zeros(1, dtype=torch.int64, device=X.device)
+        opts.evals_out = evals.data_ptr()
+        opts.nonconv_count = nonconv.data_ptr()
+    with torch.cuda.device(X.device):
+        check(lib().birkhoff4_forward_ex(_ptr(X), _ptr(out), _ptr(b), T, ctypes.byref(opts),
+                                         _stream(X)), "birkhoff4_forward_ex")
+    res = (out,)
+    if return_dual:
+        res += (b,)
+    if return_stats:
+        res += (evals, nonconv)
+    return res[0] if len(res) == 1 else res
+
+
+def backward(dP: torch.Tensor, *, P: torch.Tensor = None, X: torch.Tensor = None,
+             out: torch.Tensor = None) -> torch.Tensor:
+    """dX = (dP/dX)^T dP by implicit differentiation, from the stored P or,
+    if P is None, from X (P recomputed inside the kernel)."""
+    T = _check_tokens(dP, "dP")
+    src = P if P is not None else X
+    if src is None:
+        raise ValueError("backward needs P or X")
+    _check_tokens(src, "P" if P is not None else "X")
+    if src.shape != dP.shape or src.dtype != dP.dtype or src.device != dP.device:
+        raise ValueError("P/X and dP must match in shape, dtype and device")
+    if out is None:
+        out = torch.empty_like(dP)
+    fn = lib().birkhoff4_backward if dP.dtype == torch.float32 else lib().birkhoff4_backward_bf16
+    with torch.cuda.device(dP.device):
+        check(fn(_ptr(X), _ptr(P), _ptr(dP), _ptr(out), T, _stream(dP)), "birkhoff4_backward")
+    return out
+
+
+def forward_backward(X: torch.Tensor, dP: torch.Tensor, *, want_P: bool = True):
+    """One fused pass: (P, dX) (P is None if not wanted)."""
+    T = _check_tokens(X, "X")
+    _check_tokens(dP, "dP")
+    if X.shape != dP.shape or X.dtype != dP.dtype or X.device != dP.device:
+        raise ValueError("X and dP must match in shape, dtype and device")
+    P = torch.empty_like(X) if want_P else None
+    dX = torch.empty_like(dP)
+    fn = (lib().birkhoff4_forward_backward if X.dtype == torch.float32
+          else lib().birkhoff4_forward_backward_bf16)
+    with torch.cuda.device(X.device):
+        check(fn(_ptr(X), _ptr(dP), _ptr(P), _ptr(dX), T, _stream(X)), "birkhoff4_forward_backward")
+    return P, dX
+
+
+def sinkhorn(X: torch.Tensor, iters: int = 20, *, out: torch.Tensor = None) -> torch.Tensor:
+    """Fixed-iteration log-domain Sinkhorn-Knopp (the reference scheme)."""
+    T = _check_tokens(X, "X")
+    if out is None:
+        out = torch.empty_like(X)
+    fn = lib().birkhoff4_sinkhorn if X.dtype == torch.float32 else lib().birkhoff4_sinkhorn_bf16
+    with torch.cuda.device(X.device):
+        check(fn(_ptr(X), _ptr(out), int(iters), T, _stream(X)), "birkhoff4_sinkhorn")
+    return out
+
+
+class Projection(torch.autograd.Function):
+    """P = project(X); the backward is the implicit-differentiation kernel
+    applied to the saved P (nothing of the forward iteration is stored)."""
+
+    @staticmethod
+    def forward(ctx, X):
+        Xc = X.contiguous()
+        P = forward(Xc)
+        ctx.save_for_backward(P)
+        return P
+
+    @staticmethod
+    def backward(ctx, dP):
+        (P,) = ctx.saved_tensors
+        return backward(dP.contiguous().to(P.dtype), P=P)
+
+
+def project(X: torch.Tensor) -> torch.Tensor:
+    """Differentiable per-token Birkhoff projection of X [..., 4, 4]."""
+    return Projection.apply(X)

@@ -1,0 +1,149 @@
+// b4_launch.cuh -- host-side launch of the token-stream kernels: TMA tensor
+// maps, tile configuration per pass, persistent grid sizing, chunking of very
+// long token arrays.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "b4_kernels.cuh"
+
+namespace b4 {
+
+// Tile shape per pass: tokens per CTA step, input stages, output stages.
+template <Mode M, class TIn>
+struct TileCfg {
+  static constexpr int TILE = 128;
+  static constexpr int NSTAGE = 3;
+  static constexpr int NOSTAGE = 2;
+};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a [T, 16] row array (one token per row), box [16, tile].
+template <class T>
+inline bool encode_rows(CUtensorMap* map, const void* ptr, int64_t ntok, int tile) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {16, static_cast<cuuint64_t>(ntok)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(TileIO<T>::ROW_BYTES)};
+  const cuuint32_t box[2] = {16, static_cast<cuuint32_t>(tile)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, TileIO<T>::TMA_TYPE, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, TileIO<T>::TMA_SWIZZLE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int sm_count(int dev) {
+  static std::atomic<int> cache[64];
+  if (dev < 0 || dev >= 64) return 0;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kChunkTokens = int64_t(1) << 30;  // TMA row coordinates stay in int32
+
+template <class T>
+inline const void* advance(const void* p, int64_t tokens) {
+  return p == nullptr ? nullptr
+                      : static_cast<const void*>(static_cast<const unsigned char*>(p) +
+                                                 tokens * TileIO<T>::ROW_BYTES);
+}
+template <class T>
+inline void* advance(void* p, int64_t tokens) {
+  return p == nullptr ? nullptr : static_cast<void*>(static_cast<unsigned char*>(p) + tokens * TileIO<T>::ROW_BYTES);
+}
+
+// Enqueue one pass over la.T tokens on `stream`.  Returns the CUDA error of
+// the preparation or launch (cudaSuccess if everything was enqueued).
+template <Mode M, class TIn, class TOut>
+cudaError_t launch(const LaunchArgs& la, cudaStream_t stream) {
+  constexpr int NIN = ModeTraits<M>::NIN;
+  constexpr int NOUT = ModeTraits<M>::NOUT;
+  using C = TileCfg<M, TIn>;
+  using S = StreamShape<M, TIn, TOut, C::TILE, C::NSTAGE, C::NOSTAGE>;
+
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const int nsm = sm_count(dev);
+  if (nsm <= 0) return cudaErrorInvalidDevice;
+
+  bool aligned = true;
+  for (int k = 0; k < NIN; ++k) aligned = aligned && aligned16(la.in[k]);
+  for (int k = 0; k < NOUT; ++k) aligned = aligned && aligned16(la.out[k]);
+
+  auto kern = stream_kernel<M, TIn, TOut, C::TILE, C::NSTAGE, C::NOSTAGE>;
+  int grid_cap = 0;
+  if (aligned) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    int occ = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::TILE, S::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    grid_cap = nsm * std::max(occ, 1);
+  }
+
+  for (int64_t done = 0; done < la.T; done += kChunkTokens) {
+    const int64_t n = std::min(la.T - done, kChunkTokens);
+    KParams p;
+    memset(&p, 0, sizeof(p));
+    for (int k = 0; k < NIN; ++k) p.gin[k] = advance<TIn>(la.in[k], done);
+    for (int k = 0; k < NOUT; ++k) p.gout[k] = advance<TOut>(la.out[k], done);
+    p.b = la.b ? la.b + 4 * done : nullptr;
+    p.b_vec = aligned16(la.b) ? 1 : 0;
+    p.evals_out = la.evals_out ? la.evals_out + done : nullptr;
+    p.nonconv = la.nonconv;
+    p.fault = la.fault;
+    p.T = n;
+    p.cfg = la.cfg;
+    p.iters = la.iters;
+    bool use_tma = aligned;
+    if (use_tma) {
+      for (int k = 0; k < NIN && use_tma; ++k) use_tma = encode_rows<TIn>(&p.in[k], p.gin[k], n, C::TILE);
+      for (int k = 0; k < NOUT && use_tma; ++k) use_tma = encode_rows<TOut>(&p.out[k], p.gout[k], n, C::TILE);
+    }
+    if (use_tma) {
+      p.ntiles = static_cast<int32_t>((n + C::TILE - 1) / C::TILE);
+      const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, grid_cap));
+      kern<<<grid, C::TILE, S::SMEM_BYTES, stream>>>(p);
+    } else {
+      const int64_t blocks = (n + 255) / 256;
+      const int grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(nsm) * 8));
+      plain_kernel<M, TIn, TOut><<<grid, 256, 0, stream>>>(p);
+    }
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace b4

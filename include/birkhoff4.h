@@ -1,0 +1,193 @@
+/*
+ * birkhoff4.h -- C ABI of libbirkhoff4.so: the per-token 4x4 Birkhoff
+ * projection on one NVIDIA GB300 (sm_103a).
+ *
+ * Source: "Accelerating the Birkhoff Projection for Manifold-Constrained
+ * Hyper-Connections" (technical summary of arXiv 2606.07574; Spanish and
+ * French renderings), cited below as [mHC sN]:
+ *   s1    mHC projects each token's residual mixing matrix onto the Birkhoff
+ *         polytope; current practice is Sinkhorn-Knopp with a small fixed
+ *         iteration count (e.g. 20);
+ *   s2    the projection is entropic optimal transport;
+ *   s2.1  forward: Newton's method on the dual reduced to m-1 = 3 free
+ *         variables, closed-form gradient and Hessian, rows shifted by their
+ *         maximum before the softmax;
+ *   s2.2  backward: implicit differentiation, the last Newton Hessian being
+ *         the matrix of the linear system;
+ *   s2.3  one kernel processes many 4x4 matrices in a batch.
+ *
+ * The operation.  A token is a logit matrix X in R^{4x4}.  Its projection is
+ *   P = diag(e^a) exp(X) diag(e^b),   P 1 = 1,  P^T 1 = 1,
+ * the unique doubly stochastic matrix of that form (entropic OT with
+ * epsilon = 1 and unit marginals).  b is the column dual in natural-log
+ * units, gauge b[3] = 0.  The backward pass maps an upstream gradient
+ * G = dL/dP to dX = (dP/dX)^T G.
+ *
+ * Layout.  X, P, dP (= G) and dX are contiguous row-major [T,4,4] arrays in
+ * device memory: element (t,i,j) at offset 16*t + 4*i + j (i = row,
+ * j = column).  b is [T,4] float32, b[t][3] = 0.  fp32 arrays hold float;
+ * bf16 arrays hold bfloat16 bit patterns (uint16_t).  All arithmetic is fp32;
+ * bf16 inputs are widened exactly and bf16 outputs are rounded to nearest
+ * even.
+ *
+ * Ownership and execution.  Every pointer is caller-owned device memory; the
+ * library allocates nothing.  Work is enqueued on `stream` and runs
+ * asynchronously; the caller synchronises.  Calls on different streams or
+ * host threads are independent.  In-place use is allowed where noted: each
+ * token is read completely before any of it is written.
+ *
+ * Errors.  Every entry point returns 0 (B4_OK) or a positive code:
+ *   B4_EINVAL   a NULL pointer with T > 0, T < 0, a bad option, iters < 0;
+ *   B4_ECUDA    a CUDA error while preparing or launching (no kernel ran, or
+ *               the launch failed); birkhoff4_last_cuda_error() returns the
+ *               cudaError_t value (the library links its own CUDA runtime,
+ *               so the caller's cudaGetLastError does not see it);
+ *   B4_ENOTIMPL not available in this build.
+ * T = 0 returns B4_OK and launches nothing.  Arguments are checked on the
+ * host before any CUDA call.  A base address that is not 16-byte aligned is
+ * not an error: it selects a slower kernel with plain loads.  Kernels never
+ * trap.  A token whose X holds a NaN or an infinity gets an all-NaN P (and
+ * NaN b); other tokens are unaffected.  Not reaching the tolerance within the
+ * iteration cap is not an error: P is the last iterate, and the _ex variant
+ * can count such tokens.
+ */
+#ifndef BIRKHOFF4_H
+#define BIRKHOFF4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BIRKHOFF4_VERSION 1
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *birkhoff4_stream_t;
+
+enum birkhoff4_status {
+    B4_OK = 0,
+    B4_EINVAL = 1,
+    B4_ECUDA = 2,
+    B4_ENOTIMPL = 3
+};
+
+enum birkhoff4_dtype {
+    B4_F32 = 0,
+    B4_BF16 = 1
+};
+
+/* Options of birkhoff4_forward_ex.  Zero-initialise, then set fields. */
+typedef struct birkhoff4_opts {
+    int32_t in_dtype;   /* B4_F32 or B4_BF16 (X) */
+    int32_t out_dtype;  /* B4_F32 or B4_BF16 (P) */
+    int32_t max_evals;  /* cap on evaluations of P per token, 1..1024; 0 = 48 */
+    float tol;          /* stop at max_j |colsum_j(P) - 1| <= tol; 0 = 1e-6 */
+    int32_t *evals_out; /* NULL or device [T]: evaluations used per token */
+    unsigned long long *nonconv_count; /* NULL or device counter: += tokens
+                                          that stopped above tol */
+} birkhoff4_opts;
+
+/* ---------------------------------------------------------------------- */
+/* Forward [mHC s2.1]: X -> P (and optionally b).                          */
+/*                                                                        */
+/* Per token: b starts from the column-mean estimate                       */
+/* b_j = -(mean_i X_ij - mean_i X_i3); each evaluation forms the row       */
+/* softmax of X + b (first in the log domain with every row shifted by its */
+/* maximum, then by multiplicative updates of the previous P, refreshed in */
+/* the log domain every 8 evaluations); the gradient is colsum(P) - 1 and  */
+/* the Hessian sum_i diag(p_i) - p_i p_i^T restricted to columns 0..2; the */
+/* 3x3 Newton system is solved by Laplacian elimination; the step is       */
+/* damped by 1/(1+lambda) when the Newton decrement lambda exceeds 1 and   */
+/* clamped to 4 in the max norm.  The loop stops when the residual         */
+/* max_j |colsum_j - 1| <= tol (1e-6), when it stagnates below 64*tol, or  */
+/* after max_evals (48) evaluations.  P is the last evaluation (unit row   */
+/* sums up to rounding).                                                   */
+/*                                                                        */
+/* X: [T,4,4] (read).  P: [T,4,4] (written; may equal X).  b: NULL or      */
+/* [T,4] float32 (written).                                               */
+/* ---------------------------------------------------------------------- */
+int birkhoff4_forward(const float *X, float *P, float *b, int64_t T, birkhoff4_stream_t stream);
+int birkhoff4_forward_bf16(const uint16_t *X, uint16_t *P, float *b, int64_t T,
+                           birkhoff4_stream_t stream);
+/* Any dtype pair (e.g. bf16 X -> fp32 P), tolerance, cap and statistics. */
+int birkhoff4_forward_ex(const void *X, void *P, float *b, int64_t T, const birkhoff4_opts *opts,
+                         birkhoff4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Backward [mHC s2.2]: (P, G) -> dX = (dP/dX)^T G, nothing unrolled.      */
+/*                                                                        */
+/* With D_kl = G_kl - sum_j p_kj G_kj, v_l = sum_k p_kl D_kl and lambda    */
+/* the solution of H lambda = v (H = the dual Hessian at P, the matrix of  */
+/* the last Newton step, lambda_3 = 0):                                    */
+/*   dX_kq = p_kq (D_kq - sum_l p_kl (lambda_q - lambda_l)).               */
+/* P is first rescaled to unit row sums (a bf16 P is off by up to 2^-8).   */
+/* H is regularised by adding 1e-7 * max_e w_e to its edge weights w_e     */
+/* (a relative change of 1e-7 on well-conditioned tokens; it bounds the    */
+/* amplification of rounding on nearly one-hot P).                         */
+/*                                                                        */
+/* X: [T,4,4] or NULL; read only when P is NULL, in which case P is        */
+/* recomputed from X by the forward iteration (nothing stored between the  */
+/* passes).  P: [T,4,4] from birkhoff4_forward, or NULL.  dP: [T,4,4].     */
+/* dX: [T,4,4] (written; may equal dP or P).                               */
+/* ---------------------------------------------------------------------- */
+int birkhoff4_backward(const float *X, const float *P, const float *dP, float *dX, int64_t T,
+                       birkhoff4_stream_t stream);
+int birkhoff4_backward_bf16(const uint16_t *X, const uint16_t *P, const uint16_t *dP,
+                            uint16_t *dX, int64_t T, birkhoff4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Fused forward + backward [mHC s2.1, s2.2]: one pass reads X and dP and  */
+/* writes P (if non-NULL) and dX, with the backward using the fp32 P held  */
+/* in registers (the Hessian of the last Newton step reused directly).     */
+/* ---------------------------------------------------------------------- */
+int birkhoff4_forward_backward(const float *X, const float *dP, float *P, float *dX, int64_t T,
+                               birkhoff4_stream_t stream);
+int birkhoff4_forward_backward_bf16(const uint16_t *X, const uint16_t *dP, uint16_t *P,
+                                    uint16_t *dX, int64_t T, birkhoff4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Reference: fixed-iteration Sinkhorn-Knopp [mHC s1], the scheme current  */
+/* mHC uses (e.g. iters = 20), kept for the accuracy comparison.           */
+/* Log domain, b = 0 start; one iteration is a row normalisation           */
+/* a_i = -LSE_j(X_ij + b_j) followed by a column normalisation             */
+/* b_j = -LSE_i(X_ij + a_i); P = exp(X + a 1^T + 1 b^T) after the last     */
+/* iteration (iters = 0 gives exp(X)).                                     */
+/* X: [T,4,4] (read).  P: [T,4,4] (written; may equal X).  iters >= 0.     */
+/* ---------------------------------------------------------------------- */
+int birkhoff4_sinkhorn(const float *X, float *P, int iters, int64_t T, birkhoff4_stream_t stream);
+int birkhoff4_sinkhorn_bf16(const uint16_t *X, uint16_t *P, int iters, int64_t T,
+                            birkhoff4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Diagnostics.                                                           */
+/* ---------------------------------------------------------------------- */
+/* Message for a status code (static string, never NULL). */
+const char *birkhoff4_strerror(int code);
+/* BIRKHOFF4_VERSION of the loaded library. */
+int birkhoff4_version(void);
+/* cudaError_t value behind the last B4_ECUDA returned on this host thread
+ * (0 if none). */
+int birkhoff4_last_cuda_error(void);
+/* Device-side fault latch of the current device.  Kernels wait on their   */
+/* own TMA transfers with a time limit (2 s); a wait that runs out sets    */
+/* bit 0, the kernel drains what it issued and returns early (its tile     */
+/* outputs are then incomplete).  Synchronises the device; writes the      */
+/* latch to *out and clears it if `clear` is non-zero.                     */
+int birkhoff4_device_status(unsigned int *out, int clear);
+/* Self-test of that time limit: one CTA waits on a barrier nothing        */
+/* completes, for limit_ns nanoseconds (1..10^9), then records bit 1 in    */
+/* the latch and returns.  Synchronous.  Faults nothing.                   */
+int birkhoff4_selftest_wait_timeout(int64_t limit_ns);
+/* Microbenchmark of the ex2 (MUFU) rate: n_blocks CTAs of 256 threads run */
+/* `iters` dependent-chain-free ex2.approx per thread; out[0] receives the */
+/* elapsed device time in ms (measured with events on `stream`), out[1]    */
+/* the number of ex2 executed.  Synchronous.                               */
+int birkhoff4_mufu_probe(float *out_host, int n_blocks, int iters, birkhoff4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BIRKHOFF4_H */

@@ -1,0 +1,129 @@
+"""The C ABI boundary on the host (no GPU needed).
+
+libbirkhoff4.so must load, export every function include/birkhoff4.h
+declares, and reject invalid arguments on the host before any CUDA call
+(these checks never touch a device, so they run on a CPU-only machine).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from birkhoff_projection_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "birkhoff4.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(birkhoff4_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    return _lib.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+    # and the binding covers exactly the header
+    assert set(names) == set(_lib.SIGNATURES)
+
+
+def test_version_and_strerror(L):
+    assert L.birkhoff4_version() == 1
+    for code in (0, 1, 2, 3, 99):
+        s = L.birkhoff4_strerror(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert b"invalid" in L.birkhoff4_strerror(_lib.B4_EINVAL)
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: rejected before use
+
+
+def test_negative_T_is_einval(L):
+    assert L.birkhoff4_forward(FAKE, FAKE, None, -1, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_forward_bf16(FAKE, FAKE, None, -5, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_backward(None, FAKE, FAKE, FAKE, -1, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_forward_backward(FAKE, FAKE, FAKE, FAKE, -1, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_sinkhorn(FAKE, FAKE, 20, -1, None) == _lib.B4_EINVAL
+
+
+def test_null_pointers_are_einval(L):
+    assert L.birkhoff4_forward(None, FAKE, None, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_forward(FAKE, None, None, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_backward(None, None, FAKE, FAKE, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_backward(None, FAKE, None, FAKE, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_backward(None, FAKE, FAKE, None, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_backward_bf16(None, None, FAKE, FAKE, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_forward_backward(None, FAKE, FAKE, FAKE, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_forward_backward(FAKE, None, FAKE, FAKE, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_forward_backward_bf16(FAKE, FAKE, FAKE, None, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_sinkhorn(None, FAKE, 20, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_sinkhorn_bf16(FAKE, None, 20, 4, None) == _lib.B4_EINVAL
+
+
+def test_bad_options_are_einval(L):
+    def opts(**kw):
+        o = _lib.Opts(in_dtype=0, out_dtype=0, max_evals=0, tol=0.0)
+        for k, v in kw.items():
+            setattr(o, k, v)
+        return ctypes.byref(o)
+
+    f = L.birkhoff4_forward_ex
+    assert f(FAKE, FAKE, None, 4, None, None) == _lib.B4_EINVAL  # NULL options
+    assert f(FAKE, FAKE, None, 4, opts(in_dtype=2), None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, None, 4, opts(out_dtype=-1), None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, None, 4, opts(max_evals=-1), None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, None, 4, opts(max_evals=1025), None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, None, 4, opts(tol=-1.0), None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, None, 4, opts(tol=float("nan")), None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, None, 4, opts(tol=float("inf")), None) == _lib.B4_EINVAL
+
+
+def test_negative_iters_is_einval(L):
+    assert L.birkhoff4_sinkhorn(FAKE, FAKE, -1, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_sinkhorn_bf16(FAKE, FAKE, -3, 4, None) == _lib.B4_EINVAL
+
+
+def test_empty_batch_is_a_no_op(L):
+    # T = 0 returns before any CUDA call, even with NULL pointers
+    assert L.birkhoff4_forward(None, None, None, 0, None) == _lib.B4_OK
+    assert L.birkhoff4_forward_bf16(None, None, None, 0, None) == _lib.B4_OK
+    assert L.birkhoff4_backward(None, None, None, None, 0, None) == _lib.B4_OK
+    assert L.birkhoff4_backward_bf16(None, None, None, None, 0, None) == _lib.B4_OK
+    assert L.birkhoff4_forward_backward(None, None, None, None, 0, None) == _lib.B4_OK
+    assert L.birkhoff4_sinkhorn(None, None, 20, 0, None) == _lib.B4_OK
+    o = _lib.Opts(in_dtype=1, out_dtype=0, max_evals=0, tol=0.0)
+    assert L.birkhoff4_forward_ex(None, None, None, 0, ctypes.byref(o), None) == _lib.B4_OK
+
+
+def test_diagnostic_argument_checks(L):
+    assert L.birkhoff4_device_status(None, 0) == _lib.B4_EINVAL
+    assert L.birkhoff4_selftest_wait_timeout(0) == _lib.B4_EINVAL
+    assert L.birkhoff4_selftest_wait_timeout(2_000_000_000) == _lib.B4_EINVAL
+    out = (ctypes.c_float * 2)()
+    assert L.birkhoff4_mufu_probe(None, 1, 1, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_mufu_probe(out, 0, 1, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_mufu_probe(out, 1, 0, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_last_cuda_error() == 0
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+
+    import birkhoff_projection_gb300 as b4
+
+    x = torch.zeros(3, 4, 4)
+    with pytest.raises(ValueError):
+        b4.forward(x)
+    with pytest.raises(ValueError):
+        b4.backward(x, P=x)
+    with pytest.raises(ValueError):
+        b4.sinkhorn(x)
