@@ -1,0 +1,379 @@
+"""Throughput of the per-token 4x4 Birkhoff projection on GB300.
+
+One step = one forward pass (X -> P, Newton on the reduced dual) followed by
+one backward pass (P, dP -> dX, implicit differentiation) over T = 2^26
+tokens of X ~ N(0,1) fp32 (the throughput-sweep workload at its largest
+size), inputs resident in HBM.  Every tensor is 4.3 GB, far larger than the
+129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  With --gpus N > 1 (launched by torchrun) each
+rank projects its own 2^26 tokens (weak scaling, no collective on the data
+path); the reported time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "4×4 Birkhoff proj tokens/s fwd & fwd+bwd at 2^26 tokens; % of roofline"
+LOG2_T = 26
+SIGMA = 1.0
+BYTES_FWD_F32 = 128  # X read + P written per token
+BYTES_BWD_F32 = 192  # P, dP read + dX written per token
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["b4_device.cuh", "b4_math.cuh", "b4_kernels.cuh", "b4_launch.cuh", "b4_types.h",
+                  "k_forward.cu", "k_backward.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "birkhoff_projection_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_PATH) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """Per-token DRAM bytes of each kernel from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    try:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
+        return None
+    out, src = {}, None
+    for ln in lines:
+        parts = ln.split()
+        if len(parts) >= 2 and parts[0] == "kernel_source_hash":
+            src = parts[1]
+        if len(parts) >= 3 and parts[0] == "dram_bytes_per_token":
+            out[parts[1]] = float(parts[2])
+    if src != kernel_source_hash():
+        return None
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        self.out = self.proc.stdout.read()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=5)
+
+    def summary(self):
+        rows = []
+        for ln in self.out.strip().splitlines():
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                rows.append((float(p[0]), float(p[1]), p[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def cpu_baseline(X_host, G_host, target_s: float = 12.0):
+    """The float64 oracle (Newton forward + implicit backward) on the host
+    cores, on a bounded prefix of the same tokens."""
+    import oracle
+
+    oracle.build()
+    n = 1 << 16
+    t0 = time.perf_counter()
+    P = oracle.project64(X_host[:n])
+    oracle.backward64(P, G_host[:n])
+    dt = time.perf_counter() - t0
+    n = int(min(X_host.shape[0], max(n, n * target_s / max(dt, 1e-3))))
+    t0 = time.perf_counter()
+    P = oracle.project64(X_host[:n])
+    oracle.backward64(P, G_host[:n])
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "first %d tokens of the workload, float64 Newton forward + implicit "
+                      "backward, %.1f s" % (n, dt)}
+
+
+def run_reference(args):
+    """The reference arm: the float64 oracle as it stands, on host cores."""
+    import numpy as np
+
+    import oracle
+    from birkhoff_projection_gb300 import workloads
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    oracle.build()
+    n = 1 << 18  # tokens per step: a bounded sample of the workload
+    X, G = workloads.sweep(18, SIGMA)  # same distribution, host generator
+    x = X.double().numpy()
+    g = G.double().numpy()
+    for _ in range(args.warmup):
+        oracle.backward64(oracle.project64(x), g)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.backward64(oracle.project64(x), g)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": "sweep T=2^26 sigma=1 fwd+bwd (host sample of 2^18 tokens per step)",
+                   "tokens": 1 << LOG2_T, "sigma": SIGMA},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": "2^18 tokens per step, float64 Newton "
+                                                     "forward + implicit backward"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--log2-tokens", type=int, default=LOG2_T)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    import birkhoff_projection_gb300 as b4
+    from birkhoff_projection_gb300 import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    warmup = max(args.warmup, 3)
+
+    X, G = workloads.sweep(args.log2_tokens, SIGMA, device=dev)
+    T = X.shape[0]
+    P = torch.empty_like(X)
+    dX = torch.empty_like(X)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        b4.forward(X, out=P)
+        if ev is not None:
+            ev[1].record(stream)
+        b4.backward(G, P=P, out=dX)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    # evaluation counts of this input (outside the timed region)
+    _, evals, nonconv = b4.forward(X, return_stats=True)
+    mean_evals = float(evals.float().mean())
+    torch.cuda.synchronize(dev)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            step(evs[k])
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    if dist is not None:
+        dist.barrier()
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = evs[0][0].elapsed_time(evs[-1][2])
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms * 1e-3)
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_avg = statistics.mean(bwd_ms)
+    peak, peak_kind = hbm_peak()
+    fwd_gbs = BYTES_FWD_F32 * T / (fwd_avg * 1e-3) / 1e9
+    bwd_gbs = BYTES_BWD_F32 * T / (bwd_avg * 1e-3) / 1e9
+    traffic = recorded_traffic()
+    dominant = "forward" if fwd_avg >= bwd_avg else "backward"
+    dom = {"forward": (fwd_gbs, BYTES_FWD_F32, "forward_f32"),
+           "backward": (bwd_gbs, BYTES_BWD_F32, "backward_f32")}[dominant]
+    tr = None if traffic is None or dom[2] not in traffic else traffic[dom[2]] * T
+
+    # MUFU ceiling: measured ex2 rate against the evaluations this input needed
+    mufu = (ctypes_probe(b4, dev))
+    mufu_per_token = 20.0 + (mean_evals - 1.0) * 12.0
+    clocks = clk.summary()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "sweep T=2^%d sigma=1 fp32, forward + backward" % args.log2_tokens,
+                   "tokens_per_gpu": T, "sigma": SIGMA,
+                   "l2": "inputs larger than L2 (%.1f GB per tensor, L2 129 MB)" % (T * 64 / 1e9)},
+        "fwd": {"tokens_per_s": world * T / (fwd_avg * 1e-3), "ms": fwd_avg, "gbs": fwd_gbs,
+                "hbm_frac": fwd_gbs / peak, "mean_evals": mean_evals,
+                "nonconverged": int(nonconv.item())},
+        "bwd": {"tokens_per_s": world * T / (bwd_avg * 1e-3), "ms": bwd_avg, "gbs": bwd_gbs,
+                "hbm_frac": bwd_gbs / peak},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dom[0], "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": dom[0] / peak,
+                     "traffic": tr, "algorithmic_bytes": dom[1] * T},
+        "roofline_fwd_bwd": {
+            "hbm_bound_tokens_per_s": peak * 1e9 / (BYTES_FWD_F32 + BYTES_BWD_F32),
+            "frac": value / world / (peak * 1e9 / (BYTES_FWD_F32 + BYTES_BWD_F32))},
+        "mufu": {"ex2_per_s": mufu, "ops_per_token_fwd": mufu_per_token,
+                 "bound_tokens_per_s": (mufu / mufu_per_token) if mufu else None},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "wall_s": wall,
+    }
+    line["e2e"] = e2e_host(b4, X, G, dev, steps=3)
+    if not args.no_cpu_baseline:
+        idx = slice(0, 1 << 22)
+        line["cpu_baseline"] = cpu_baseline(X[idx].double().cpu().numpy(),
+                                            G[idx].double().cpu().numpy())
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def ctypes_probe(b4, dev):
+    """MUFU ex2 operations per second on this GPU (microbenchmark)."""
+    import ctypes
+
+    import torch
+
+    L = b4.lib()
+    out = (ctypes.c_float * 2)()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    s = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    L.birkhoff4_mufu_probe(out, nsm * 8, 256, s)  # warm-up
+    if L.birkhoff4_mufu_probe(out, nsm * 8, 4096, s) != 0 or out[0] <= 0:
+        return None
+    return float(out[1]) / (float(out[0]) * 1e-3)
+
+
+def e2e_host(b4, X, G, dev, steps=3):
+    """The same step through the public API with host buffers: pinned host
+    X, dP -> device, forward + backward, P and dX -> host, every step inside
+    the timed region."""
+    import torch
+
+    T = X.shape[0]
+    Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    Gh = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
+    Ph = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    dXh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    Xh.copy_(X)
+    Gh.copy_(G)
+    Xd = torch.empty_like(X)
+    Gd = torch.empty_like(G)
+    Pd = torch.empty_like(X)
+    dXd = torch.empty_like(X)
+
+    def one():
+        Xd.copy_(Xh, non_blocking=True)
+        Gd.copy_(Gh, non_blocking=True)
+        b4.forward(Xd, out=Pd)
+        b4.backward(Gd, P=Pd, out=dXd)
+        Ph.copy_(Pd, non_blocking=True)
+        dXh.copy_(dXd, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    s = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        one()
+    e1.record(s)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = X.numel() * X.element_size()
+    return {"value": T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": 2 * nbytes,
+            "d2h_bytes_per_step": 2 * nbytes, "ms_per_step": ms, "steps": steps}
+
+
+if __name__ == "__main__":
+    main()

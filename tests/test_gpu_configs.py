@@ -1,0 +1,131 @@
+"""GPU parity on the five workloads at their full sizes, through the C ABI,
+in the launch configuration the benchmark times (the same entry points on the
+same persistent grid).
+
+  small_normal     T = 4096 N(0,1)                 forward, every token
+  normal_1m        T = 2^20 N(0,1), dP N(0,1)      forward + backward, every
+                                                   token; finite differences
+                                                   on a 4096-token sample
+  large_magnitude  T = 2^20, 20 N(0,1) + r_i + c_j  forward + backward, and
+                                                   20-iteration Sinkhorn-Knopp
+                                                   for the accuracy comparison
+  mhc_batch        bf16 [64,32,8192,4,4] = 2^24    fused forward + backward
+  sweep            T = 2^12..2^26, sigma 1 and 10  forward and backward;
+                                                   oracle on every token up
+                                                   to 2^22, on a 2^20-token
+                                                   random sample above, device
+                                                   residual on every token
+"""
+import numpy as np
+import pytest
+import torch
+
+import birkhoff_projection_gb300 as b4
+import oracle
+from birkhoff_projection_gb300 import workloads
+from _helpers import (TOL_DX_REL, TOL_P_LARGE, TOL_P_SMALL, TOL_RES_LARGE, TOL_RES_SMALL,
+                      bf16_ulp, max_abs_err, near_bf16_midpoint, np64, rel_fro, residual,
+                      residual_gpu, rne_bf16, to_bf16_values)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+CHUNK = 1 << 21  # tokens per oracle call (bounds host memory)
+
+
+def oracle_forward_backward(X, G=None):
+    """(P*, dX*) in float64 for tensors on any device, chunked."""
+    Ps, dXs = [], []
+    for s in range(0, X.shape[0], CHUNK):
+        x = np64(X[s:s + CHUNK])
+        p = oracle.project64(x)
+        Ps.append(p)
+        if G is not None:
+            dXs.append(oracle.backward64(p, np64(G[s:s + CHUNK])))
+    P = np.concatenate(Ps)
+    return (P, np.concatenate(dXs)) if G is not None else P
+
+
+def test_small_normal_forward():
+    X = workloads.small_normal(DEV)
+    P = b4.forward(X)
+    Pst = oracle_forward_backward(X)
+    assert max_abs_err(np64(P), Pst) <= TOL_P_SMALL
+    assert residual(np64(P)).max() <= TOL_RES_SMALL
+
+
+def test_normal_1m_forward_backward():
+    X, G = workloads.normal_1m(device=DEV)
+    P = b4.forward(X)
+    dX = b4.backward(G, P=P)
+    Pst, dXst = oracle_forward_backward(X, G)
+    Pg = np64(P)
+    assert max_abs_err(Pg, Pst) <= TOL_P_SMALL
+    assert residual(Pg).max() <= TOL_RES_SMALL
+    assert rel_fro(np64(dX), dXst) <= TOL_DX_REL
+    # the backward against finite differences of the oracle forward
+    idx = np.random.default_rng(0).choice(X.shape[0], 4096, replace=False)
+    fd = oracle.fd_backward64(np64(X)[idx], np64(G)[idx], h=1e-3)
+    assert rel_fro(np64(dX)[idx], fd) <= TOL_DX_REL
+
+
+def test_large_magnitude_forward_backward_and_sinkhorn20():
+    X, G = workloads.large_magnitude(device=DEV)
+    P, evals, nonconv = b4.forward(X, return_stats=True)
+    dX = b4.backward(G, P=P)
+    Pst, dXst = oracle_forward_backward(X, G)
+    Pg = np64(P)
+    err = np.abs(Pg - Pst).reshape(len(Pg), -1).max(1)
+    assert err.max() <= TOL_P_LARGE
+    assert residual(Pg).max() <= TOL_RES_LARGE
+    assert int(nonconv.item()) == 0
+    assert rel_fro(np64(dX), dXst) <= TOL_DX_REL
+    # the fixed-iteration reference on the same tokens: far less accurate
+    P20 = np64(b4.sinkhorn(X, iters=20))
+    err20 = np.abs(P20 - Pst).reshape(len(P20), -1).max(1)
+    assert np.median(err20) >= 100 * np.median(err)
+    assert np.median(residual(P20)) >= 100 * np.median(residual(Pg))
+
+
+def test_mhc_batch_bf16_fused():
+    Xb, Gb = workloads.mhc_batch(device=DEV)
+    P, dX = b4.forward_backward(Xb, Gb)
+    assert P.dtype == torch.bfloat16 and dX.dtype == torch.bfloat16
+    T = Xb.numel() // 16
+    Xf, Gf = Xb.reshape(T, 4, 4), Gb.reshape(T, 4, 4)
+    Pg, dXg = P.reshape(T, 4, 4), dX.reshape(T, 4, 4)
+    for s in range(0, T, CHUNK):
+        Pst, dXst = oracle_forward_backward(Xf[s:s + CHUNK], Gf[s:s + CHUNK])
+        p = to_bf16_values(Pg[s:s + CHUNK])
+        want = rne_bf16(Pst)
+        diff = p != want
+        # a difference is allowed only next to a rounding midpoint, by one ulp
+        assert not (diff & ~near_bf16_midpoint(Pst, 4e-6)).any()
+        assert (np.abs(p - want)[diff] <= bf16_ulp(Pst)[diff] * 1.001).all()
+        d = to_bf16_values(dXg[s:s + CHUNK])
+        scale = np.abs(dXst).reshape(len(d), -1).max(1)[:, None, None]
+        assert (np.abs(d - dXst) <= bf16_ulp(dXst) + 1e-4 * scale).all()
+    # marginals on the fp32-output path (bf16 in, fp32 out)
+    P32 = b4.forward(Xb.reshape(T, 4, 4), out_dtype=torch.float32)
+    assert float(residual_gpu(P32).max()) <= TOL_RES_SMALL
+
+
+@pytest.mark.parametrize("sigma", workloads.SWEEP_SIGMAS)
+@pytest.mark.parametrize("log2_T", workloads.SWEEP_LOG2_T)
+def test_sweep(log2_T, sigma):
+    X, G = workloads.sweep(log2_T, sigma, device=DEV)
+    T = X.shape[0]
+    P = b4.forward(X)
+    dX = b4.backward(G, P=P)
+    tol_p, tol_r = (TOL_P_SMALL, TOL_RES_SMALL) if sigma == 1.0 else (TOL_P_LARGE, TOL_RES_LARGE)
+    # device-side residual on every token
+    assert float(residual_gpu(P).max()) <= tol_r
+    if T <= (1 << 22):
+        idx = None
+    else:
+        g = torch.Generator(device="cpu").manual_seed(log2_T)
+        idx = torch.randperm(T, generator=g)[: 1 << 20].to(DEV)
+    Xs, Gs = (X, G) if idx is None else (X[idx], G[idx])
+    Ps, dXs = (P, dX) if idx is None else (P[idx], dX[idx])
+    Pst, dXst = oracle_forward_backward(Xs, Gs)
+    assert max_abs_err(np64(Ps), Pst) <= tol_p
+    assert rel_fro(np64(dXs), dXst) <= TOL_DX_REL
