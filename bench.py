@@ -77,7 +77,7 @@ def recorded_traffic():
 class ClockSampler:
     """nvidia-smi samples (200 ms) while the timed region runs."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -90,7 +90,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
@@ -110,23 +110,33 @@ class ClockSampler:
                 self.proc.kill()
             self._t.join(timeout=5)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen; restricted to samples
+        inside [t0, t1] (host wall clock) when any fall there."""
+        import datetime
+
         rows = []
         for ln in self.out.strip().splitlines():
             p = [x.strip() for x in ln.split(",")]
-            if len(p) < 8:
+            if len(p) < 9:
                 continue
             try:
-                rows.append((float(p[0]), float(p[1]), p[4:8]))
+                ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(p[1]), float(p[2]), p[5:9]))
             except ValueError:
                 continue
-        if not rows:
+        inside = [r for r in rows if t0 is not None and t0 <= r[0] <= t1]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "warm-up and timed region"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows),
-                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
-                "samples": len(rows)}
+        reasons = sorted({names[i] for _, _, _, r in inside for i in range(4)
+                          if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
 
 
 def cpu_baseline(X_host, G_host, target_s: float = 12.0):
@@ -191,11 +201,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--log2-tokens", type=int, default=LOG2_T)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -234,26 +245,29 @@ def main():
         if ev is not None:
             ev[2].record(stream)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize(dev)
     # evaluation counts of this input (outside the timed region)
     _, evals, nonconv = b4.forward(X, return_stats=True)
     mean_evals = float(evals.float().mean())
+    del evals
     torch.cuda.synchronize(dev)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        t0 = time.perf_counter()
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
         for k in range(args.steps):
             step(evs[k])
         torch.cuda.synchronize(dev)
-        wall = time.perf_counter() - t0
-    if dist is not None:
-        dist.barrier()
+        t1 = time.time()
+        if dist is not None:
+            dist.barrier()
+        time.sleep(0.1)  # let the sampler flush its last line
+    wall = t1 - t0
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     total_ms = evs[0][0].elapsed_time(evs[-1][2])
@@ -277,7 +291,7 @@ def main():
     # MUFU ceiling: measured ex2 rate against the evaluations this input needed
     mufu = (ctypes_probe(b4, dev))
     mufu_per_token = 20.0 + (mean_evals - 1.0) * 12.0
-    clocks = clk.summary()
+    clocks = clk.summary(t0, t1)
 
     if rank != 0:
         if dist is not None:
@@ -308,7 +322,8 @@ def main():
         "clocks": clocks,
         "wall_s": wall,
     }
-    line["e2e"] = e2e_host(b4, X, G, dev, steps=3)
+    if not args.no_e2e:
+        line["e2e"] = e2e_host(b4, X, G, dev, steps=3)
     if not args.no_cpu_baseline:
         idx = slice(0, 1 << 22)
         line["cpu_baseline"] = cpu_baseline(X[idx].double().cpu().numpy(),
@@ -336,8 +351,8 @@ def ctypes_probe(b4, dev):
 
 def e2e_host(b4, X, G, dev, steps=3):
     """The same step through the public API with host buffers: pinned host
-    X, dP -> device, forward + backward, P and dX -> host, every step inside
-    the timed region."""
+    X and dP in, P and dX out, streamed in chunks through the GPU
+    (forward_backward_host); every copy is inside the timed region."""
     import torch
 
     T = X.shape[0]
@@ -347,32 +362,21 @@ def e2e_host(b4, X, G, dev, steps=3):
     dXh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
     Xh.copy_(X)
     Gh.copy_(G)
-    Xd = torch.empty_like(X)
-    Gd = torch.empty_like(G)
-    Pd = torch.empty_like(X)
-    dXd = torch.empty_like(X)
-
-    def one():
-        Xd.copy_(Xh, non_blocking=True)
-        Gd.copy_(Gh, non_blocking=True)
-        b4.forward(Xd, out=Pd)
-        b4.backward(Gd, P=Pd, out=dXd)
-        Ph.copy_(Pd, non_blocking=True)
-        dXh.copy_(dXd, non_blocking=True)
-
-    one()
+    ws = b4.host_workspace(dev, X.dtype)
+    b4.forward_backward_host(Xh, Gh, Ph, dXh, device=dev, workspace=ws)
     torch.cuda.synchronize(dev)
     s = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
     for _ in range(steps):
-        one()
+        b4.forward_backward_host(Xh, Gh, Ph, dXh, device=dev, workspace=ws)
     e1.record(s)
     e1.synchronize()
     ms = e0.elapsed_time(e1) / steps
     nbytes = X.numel() * X.element_size()
     return {"value": T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": 2 * nbytes,
-            "d2h_bytes_per_step": 2 * nbytes, "ms_per_step": ms, "steps": steps}
+            "d2h_bytes_per_step": 2 * nbytes, "ms_per_step": ms, "steps": steps,
+            "api": "forward_backward_host (chunks of 2^22 tokens, 3 streams)"}
 
 
 if __name__ == "__main__":

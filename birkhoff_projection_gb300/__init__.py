@@ -23,8 +23,8 @@ import torch
 from . import _lib
 from ._lib import B4_BF16, B4_F32, Birkhoff4Error, Opts, check, lib
 
-__all__ = ["project", "forward", "backward", "forward_backward", "sinkhorn", "Birkhoff4Error",
-           "lib", "Projection"]
+__all__ = ["project", "forward", "backward", "forward_backward", "forward_backward_host",
+           "sinkhorn", "Birkhoff4Error", "lib", "Projection"]
 
 _DT = {torch.float32: B4_F32, torch.bfloat16: B4_BF16}
 
@@ -128,6 +128,75 @@ def sinkhorn(X: torch.Tensor, iters: int = 20, *, out: torch.Tensor = None) -> t
     with torch.cuda.device(X.device):
         check(fn(_ptr(X), _ptr(out), int(iters), T, _stream(X)), "birkhoff4_sinkhorn")
     return out
+
+
+def forward_backward_host(X: torch.Tensor, dP: torch.Tensor, P_out: torch.Tensor,
+                          dX_out: torch.Tensor, *, device=None, chunk_tokens: int = 1 << 22,
+                          slots: int = 3, fused: bool = False, workspace=None):
+    """Forward + backward of host-resident tokens, streamed through the GPU.
+
+    X, dP (inputs) and P_out, dX_out (outputs) are CPU tensors [..., 4, 4]
+    of one dtype, pinned for the copies to overlap.  The tokens go in chunks
+    through `slots` CUDA streams, each running copy-in, forward, backward and
+    copy-out of its chunk, so the host<->device copies of one chunk overlap the
+    kernels of another.  With fused=True each chunk takes the single fused
+    pass instead of the forward and backward passes.  Returns when the copies
+    have been enqueued; synchronize the device before reading the outputs.
+
+    workspace: optional list (one per slot) of 4 device tensors of
+    chunk_tokens tokens each, reused across calls."""
+    T = X.numel() // 16
+    for name, t in (("X", X), ("dP", dP), ("P_out", P_out), ("dX_out", dX_out)):
+        if t.is_cuda or t.dtype != X.dtype or t.numel() != X.numel() or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CPU tensor like X" % name)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    xs, gs = X.reshape(T, 4, 4), dP.reshape(T, 4, 4)
+    ps, ds = P_out.reshape(T, 4, 4), dX_out.reshape(T, 4, 4)
+    own = workspace is None
+    if own:
+        workspace = host_workspace(dev, X.dtype, chunk_tokens, slots)
+    streams = [torch.cuda.Stream(device=dev) for _ in range(len(workspace))]
+    if own:  # keep the allocator from reusing them while the streams run
+        for ws, s in zip(workspace, streams):
+            for w in ws:
+                w.record_stream(s)
+    cur = torch.cuda.current_stream(dev)
+    start = torch.cuda.Event()
+    start.record(cur)
+    for s in streams:
+        s.wait_event(start)
+    for i, c0 in enumerate(range(0, T, chunk_tokens)):
+        c1 = min(T, c0 + chunk_tokens)
+        n = c1 - c0
+        slot = i % len(workspace)
+        xd, gd, pd, dd = (w[:n] for w in workspace[slot])
+        with torch.cuda.stream(streams[slot]):
+            xd.copy_(xs[c0:c1], non_blocking=True)
+            gd.copy_(gs[c0:c1], non_blocking=True)
+            if fused:
+                _fused_into(xd, gd, pd, dd)
+            else:
+                forward(xd, out=pd)
+                backward(gd, P=pd, out=dd)
+            ps[c0:c1].copy_(pd, non_blocking=True)
+            ds[c0:c1].copy_(dd, non_blocking=True)
+    for s in streams:
+        done = torch.cuda.Event()
+        done.record(s)
+        cur.wait_event(done)
+
+
+def host_workspace(device, dtype, chunk_tokens: int = 1 << 22, slots: int = 3):
+    """Device buffers for forward_backward_host (allocate once, reuse)."""
+    return [[torch.empty(chunk_tokens, 4, 4, dtype=dtype, device=device) for _ in range(4)]
+            for _ in range(slots)]
+
+
+def _fused_into(X, dP, P, dX):
+    T = _check_tokens(X, "X")
+    fn = (lib().birkhoff4_forward_backward if X.dtype == torch.float32
+          else lib().birkhoff4_forward_backward_bf16)
+    check(fn(_ptr(X), _ptr(dP), _ptr(P), _ptr(dX), T, _stream(X)), "birkhoff4_forward_backward")
 
 
 class Projection(torch.autograd.Function):

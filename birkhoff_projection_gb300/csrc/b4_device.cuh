@@ -158,41 +158,44 @@ __device__ __forceinline__ void fence_async_smem() {
 template <class T>
 struct TileIO;
 
+
 template <>
 struct TileIO<float> {
   static constexpr int ROW_BYTES = 64;
   static constexpr CUtensorMapDataType TMA_TYPE = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   static constexpr CUtensorMapSwizzle TMA_SWIZZLE = CU_TENSOR_MAP_SWIZZLE_64B;
-  __device__ __forceinline__ static void load(const unsigned char* tile, int t, float v[16]) {
+  // chunk k of the row = matrix row k
+  __device__ __forceinline__ static void load(const unsigned char* tile, int t, float2 v[8]) {
     const unsigned char* row = tile + t * 64;
     const int sw = (t >> 1) & 3;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float4 c = *reinterpret_cast<const float4*>(row + 16 * (k ^ sw));
-      v[4 * k + 0] = c.x;
-      v[4 * k + 1] = c.y;
-      v[4 * k + 2] = c.z;
-      v[4 * k + 3] = c.w;
+      v[2 * k] = make_float2(c.x, c.y);
+      v[2 * k + 1] = make_float2(c.z, c.w);
     }
   }
-  __device__ __forceinline__ static void store(unsigned char* tile, int t, const float v[16]) {
+  __device__ __forceinline__ static void store(unsigned char* tile, int t, const float2 v[8]) {
     unsigned char* row = tile + t * 64;
     const int sw = (t >> 1) & 3;
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       *reinterpret_cast<float4*>(row + 16 * (k ^ sw)) =
-          make_float4(v[4 * k + 0], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+          make_float4(v[2 * k].x, v[2 * k].y, v[2 * k + 1].x, v[2 * k + 1].y);
   }
   // Unaligned global fallback: plain element loads/stores.
-  __device__ __forceinline__ static void gload(const void* base, int64_t t, float v[16]) {
+  __device__ __forceinline__ static void gload(const void* base, int64_t t, float2 v[8]) {
     const float* p = static_cast<const float*>(base) + 16 * t;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) v[k] = __ldg(p + k);
+    for (int k = 0; k < 8; ++k) v[k] = make_float2(__ldg(p + 2 * k), __ldg(p + 2 * k + 1));
   }
-  __device__ __forceinline__ static void gstore(void* base, int64_t t, const float v[16]) {
+  __device__ __forceinline__ static void gstore(void* base, int64_t t, const float2 v[8]) {
     float* p = static_cast<float*>(base) + 16 * t;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) p[k] = v[k];
+    for (int k = 0; k < 8; ++k) {
+      p[2 * k] = v[k].x;
+      p[2 * k + 1] = v[k].y;
+    }
   }
 };
 
@@ -201,43 +204,40 @@ struct TileIO<bf16_t> {
   static constexpr int ROW_BYTES = 32;
   static constexpr CUtensorMapDataType TMA_TYPE = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   static constexpr CUtensorMapSwizzle TMA_SWIZZLE = CU_TENSOR_MAP_SWIZZLE_32B;
-  __device__ __forceinline__ static void load(const unsigned char* tile, int t, float v[16]) {
+  // chunk k of the row = matrix rows 2k and 2k+1
+  __device__ __forceinline__ static void load(const unsigned char* tile, int t, float2 v[8]) {
     const unsigned char* row = tile + t * 32;
     const int sw = (t >> 2) & 1;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const uint4 c = *reinterpret_cast<const uint4*>(row + 16 * (k ^ sw));
-      v[8 * k + 0] = bf16lo(c.x);
-      v[8 * k + 1] = bf16hi(c.x);
-      v[8 * k + 2] = bf16lo(c.y);
-      v[8 * k + 3] = bf16hi(c.y);
-      v[8 * k + 4] = bf16lo(c.z);
-      v[8 * k + 5] = bf16hi(c.z);
-      v[8 * k + 6] = bf16lo(c.w);
-      v[8 * k + 7] = bf16hi(c.w);
+      v[4 * k + 0] = make_float2(bf16lo(c.x), bf16hi(c.x));
+      v[4 * k + 1] = make_float2(bf16lo(c.y), bf16hi(c.y));
+      v[4 * k + 2] = make_float2(bf16lo(c.z), bf16hi(c.z));
+      v[4 * k + 3] = make_float2(bf16lo(c.w), bf16hi(c.w));
     }
   }
-  __device__ __forceinline__ static void store(unsigned char* tile, int t, const float v[16]) {
+  __device__ __forceinline__ static void store(unsigned char* tile, int t, const float2 v[8]) {
     unsigned char* row = tile + t * 32;
     const int sw = (t >> 2) & 1;
 #pragma unroll
     for (int k = 0; k < 2; ++k)
       *reinterpret_cast<uint4*>(row + 16 * (k ^ sw)) =
-          make_uint4(pack_bf16(v[8 * k + 0], v[8 * k + 1]), pack_bf16(v[8 * k + 2], v[8 * k + 3]),
-                     pack_bf16(v[8 * k + 4], v[8 * k + 5]), pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+          make_uint4(pack_bf16(v[4 * k].x, v[4 * k].y), pack_bf16(v[4 * k + 1].x, v[4 * k + 1].y),
+                     pack_bf16(v[4 * k + 2].x, v[4 * k + 2].y), pack_bf16(v[4 * k + 3].x, v[4 * k + 3].y));
   }
-  __device__ __forceinline__ static void gload(const void* base, int64_t t, float v[16]) {
+  __device__ __forceinline__ static void gload(const void* base, int64_t t, float2 v[8]) {
     const unsigned short* p = static_cast<const unsigned short*>(base) + 16 * t;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) v[k] = bf16lo(__ldg(p + k));
+    for (int k = 0; k < 8; ++k) v[k] = make_float2(bf16lo(__ldg(p + 2 * k)), bf16lo(__ldg(p + 2 * k + 1)));
   }
-  __device__ __forceinline__ static void gstore(void* base, int64_t t, const float v[16]) {
+  __device__ __forceinline__ static void gstore(void* base, int64_t t, const float2 v[8]) {
     unsigned short* p = static_cast<unsigned short*>(base) + 16 * t;
 #pragma unroll
-    for (int k = 0; k < 16; k += 2) {
-      const uint32_t w = pack_bf16(v[k], v[k + 1]);
-      p[k] = static_cast<unsigned short>(w & 0xffffu);
-      p[k + 1] = static_cast<unsigned short>(w >> 16);
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t w = pack_bf16(v[k].x, v[k].y);
+      p[2 * k] = static_cast<unsigned short>(w & 0xffffu);
+      p[2 * k + 1] = static_cast<unsigned short>(w >> 16);
     }
   }
 };

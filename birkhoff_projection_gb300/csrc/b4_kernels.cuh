@@ -51,8 +51,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // a partial last tile (their results are dropped).
 template <Mode M>
 __device__ __forceinline__ void token_compute(const KParams& a, int64_t tok, bool valid,
-                                              const float in0[16], const float in1[16],
-                                              float out0[16], float out1[16]) {
+                                              const Tok& in0, const Tok& in1, Tok& out0,
+                                              Tok& out1) {
   if constexpr (M == Mode::Sinkhorn) {
     sinkhorn_fixed(in0, out0, a.iters);
   } else if constexpr (M == Mode::Backward) {
@@ -60,7 +60,7 @@ __device__ __forceinline__ void token_compute(const KParams& a, int64_t tok, boo
   } else {
     float beta[3];
     int evals;
-    float* p = (M == Mode::Recompute) ? out1 : out0;  // out1 is scratch there
+    Tok& p = (M == Mode::Recompute) ? out1 : out0;  // out1 is scratch there
     const bool ok = newton_forward(in0, p, beta, evals, a.cfg);
     if constexpr (M == Mode::Forward) {
       if (a.b != nullptr && valid) {
@@ -101,8 +101,8 @@ struct StreamShape {
   static_assert(TILE <= 256, "TMA box rows <= 256");
 };
 
-template <Mode M, class TIn, class TOut, int TILE, int NSTAGE, int NOSTAGE>
-__global__ void __launch_bounds__(TILE) stream_kernel(const __grid_constant__ KParams a) {
+template <Mode M, class TIn, class TOut, int TILE, int NSTAGE, int NOSTAGE, int MINB>
+__global__ void __launch_bounds__(TILE, MINB) stream_kernel(const __grid_constant__ KParams a) {
   using S = StreamShape<M, TIn, TOut, TILE, NSTAGE, NOSTAGE>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -153,9 +153,9 @@ __global__ void __launch_bounds__(TILE) stream_kernel(const __grid_constant__ KP
       failed = true;
       break;
     }
-    float in0[16], in1[16];
-    TileIO<TIn>::load(in_stage + s * S::STAGE_BYTES, tid, in0);
-    if constexpr (S::NIN == 2) TileIO<TIn>::load(in_stage + s * S::STAGE_BYTES + S::IN_BYTES, tid, in1);
+    Tok in0, in1;
+    TileIO<TIn>::load(in_stage + s * S::STAGE_BYTES, tid, in0.v);
+    if constexpr (S::NIN == 2) TileIO<TIn>::load(in_stage + s * S::STAGE_BYTES + S::IN_BYTES, tid, in1.v);
     __syncthreads();  // stage s fully read: refill it
     if (tid == 0) {
       pending &= ~(1u << s);
@@ -165,15 +165,15 @@ __global__ void __launch_bounds__(TILE) stream_kernel(const __grid_constant__ KP
 
     const int64_t tok = static_cast<int64_t>(tile) * TILE + tid;
     const bool valid = tok < a.T;
-    float out0[16], out1[16];
+    Tok out0, out1;
     token_compute<M>(a, tok, valid, in0, in1, out0, out1);
 
     const int os = it % NOSTAGE;
     if (tid == 0) bulk_wait_read<NOSTAGE - 1>();  // the store that used stage os is done
     __syncthreads();
     unsigned char* ob = out_stage + os * S::OSTAGE_BYTES;
-    TileIO<TOut>::store(ob, tid, out0);
-    if constexpr (S::NOUT == 2) TileIO<TOut>::store(ob + S::OUT_BYTES, tid, out1);
+    TileIO<TOut>::store(ob, tid, out0.v);
+    if constexpr (S::NOUT == 2) TileIO<TOut>::store(ob + S::OUT_BYTES, tid, out1.v);
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
@@ -202,18 +202,18 @@ __global__ void __launch_bounds__(256) plain_kernel(const __grid_constant__ KPar
        base += static_cast<int64_t>(gridDim.x) * 256) {
     const int64_t tok = base + threadIdx.x;
     const bool valid = tok < a.T;
-    float in0[16], in1[16], out0[16], out1[16];
+    Tok in0, in1, out0, out1;
     if (valid) {
-      TileIO<TIn>::gload(a.gin[0], tok, in0);
-      if constexpr (NIN == 2) TileIO<TIn>::gload(a.gin[1], tok, in1);
+      TileIO<TIn>::gload(a.gin[0], tok, in0.v);
+      if constexpr (NIN == 2) TileIO<TIn>::gload(a.gin[1], tok, in1.v);
     } else {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) in0[k] = in1[k] = 0.0f;
+      for (int k = 0; k < 8; ++k) in0.v[k] = in1.v[k] = make_float2(0.0f, 0.0f);
     }
     token_compute<M>(a, tok, valid, in0, in1, out0, out1);
     if (valid) {
-      TileIO<TOut>::gstore(a.gout[0], tok, out0);
-      if constexpr (NOUT == 2) TileIO<TOut>::gstore(a.gout[1], tok, out1);
+      TileIO<TOut>::gstore(a.gout[0], tok, out0.v);
+      if constexpr (NOUT == 2) TileIO<TOut>::gstore(a.gout[1], tok, out1.v);
     }
   }
 }

@@ -16,12 +16,42 @@
 
 namespace b4 {
 
-// Tile shape per pass: tokens per CTA step, input stages, output stages.
+// Tile shape per pass: tokens per CTA step, input stages, output stages,
+// minimum resident CTAs per SM (register budget).  Compute-heavy passes
+// (Newton forward, fused, recompute) trade stages for resident warps;
+// streaming passes keep more bytes in flight.
+#ifndef B4_FWD_TILE
+#define B4_FWD_TILE 128
+#endif
+#ifndef B4_FWD_NSTAGE
+#define B4_FWD_NSTAGE 3
+#endif
+#ifndef B4_FWD_NOSTAGE
+#define B4_FWD_NOSTAGE 2
+#endif
+#ifndef B4_FWD_MINB
+#define B4_FWD_MINB 1
+#endif
+#ifndef B4_BWD_TILE
+#define B4_BWD_TILE 128
+#endif
+#ifndef B4_BWD_NSTAGE
+#define B4_BWD_NSTAGE 3
+#endif
+#ifndef B4_BWD_NOSTAGE
+#define B4_BWD_NOSTAGE 2
+#endif
+#ifndef B4_BWD_MINB
+#define B4_BWD_MINB 1
+#endif
+
 template <Mode M, class TIn>
 struct TileCfg {
-  static constexpr int TILE = 128;
-  static constexpr int NSTAGE = 3;
-  static constexpr int NOSTAGE = 2;
+  static constexpr bool STREAMING = (M == Mode::Backward);
+  static constexpr int TILE = STREAMING ? B4_BWD_TILE : B4_FWD_TILE;
+  static constexpr int NSTAGE = STREAMING ? B4_BWD_NSTAGE : B4_FWD_NSTAGE;
+  static constexpr int NOSTAGE = STREAMING ? B4_BWD_NOSTAGE : B4_FWD_NOSTAGE;
+  static constexpr int MINB = STREAMING ? B4_BWD_MINB : B4_FWD_MINB;
 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -101,7 +131,7 @@ cudaError_t launch(const LaunchArgs& la, cudaStream_t stream) {
   for (int k = 0; k < NIN; ++k) aligned = aligned && aligned16(la.in[k]);
   for (int k = 0; k < NOUT; ++k) aligned = aligned && aligned16(la.out[k]);
 
-  auto kern = stream_kernel<M, TIn, TOut, C::TILE, C::NSTAGE, C::NOSTAGE>;
+  auto kern = stream_kernel<M, TIn, TOut, C::TILE, C::NSTAGE, C::NOSTAGE, C::MINB>;
   int grid_cap = 0;
   if (aligned) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);

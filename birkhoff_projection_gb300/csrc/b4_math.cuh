@@ -7,8 +7,10 @@
 // shift), s2.2 (implicit-differentiation backward, Hessian reuse), s1
 // (fixed-iteration Sinkhorn-Knopp as used in current mHC).
 //
-// Notation: x = X (row-major, x[4i+j]), p = P, beta = the column dual in
-// base-2 units (beta_j = b_j * log2(e)), beta_3 = 0.
+// A token lives in registers as eight float2 pairs (row i = pairs 2i, 2i+1:
+// (x_i0, x_i1), (x_i2, x_i3)), so that row scalings, row sums and column
+// sums run on the packed fp32x2 FMA pipe (FFMA2/FADD2/FMUL2, sm_100+).
+// beta is the column dual in base-2 units (beta_j = b_j log2 e), beta_3 = 0.
 #pragma once
 
 #include "b4_device.cuh"
@@ -16,48 +18,70 @@
 
 namespace b4 {
 
+struct Tok {
+  float2 v[8];  // v[2i] = (t_i0, t_i1), v[2i+1] = (t_i2, t_i3)
+  __device__ __forceinline__ float at(int i, int j) const {
+    const float2 q = v[2 * i + (j >> 1)];
+    return (j & 1) ? q.y : q.x;
+  }
+};
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 splat(float a) { return make_float2(a, a); }
+
 // Newton-step safeguards (values chosen by simulation of this exact fp32
 // iteration on N(0,1), N(0,10^2) and large-magnitude (|X| ~ 200) tokens):
 constexpr float kRidge = 1e-7f;      // added to every Hessian edge weight
-constexpr float kDampAbove = 1.0f;   // damp when the Newton decrement exceeds this
 constexpr float kClamp = 4.0f;       // max-norm of a step, natural-log units
 constexpr float kStagnation = 64.0f; // stop if residual <= 64 tol and not halving
 constexpr int kRefreshEvery = 8;     // log-domain re-evaluation period
 
-// Row softmax of (x*log2e + beta) in base 2, every row shifted by its
+// Row softmax of (x log2e + beta) in base 2, every row shifted by its
 // maximum [s2.1, numerical stability].
-__device__ __forceinline__ void eval_log(const float x[16], const float beta[3], float p[16]) {
+__device__ __forceinline__ void eval_log(const Tok& x, const float beta[3], Tok& p) {
+  const float2 L = splat(LOG2E);
+  const float2 b01 = make_float2(beta[0], beta[1]), b23 = make_float2(beta[2], 0.0f);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float z0 = fmaf(x[4 * i + 0], LOG2E, beta[0]);
-    const float z1 = fmaf(x[4 * i + 1], LOG2E, beta[1]);
-    const float z2 = fmaf(x[4 * i + 2], LOG2E, beta[2]);
-    const float z3 = x[4 * i + 3] * LOG2E;
-    const float m = fmaxf(max3(z0, z1, z2), z3);
-    const float e0 = ex2(z0 - m), e1 = ex2(z1 - m), e2 = ex2(z2 - m), e3 = ex2(z3 - m);
-    const float r = rcp((e0 + e1) + (e2 + e3));
-    p[4 * i + 0] = e0 * r;
-    p[4 * i + 1] = e1 * r;
-    p[4 * i + 2] = e2 * r;
-    p[4 * i + 3] = e3 * r;
+    float2 z01 = fma2(x.v[2 * i], L, b01);
+    float2 z23 = fma2(x.v[2 * i + 1], L, b23);
+    const float m = fmaxf(max3(z01.x, z01.y, z23.x), z23.y);
+    z01 = add2(z01, splat(-m));
+    z23 = add2(z23, splat(-m));
+    const float2 e01 = make_float2(ex2(z01.x), ex2(z01.y));
+    const float2 e23 = make_float2(ex2(z23.x), ex2(z23.y));
+    const float2 s = add2(e01, e23);
+    const float2 r = splat(rcp(s.x + s.y));
+    p.v[2 * i] = mul2(e01, r);
+    p.v[2 * i + 1] = mul2(e23, r);
   }
 }
 
 // The same row softmax after beta_j -= d_j, from the previous (row-normalised)
 // p: p_ij <- p_ij 2^{-d_j} / sum_k p_ik 2^{-d_k}.  Mathematically identical to
 // eval_log at the new beta; its rounding does not grow with |X|.
-__device__ __forceinline__ void eval_mul(float p[16], const float d[3]) {
-  const float w0 = ex2(-d[0]), w1 = ex2(-d[1]), w2 = ex2(-d[2]);
+__device__ __forceinline__ void eval_mul(Tok& p, const float d[3]) {
+  const float2 w01 = make_float2(ex2(-d[0]), ex2(-d[1]));
+  const float2 w23 = make_float2(ex2(-d[2]), 1.0f);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float q0 = p[4 * i + 0] * w0, q1 = p[4 * i + 1] * w1, q2 = p[4 * i + 2] * w2;
-    const float q3 = p[4 * i + 3];
-    const float r = rcp((q0 + q1) + (q2 + q3));
-    p[4 * i + 0] = q0 * r;
-    p[4 * i + 1] = q1 * r;
-    p[4 * i + 2] = q2 * r;
-    p[4 * i + 3] = q3 * r;
+    const float2 q01 = mul2(p.v[2 * i], w01);
+    const float2 q23 = mul2(p.v[2 * i + 1], w23);
+    const float2 s = add2(q01, q23);
+    const float2 r = splat(rcp(s.x + s.y));
+    p.v[2 * i] = mul2(q01, r);
+    p.v[2 * i + 1] = mul2(q23, r);
   }
+}
+
+// Column sums minus one (the gradient of the reduced dual [s2.1]), all four.
+__device__ __forceinline__ void colsum_minus_one(const Tok& p, float2& g01, float2& g23) {
+  const float2 c01 = add2(add2(p.v[0], p.v[2]), add2(p.v[4], p.v[6]));
+  const float2 c23 = add2(add2(p.v[1], p.v[3]), add2(p.v[5], p.v[7]));
+  g01 = add2(c01, splat(-1.0f));
+  g23 = add2(c23, splat(-1.0f));
 }
 
 // Edge weights of the dual Hessian seen as a graph Laplacian over the four
@@ -66,18 +90,24 @@ __device__ __forceinline__ void eval_mul(float p[16], const float d[3]) {
 //   sum_i diag(p_i) - p_i p_i^T, restricted to columns 0..2 by b_3 = 0],
 // which keeps the diagonal free of the cancellation in p (1 - p) when a row
 // is nearly one-hot.  Order: 01, 02, 03, 12, 13, 23.
-__device__ __forceinline__ void laplacian_weights(const float p[16], float w[6], float base) {
-  w[0] = w[1] = w[2] = w[3] = w[4] = w[5] = base;
+__device__ __forceinline__ void laplacian_weights(const Tok& p, float w[6], float base) {
+  float2 w0213 = splat(base);  // (w02, w13) accumulate as a pair
+  float w01 = base, w03 = base, w12 = base, w23 = base;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float a = p[4 * i + 0], b = p[4 * i + 1], c = p[4 * i + 2], d = p[4 * i + 3];
-    w[0] = fmaf(a, b, w[0]);
-    w[1] = fmaf(a, c, w[1]);
-    w[2] = fmaf(a, d, w[2]);
-    w[3] = fmaf(b, c, w[3]);
-    w[4] = fmaf(b, d, w[4]);
-    w[5] = fmaf(c, d, w[5]);
+    const float2 ab = p.v[2 * i], cd = p.v[2 * i + 1];
+    w0213 = fma2(ab, cd, w0213);
+    w01 = fmaf(ab.x, ab.y, w01);
+    w03 = fmaf(ab.x, cd.y, w03);
+    w12 = fmaf(ab.y, cd.x, w12);
+    w23 = fmaf(cd.x, cd.y, w23);
   }
+  w[0] = w01;
+  w[1] = w0213.x;
+  w[2] = w03;
+  w[3] = w12;
+  w[4] = w0213.y;
+  w[5] = w23;
 }
 
 // Solve H x = g (H the Laplacian of weights w with column 3 grounded) by
@@ -109,54 +139,54 @@ __device__ __forceinline__ void laplacian_solve(const float w[6], const float g[
 
 // Forward solve of one token [s2.1].  Returns true if the residual reached
 // tol (or its stagnation floor); p is the last evaluation, beta the dual.
-__device__ __forceinline__ bool newton_forward(const float x[16], float p[16], float beta[3],
-                                               int& evals, const NewtonCfg& cfg) {
+__device__ __forceinline__ bool newton_forward(const Tok& x, Tok& p, float beta[3], int& evals,
+                                               const NewtonCfg& cfg) {
   // Column-mean start: the exact dual when X_ij = u_i + v_j, and a first-order
   // estimate otherwise: b_j = -(mean_i X_ij - mean_i X_i3).
-  float cs[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) cs[j] = (x[j] + x[4 + j]) + (x[8 + j] + x[12 + j]);
-  const float all = (cs[0] + cs[1]) + (cs[2] + cs[3]);
+  const float2 cs01 = add2(add2(x.v[0], x.v[2]), add2(x.v[4], x.v[6]));
+  const float2 cs23 = add2(add2(x.v[1], x.v[3]), add2(x.v[5], x.v[7]));
+  const float all = (cs01.x + cs01.y) + (cs23.x + cs23.y);
   if (!isfinite(all)) {
     // NaN or infinite logits (or sums beyond the fp32 range): no projection
+    const float nan = __int_as_float(0x7fffffff);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) p[k] = __int_as_float(0x7fffffff);
-    beta[0] = beta[1] = beta[2] = __int_as_float(0x7fffffff);
+    for (int k = 0; k < 8; ++k) p.v[k] = splat(nan);
+    beta[0] = beta[1] = beta[2] = nan;
     evals = 0;
     return false;
   }
-#pragma unroll
-  for (int j = 0; j < 3; ++j) beta[j] = (cs[3] - cs[j]) * (0.25f * LOG2E);
+  const float q = 0.25f * LOG2E;
+  beta[0] = (cs23.y - cs01.x) * q;
+  beta[1] = (cs23.y - cs01.y) * q;
+  beta[2] = (cs23.y - cs23.x) * q;
   eval_log(x, beta, p);
   evals = 1;
   float prev = 3.0e38f;
   for (int k = 0;; ++k) {
-    // gradient: column sums of the row softmax minus one [s2.1]
-    float g[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) g[j] = ((p[j] + p[4 + j]) + (p[8 + j] + p[12 + j])) - 1.0f;
-    const float res = fmaxf(max3(fabsf(g[0]), fabsf(g[1]), fabsf(g[2])), fabsf(g[3]));
-    if (res <= cfg.tol) return true;
-    if (res <= kStagnation * cfg.tol && res > 0.5f * prev) return true;
+    float2 g01, g23;
+    colsum_minus_one(p, g01, g23);
+    const float res = fmaxf(max3(fabsf(g01.x), fabsf(g01.y), fabsf(g23.x)), fabsf(g23.y));
+    const bool stop = (res <= cfg.tol) || (res <= kStagnation * cfg.tol && res > 0.5f * prev);
+    if (stop) return true;
     if (evals >= cfg.max_evals) return false;
     prev = res;
     // Newton step on b_0..b_2 (natural-log units)
     float w[6], d[3];
+    const float g[3] = {g01.x, g01.y, g23.x};
     laplacian_weights(p, w, kRidge);
     laplacian_solve(w, g, d);
-    // damped when the Newton decrement lambda = sqrt(g^T H^-1 g) exceeds 1
+    // damped by 1/(1 + lambda) when the Newton decrement lambda =
+    // sqrt(g^T H^-1 g) exceeds 1, and clamped to kClamp in the max norm
     const float lam2 = fmaf(g[0], d[0], fmaf(g[1], d[1], g[2] * d[2]));
-    float scale = LOG2E;
-    if (lam2 > kDampAbove * kDampAbove) scale *= rcp(1.0f + lam2 * rsqrt(lam2));
-    // and clamped to kClamp in the max norm
-    const float dmax = max3(fabsf(d[0]), fabsf(d[1]), fabsf(d[2])) * scale;
-    if (dmax > kClamp * LOG2E) scale *= (kClamp * LOG2E) * rcp(dmax);
+    const float damp = (lam2 > 1.0f) ? rcp(1.0f + lam2 * rsqrt(lam2)) : 1.0f;
+    const float dmax = fmaxf(max3(fabsf(d[0]), fabsf(d[1]), fabsf(d[2])), 1e-30f);
+    const float scale = LOG2E * fminf(damp, kClamp * rcp(dmax));
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
       d[j] *= scale;  // base-2 units
       beta[j] -= d[j];
     }
-    if ((k + 1) % kRefreshEvery == 0)
+    if ((k & (kRefreshEvery - 1)) == kRefreshEvery - 1)
       eval_log(x, beta, p);
     else
       eval_mul(p, d);
@@ -171,61 +201,66 @@ __device__ __forceinline__ bool newton_forward(const float x[16], float p[16], f
 // The two sums are written in their difference forms (valid for unit row
 // sums, enforced first) so that nothing cancels when a row is nearly one-hot;
 // H is regularised by 1e-7 * max weight.
-__device__ __forceinline__ void implicit_backward(const float pin[16], const float G[16],
-                                                  float dx[16]) {
-  float p[16];
+__device__ __forceinline__ void implicit_backward(const Tok& pin, const Tok& G, Tok& dx) {
+  Tok p;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float r = rcp((pin[4 * k] + pin[4 * k + 1]) + (pin[4 * k + 2] + pin[4 * k + 3]));
-#pragma unroll
-    for (int j = 0; j < 4; ++j) p[4 * k + j] = pin[4 * k + j] * r;
+    const float2 s = add2(pin.v[2 * k], pin.v[2 * k + 1]);
+    const float2 r = splat(rcp(s.x + s.y));
+    p.v[2 * k] = mul2(pin.v[2 * k], r);
+    p.v[2 * k + 1] = mul2(pin.v[2 * k + 1], r);
   }
-  float D[16];
+  Tok D;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float* g = G + 4 * k;
-    const float* q = p + 4 * k;
-    const float e01 = g[0] - g[1], e02 = g[0] - g[2], e03 = g[0] - g[3];
-    const float e12 = g[1] - g[2], e13 = g[1] - g[3], e23 = g[2] - g[3];
-    D[4 * k + 0] = fmaf(q[1], e01, fmaf(q[2], e02, q[3] * e03));
-    D[4 * k + 1] = fmaf(q[2], e12, fmaf(q[3], e13, -q[0] * e01));
-    D[4 * k + 2] = fmaf(q[3], e23, -fmaf(q[0], e02, q[1] * e12));
-    D[4 * k + 3] = -fmaf(q[0], e03, fmaf(q[1], e13, q[2] * e23));
+    const float g0 = G.at(k, 0), g1 = G.at(k, 1), g2 = G.at(k, 2), g3 = G.at(k, 3);
+    const float q0 = p.at(k, 0), q1 = p.at(k, 1), q2 = p.at(k, 2), q3 = p.at(k, 3);
+    const float e01 = g0 - g1, e02 = g0 - g2, e03 = g0 - g3;
+    const float e12 = g1 - g2, e13 = g1 - g3, e23 = g2 - g3;
+    D.v[2 * k] = make_float2(fmaf(q1, e01, fmaf(q2, e02, q3 * e03)),
+                             fmaf(q2, e12, fmaf(q3, e13, -q0 * e01)));
+    D.v[2 * k + 1] = make_float2(fmaf(q3, e23, -fmaf(q0, e02, q1 * e12)),
+                                 -fmaf(q0, e03, fmaf(q1, e13, q2 * e23)));
   }
-  float v[3];
+  // v_l = sum_k p_kl D_kl for l = 0..2 (the column-3 half is unused)
+  float2 v01 = mul2(p.v[0], D.v[0]);
+  float2 v23 = mul2(p.v[1], D.v[1]);
 #pragma unroll
-  for (int l = 0; l < 3; ++l)
-    v[l] = fmaf(p[l], D[l], fmaf(p[4 + l], D[4 + l], fmaf(p[8 + l], D[8 + l], p[12 + l] * D[12 + l])));
+  for (int k = 1; k < 4; ++k) {
+    v01 = fma2(p.v[2 * k], D.v[2 * k], v01);
+    v23 = fma2(p.v[2 * k + 1], D.v[2 * k + 1], v23);
+  }
   float w[6];
   laplacian_weights(p, w, 0.0f);
   const float wmax = fmaxf(max3(w[0], w[1], w[2]), max3(w[3], w[4], w[5]));
   const float ridge = 1e-7f * wmax;
 #pragma unroll
   for (int e = 0; e < 6; ++e) w[e] += ridge;
+  const float v[3] = {v01.x, v01.y, v23.x};
   float lam[3];
   laplacian_solve(w, v, lam);
   const float l01 = lam[0] - lam[1], l02 = lam[0] - lam[2], l12 = lam[1] - lam[2];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float* q = p + 4 * k;
-    const float c0 = fmaf(q[1], l01, fmaf(q[2], l02, q[3] * lam[0]));
-    const float c1 = fmaf(q[2], l12, fmaf(q[3], lam[1], -q[0] * l01));
-    const float c2 = fmaf(q[3], lam[2], -fmaf(q[0], l02, q[1] * l12));
-    const float c3 = -fmaf(q[0], lam[0], fmaf(q[1], lam[1], q[2] * lam[2]));
-    dx[4 * k + 0] = q[0] * (D[4 * k + 0] - c0);
-    dx[4 * k + 1] = q[1] * (D[4 * k + 1] - c1);
-    dx[4 * k + 2] = q[2] * (D[4 * k + 2] - c2);
-    dx[4 * k + 3] = q[3] * (D[4 * k + 3] - c3);
+    const float q0 = p.at(k, 0), q1 = p.at(k, 1), q2 = p.at(k, 2), q3 = p.at(k, 3);
+    const float c0 = fmaf(q1, l01, fmaf(q2, l02, q3 * lam[0]));
+    const float c1 = fmaf(q2, l12, fmaf(q3, lam[1], -q0 * l01));
+    const float c2 = fmaf(q3, lam[2], -fmaf(q0, l02, q1 * l12));
+    const float c3 = -fmaf(q0, lam[0], fmaf(q1, lam[1], q2 * lam[2]));
+    dx.v[2 * k] = mul2(p.v[2 * k], add2(D.v[2 * k], make_float2(-c0, -c1)));
+    dx.v[2 * k + 1] = mul2(p.v[2 * k + 1], add2(D.v[2 * k + 1], make_float2(-c2, -c3)));
   }
 }
 
 // Fixed-iteration log-domain Sinkhorn-Knopp [s1]: `iters` times a row
 // normalisation then a column normalisation, from b = 0; P = exp(X + a + b).
 // Base-2 duals; every log-sum-exp is shifted by its maximum.
-__device__ __forceinline__ void sinkhorn_fixed(const float x[16], float p[16], int iters) {
+__device__ __forceinline__ void sinkhorn_fixed(const Tok& x, Tok& p, int iters) {
   float y[16];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) y[k] = x[k] * LOG2E;
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) y[4 * i + j] = x.at(i, j) * LOG2E;
   float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
   for (int it = 0; it < iters; ++it) {
 #pragma unroll
@@ -244,9 +279,10 @@ __device__ __forceinline__ void sinkhorn_fixed(const float x[16], float p[16], i
     }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) p[4 * i + j] = ex2((y[4 * i + j] + a[i]) + b[j]);
+  for (int i = 0; i < 4; ++i) {
+    p.v[2 * i] = make_float2(ex2((y[4 * i] + a[i]) + b[0]), ex2((y[4 * i + 1] + a[i]) + b[1]));
+    p.v[2 * i + 1] = make_float2(ex2((y[4 * i + 2] + a[i]) + b[2]), ex2((y[4 * i + 3] + a[i]) + b[3]));
+  }
 }
 
 }  // namespace b4

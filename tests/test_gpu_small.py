@@ -252,3 +252,21 @@ def test_large_magnitude_small():
     assert max_abs_err(np64(P), Pst) <= TOL_P_LARGE
     assert residual(np64(P)).max() <= TOL_RES_LARGE
     assert rel_fro(np64(dX), oracle.backward64(Pst, np64(G))) <= TOL_DX_REL
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_host_streaming_api(fused):
+    """forward_backward_host: host tokens through chunked, overlapped streams
+    give the same results as the device passes (ragged last chunk)."""
+    T = 5000
+    X = normal(T, seed=24)
+    G = normal(T, seed=25)
+    P = b4.forward(X)
+    dX = b4.backward(G, P=P)
+    Xh, Gh = X.cpu().pin_memory(), G.cpu().pin_memory()
+    Ph = torch.empty_like(Xh).pin_memory()
+    dXh = torch.empty_like(Xh).pin_memory()
+    b4.forward_backward_host(Xh, Gh, Ph, dXh, device=DEV, chunk_tokens=1024, slots=3, fused=fused)
+    torch.cuda.synchronize()
+    assert torch.equal(Ph, P.cpu())
+    assert max_abs_err(dXh.double().numpy(), np64(dX)) <= 1e-6
