@@ -24,7 +24,7 @@ namespace b4 {
 #define B4_FWD_TILE 128
 #endif
 #ifndef B4_FWD_NSTAGE
-#define B4_FWD_NSTAGE 3
+#define B4_FWD_NSTAGE 2
 #endif
 #ifndef B4_FWD_NOSTAGE
 #define B4_FWD_NOSTAGE 2
@@ -33,16 +33,22 @@ namespace b4 {
 #define B4_FWD_MINB 1
 #endif
 #ifndef B4_BWD_TILE
-#define B4_BWD_TILE 128
+#define B4_BWD_TILE 256
 #endif
 #ifndef B4_BWD_NSTAGE
-#define B4_BWD_NSTAGE 3
+#define B4_BWD_NSTAGE 2
 #endif
 #ifndef B4_BWD_NOSTAGE
-#define B4_BWD_NOSTAGE 2
+#define B4_BWD_NOSTAGE 3
 #endif
 #ifndef B4_BWD_MINB
 #define B4_BWD_MINB 1
+#endif
+#ifndef B4_FWD_PERWARP
+#define B4_FWD_PERWARP 0
+#endif
+#ifndef B4_BWD_PERWARP
+#define B4_BWD_PERWARP 0
 #endif
 
 template <Mode M, class TIn>
@@ -52,6 +58,8 @@ struct TileCfg {
   static constexpr int NSTAGE = STREAMING ? B4_BWD_NSTAGE : B4_FWD_NSTAGE;
   static constexpr int NOSTAGE = STREAMING ? B4_BWD_NOSTAGE : B4_FWD_NOSTAGE;
   static constexpr int MINB = STREAMING ? B4_BWD_MINB : B4_FWD_MINB;
+  // per-warp pipelines (TILE/32 independent warps per CTA) or CTA tiles
+  static constexpr bool PERWARP = STREAMING ? (B4_BWD_PERWARP != 0) : (B4_FWD_PERWARP != 0);
 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -131,13 +139,17 @@ cudaError_t launch(const LaunchArgs& la, cudaStream_t stream) {
   for (int k = 0; k < NIN; ++k) aligned = aligned && aligned16(la.in[k]);
   for (int k = 0; k < NOUT; ++k) aligned = aligned && aligned16(la.out[k]);
 
-  auto kern = stream_kernel<M, TIn, TOut, C::TILE, C::NSTAGE, C::NOSTAGE, C::MINB>;
+  using WS = WarpShape<M, TIn, TOut, C::TILE / 32, C::NSTAGE, C::NOSTAGE>;
+  auto kern = C::PERWARP ? warp_stream_kernel<M, TIn, TOut, C::TILE / 32, C::NSTAGE, C::NOSTAGE, C::MINB>
+                         : stream_kernel<M, TIn, TOut, C::TILE, C::NSTAGE, C::NOSTAGE, C::MINB>;
+  const int smem_bytes = C::PERWARP ? WS::SMEM_BYTES : S::SMEM_BYTES;
+  const int box_rows = C::PERWARP ? 32 : C::TILE;
   int grid_cap = 0;
   if (aligned) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (err != cudaSuccess) return err;
     int occ = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::TILE, S::SMEM_BYTES);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::TILE, smem_bytes);
     if (err != cudaSuccess) return err;
     grid_cap = nsm * std::max(occ, 1);
   }
@@ -158,13 +170,14 @@ cudaError_t launch(const LaunchArgs& la, cudaStream_t stream) {
     p.iters = la.iters;
     bool use_tma = aligned;
     if (use_tma) {
-      for (int k = 0; k < NIN && use_tma; ++k) use_tma = encode_rows<TIn>(&p.in[k], p.gin[k], n, C::TILE);
-      for (int k = 0; k < NOUT && use_tma; ++k) use_tma = encode_rows<TOut>(&p.out[k], p.gout[k], n, C::TILE);
+      for (int k = 0; k < NIN && use_tma; ++k) use_tma = encode_rows<TIn>(&p.in[k], p.gin[k], n, box_rows);
+      for (int k = 0; k < NOUT && use_tma; ++k) use_tma = encode_rows<TOut>(&p.out[k], p.gout[k], n, box_rows);
     }
     if (use_tma) {
-      p.ntiles = static_cast<int32_t>((n + C::TILE - 1) / C::TILE);
-      const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, grid_cap));
-      kern<<<grid, C::TILE, S::SMEM_BYTES, stream>>>(p);
+      p.ntiles = static_cast<int32_t>((n + box_rows - 1) / box_rows);
+      const int64_t per_cta = C::TILE / box_rows;  // tiles a CTA works on at once
+      const int grid = static_cast<int>(std::min<int64_t>((p.ntiles + per_cta - 1) / per_cta, grid_cap));
+      kern<<<grid, C::TILE, smem_bytes, stream>>>(p);
     } else {
       const int64_t blocks = (n + 255) / 256;
       const int grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(nsm) * 8));
