@@ -139,6 +139,23 @@ class ClockSampler:
                 "samples": len(inside), "window": window}
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """Maximum of x over the ranks of the process group (x itself alone)."""
+    if dist is None or not dist.is_initialized():
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank: int, world: int, steps: int, max_total_ms: float) -> float:
+    """Weak scaling: every rank projects its own tokens each step; the job's
+    throughput is all ranks' tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_total_ms * 1e-3)
+
+
 def cpu_baseline(X_host, G_host, target_s: float = 12.0):
     """The float64 oracle (Newton forward + implicit backward) on the host
     cores, on a bounded prefix of the same tokens."""
@@ -229,7 +246,7 @@ def main():
     torch.cuda.set_device(dev)
     warmup = max(args.warmup, 3)
 
-    X, G = workloads.sweep(args.log2_tokens, SIGMA, device=dev)
+    X, G = workloads.sweep(args.log2_tokens, SIGMA, device=dev, shard=rank)
     T = X.shape[0]
     P = torch.empty_like(X)
     dX = torch.empty_like(X)
@@ -271,12 +288,9 @@ def main():
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     total_ms = evs[0][0].elapsed_time(evs[-1][2])
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms * 1e-3)
+    value = whole_job_tokens_per_s(T, world, args.steps, total_ms)
     fwd_avg = statistics.mean(fwd_ms)
     bwd_avg = statistics.mean(bwd_ms)
     peak, peak_kind = hbm_peak()
@@ -349,12 +363,36 @@ def ctypes_probe(b4, dev):
     return float(out[1]) / (float(out[0]) * 1e-3)
 
 
-def e2e_host(b4, X, G, dev, steps=3):
-    """The same step through the public API with host buffers: pinned host
-    X and dP in, P and dX out, streamed in chunks through the GPU
-    (forward_backward_host); every copy is inside the timed region."""
+def bind_to_gpu_numa_node(dev) -> str:
+    """Run this process on the host cores of the GPU's NUMA node, so pinned
+    host buffers (first-touched here) sit next to the GPU's host link."""
     import torch
 
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        node = int(open("/sys/bus/pci/devices/%s/numa_node" % bus).read())
+        if node < 0:
+            return "no NUMA affinity reported"
+        cpus = open("/sys/devices/system/node/node%d/cpulist" % node).read().strip()
+        sel = set()
+        for part in cpus.split(","):
+            a, _, b = part.partition("-")
+            sel.update(range(int(a), int(b or a) + 1))
+        os.sched_setaffinity(0, sel)
+        return "node %d (%d cores)" % (node, len(sel))
+    except (OSError, ValueError, AttributeError) as e:
+        return "unbound (%s)" % type(e).__name__
+
+
+def e2e_host(b4, X, G, dev, steps=3, nstreams=4, chunk=1 << 21):
+    """The same step through the C ABI with host buffers
+    (birkhoff4_forward_backward_host): pinned host X and dP in, P and dX out,
+    streamed in chunks over `nstreams` streams; every copy is inside the
+    timed region."""
+    import torch
+
+    numa = bind_to_gpu_numa_node(dev)
     T = X.shape[0]
     Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
     Gh = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
@@ -362,21 +400,24 @@ def e2e_host(b4, X, G, dev, steps=3):
     dXh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
     Xh.copy_(X)
     Gh.copy_(G)
-    ws = b4.host_workspace(dev, X.dtype)
-    b4.forward_backward_host(Xh, Gh, Ph, dXh, device=dev, workspace=ws)
+    streams = [torch.cuda.Stream(device=dev) for _ in range(nstreams)]
+    ws = b4.host_workspace(dev, X.dtype, chunk_tokens=chunk, nstreams=nstreams)
+    b4.forward_backward_host(Xh, Gh, Ph, dXh, device=dev, workspace=ws, streams=streams)
     torch.cuda.synchronize(dev)
     s = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
     for _ in range(steps):
-        b4.forward_backward_host(Xh, Gh, Ph, dXh, device=dev, workspace=ws)
+        b4.forward_backward_host(Xh, Gh, Ph, dXh, device=dev, workspace=ws, streams=streams)
     e1.record(s)
     e1.synchronize()
     ms = e0.elapsed_time(e1) / steps
     nbytes = X.numel() * X.element_size()
     return {"value": T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": 2 * nbytes,
             "d2h_bytes_per_step": 2 * nbytes, "ms_per_step": ms, "steps": steps,
-            "api": "forward_backward_host (chunks of 2^22 tokens, 3 streams)"}
+            "host_link_gbs": 4 * nbytes / (ms * 1e-3) / 1e9,
+            "api": "birkhoff4_forward_backward_host (fused pass, chunks of %d tokens, %d streams)"
+                   % (chunk, nstreams), "numa": numa}
 
 
 if __name__ == "__main__":

@@ -130,73 +130,53 @@ def sinkhorn(X: torch.Tensor, iters: int = 20, *, out: torch.Tensor = None) -> t
     return out
 
 
-def forward_backward_host(X: torch.Tensor, dP: torch.Tensor, P_out: torch.Tensor,
-                          dX_out: torch.Tensor, *, device=None, chunk_tokens: int = 1 << 22,
-                          slots: int = 3, fused: bool = False, workspace=None):
-    """Forward + backward of host-resident tokens, streamed through the GPU.
+def forward_backward_host(X: torch.Tensor, dP: torch.Tensor, P_out, dX_out: torch.Tensor, *,
+                          device=None, workspace: torch.Tensor = None, streams=None,
+                          chunk_tokens: int = 1 << 22, nstreams: int = 3):
+    """Forward + backward of host-resident tokens (birkhoff4_forward_backward_host).
 
-    X, dP (inputs) and P_out, dX_out (outputs) are CPU tensors [..., 4, 4]
-    of one dtype, pinned for the copies to overlap.  The tokens go in chunks
-    through `slots` CUDA streams, each running copy-in, forward, backward and
-    copy-out of its chunk, so the host<->device copies of one chunk overlap the
-    kernels of another.  With fused=True each chunk takes the single fused
-    pass instead of the forward and backward passes.  Returns when the copies
-    have been enqueued; synchronize the device before reading the outputs.
-
-    workspace: optional list (one per slot) of 4 device tensors of
-    chunk_tokens tokens each, reused across calls."""
+    X, dP (inputs), P_out (or None) and dX_out are contiguous CPU tensors
+    [..., 4, 4] of one dtype, pinned for the copies to overlap the kernels.
+    The tokens are streamed through the GPU in chunks, round-robin over
+    `streams` (created here if not given): copy in, fused forward+backward,
+    copy out.  workspace: a device uint8 tensor (allocated here for
+    chunk_tokens per stream if not given).  Returns once the work is
+    enqueued; the current stream waits for it, so synchronize before
+    reading the outputs."""
     T = X.numel() // 16
-    for name, t in (("X", X), ("dP", dP), ("P_out", P_out), ("dX_out", dX_out)):
+    for name, t in (("X", X), ("dP", dP), ("dX_out", dX_out)) + ((("P_out", P_out),) if P_out is not None else ()):
         if t.is_cuda or t.dtype != X.dtype or t.numel() != X.numel() or not t.is_contiguous():
             raise ValueError("%s must be a contiguous CPU tensor like X" % name)
+    if X.dtype not in _DT:
+        raise TypeError("X must be float32 or bfloat16")
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    xs, gs = X.reshape(T, 4, 4), dP.reshape(T, 4, 4)
-    ps, ds = P_out.reshape(T, 4, 4), dX_out.reshape(T, 4, 4)
-    own = workspace is None
-    if own:
-        workspace = host_workspace(dev, X.dtype, chunk_tokens, slots)
-    streams = [torch.cuda.Stream(device=dev) for _ in range(len(workspace))]
-    if own:  # keep the allocator from reusing them while the streams run
-        for ws, s in zip(workspace, streams):
-            for w in ws:
-                w.record_stream(s)
+    if streams is None:
+        streams = [torch.cuda.Stream(device=dev) for _ in range(nstreams)]
+    rb = 16 * X.element_size()
+    if workspace is None:
+        workspace = torch.empty(len(streams) * 4 * chunk_tokens * rb, dtype=torch.uint8, device=dev)
+    handles = (ctypes.c_void_p * len(streams))(*[s.cuda_stream for s in streams])
     cur = torch.cuda.current_stream(dev)
     start = torch.cuda.Event()
     start.record(cur)
     for s in streams:
         s.wait_event(start)
-    for i, c0 in enumerate(range(0, T, chunk_tokens)):
-        c1 = min(T, c0 + chunk_tokens)
-        n = c1 - c0
-        slot = i % len(workspace)
-        xd, gd, pd, dd = (w[:n] for w in workspace[slot])
-        with torch.cuda.stream(streams[slot]):
-            xd.copy_(xs[c0:c1], non_blocking=True)
-            gd.copy_(gs[c0:c1], non_blocking=True)
-            if fused:
-                _fused_into(xd, gd, pd, dd)
-            else:
-                forward(xd, out=pd)
-                backward(gd, P=pd, out=dd)
-            ps[c0:c1].copy_(pd, non_blocking=True)
-            ds[c0:c1].copy_(dd, non_blocking=True)
+    with torch.cuda.device(dev):
+        check(lib().birkhoff4_forward_backward_host(
+            _ptr(X), _ptr(dP), _ptr(P_out), _ptr(dX_out), T, _DT[X.dtype], _ptr(workspace),
+            workspace.numel(), ctypes.cast(handles, ctypes.c_void_p), len(streams)),
+            "birkhoff4_forward_backward_host")
     for s in streams:
         done = torch.cuda.Event()
         done.record(s)
         cur.wait_event(done)
+        workspace.record_stream(s)
 
 
-def host_workspace(device, dtype, chunk_tokens: int = 1 << 22, slots: int = 3):
-    """Device buffers for forward_backward_host (allocate once, reuse)."""
-    return [[torch.empty(chunk_tokens, 4, 4, dtype=dtype, device=device) for _ in range(4)]
-            for _ in range(slots)]
-
-
-def _fused_into(X, dP, P, dX):
-    T = _check_tokens(X, "X")
-    fn = (lib().birkhoff4_forward_backward if X.dtype == torch.float32
-          else lib().birkhoff4_forward_backward_bf16)
-    check(fn(_ptr(X), _ptr(dP), _ptr(P), _ptr(dX), T, _stream(X)), "birkhoff4_forward_backward")
+def host_workspace(device, dtype, chunk_tokens: int = 1 << 22, nstreams: int = 3) -> torch.Tensor:
+    """Device staging buffer for forward_backward_host (allocate once, reuse)."""
+    rb = 16 * torch.empty((), dtype=dtype).element_size()
+    return torch.empty(nstreams * 4 * chunk_tokens * rb, dtype=torch.uint8, device=device)
 
 
 class Projection(torch.autograd.Function):

@@ -29,6 +29,8 @@ SIGNATURES = {
     "birkhoff4_backward_bf16": (_int, [_vp, _vp, _vp, _vp, _i64, _vp]),
     "birkhoff4_forward_backward": (_int, [_vp, _vp, _vp, _vp, _i64, _vp]),
     "birkhoff4_forward_backward_bf16": (_int, [_vp, _vp, _vp, _vp, _i64, _vp]),
+    "birkhoff4_forward_backward_host": (_int, [_vp, _vp, _vp, _vp, _i64, ctypes.c_int32, _vp,
+                                               ctypes.c_size_t, _vp, ctypes.c_int32]),
     "birkhoff4_sinkhorn": (_int, [_vp, _vp, _int, _i64, _vp]),
     "birkhoff4_sinkhorn_bf16": (_int, [_vp, _vp, _int, _i64, _vp]),
     "birkhoff4_strerror": (ctypes.c_char_p, [_int]),

@@ -3,6 +3,7 @@
 // dispatch to the pass launchers, diagnostics.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -140,6 +141,52 @@ int sinkhorn_impl(const void* X, void* P, int iters, int64_t n, cudaStream_t s) 
   return run<Mode::Sinkhorn, T, T>(la, s);
 }
 
+// Chunked host <-> device streaming of the fused pass over caller streams.
+template <class T>
+int host_stream_impl(const void* X_h, const void* dP_h, void* P_h, void* dX_h, int64_t n,
+                     unsigned char* ws, size_t chunk, const birkhoff4_stream_t* streams,
+                     int nstreams) {
+  const size_t rb = TileIO<T>::ROW_BYTES;
+  for (int64_t c0 = 0, ci = 0; c0 < n; c0 += static_cast<int64_t>(chunk), ++ci) {
+    const int64_t m = std::min<int64_t>(static_cast<int64_t>(chunk), n - c0);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(streams[ci % nstreams]);
+    unsigned char* slot = ws + static_cast<size_t>(ci % nstreams) * 4 * chunk * rb;
+    unsigned char* dx = slot;
+    unsigned char* dg = slot + chunk * rb;
+    unsigned char* dp = slot + 2 * chunk * rb;
+    unsigned char* dd = slot + 3 * chunk * rb;
+    const size_t off = static_cast<size_t>(c0) * rb, bytes = static_cast<size_t>(m) * rb;
+    cudaError_t e = cudaMemcpyAsync(dx, static_cast<const unsigned char*>(X_h) + off, bytes,
+                                    cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dg, static_cast<const unsigned char*>(dP_h) + off, bytes,
+                          cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    const int st = fused_impl<T>(dx, dg, P_h ? dp : nullptr, dd, m, s);
+    if (st != B4_OK) return st;
+    if (P_h != nullptr) {
+      e = cudaMemcpyAsync(static_cast<unsigned char*>(P_h) + off, dp, bytes, cudaMemcpyDeviceToHost, s);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    e = cudaMemcpyAsync(static_cast<unsigned char*>(dX_h) + off, dd, bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return B4_OK;
+}
+
+int host_stream_check(const void* X_h, const void* dP_h, const void* dX_h, int64_t n, int32_t dtype,
+                      const void* ws, size_t ws_bytes, const birkhoff4_stream_t* streams,
+                      int nstreams, size_t* chunk) {
+  if (n < 0 || !dtype_ok(dtype) || nstreams < 1 || nstreams > 16) return B4_EINVAL;
+  if (n == 0) return B4_OK;
+  if (X_h == nullptr || dP_h == nullptr || dX_h == nullptr || ws == nullptr || streams == nullptr)
+    return B4_EINVAL;
+  const size_t rb = dtype == B4_F32 ? 64 : 32;
+  *chunk = ws_bytes / (static_cast<size_t>(nstreams) * 4 * rb);
+  if (*chunk < 1) return B4_EINVAL;
+  return B4_OK;
+}
+
 // Throughput probe of MUFU ex2: eight independent recurrences a <- 2^-a per
 // thread (each stays in [0.5, 1]), so the MUFU pipe, not latency, limits it.
 __global__ void __launch_bounds__(256) mufu_probe_kernel(float* sink, int iters) {
@@ -236,6 +283,20 @@ int birkhoff4_forward_backward(const float* X, const float* dP, float* P, float*
 int birkhoff4_forward_backward_bf16(const uint16_t* X, const uint16_t* dP, uint16_t* P,
                                     uint16_t* dX, int64_t T, birkhoff4_stream_t stream) {
   return fused_impl<bf16_t>(X, dP, P, dX, T, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int birkhoff4_forward_backward_host(const void* X_h, const void* dP_h, void* P_h, void* dX_h,
+                                    int64_t T, int32_t dtype, void* workspace,
+                                    size_t workspace_bytes, const birkhoff4_stream_t* streams,
+                                    int32_t nstreams) {
+  size_t chunk = 0;
+  const int st = host_stream_check(X_h, dP_h, dX_h, T, dtype, workspace, workspace_bytes, streams,
+                                   nstreams, &chunk);
+  if (st != B4_OK || T == 0) return st;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  if (dtype == B4_F32)
+    return host_stream_impl<float>(X_h, dP_h, P_h, dX_h, T, ws, chunk, streams, nstreams);
+  return host_stream_impl<bf16_t>(X_h, dP_h, P_h, dX_h, T, ws, chunk, streams, nstreams);
 }
 
 int birkhoff4_sinkhorn(const float* X, float* P, int iters, int64_t T, birkhoff4_stream_t stream) {

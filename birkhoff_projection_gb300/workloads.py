@@ -77,10 +77,12 @@ def mhc_batch(shape=MHC_SHAPE, device="cpu"):
     return x, dp
 
 
-def sweep(log2_T: int, sigma: float, device="cpu"):
-    """(X, dP) for the throughput sweep: X fp32 iid N(0, sigma^2), dP N(0,1)."""
+def sweep(log2_T: int, sigma: float, device="cpu", shard: int = 0):
+    """(X, dP) for the throughput sweep: X fp32 iid N(0, sigma^2), dP N(0,1).
+    shard k > 0 draws another 2^log2_T tokens of the same distribution (the
+    k-th rank's share of a multi-GPU job)."""
     T = 1 << log2_T
-    g = _gen(4, device)
+    g = _gen(4 + 1000 * shard, device)
     x = torch.randn(T, 4, 4, generator=g, device=device, dtype=torch.float32)
     if sigma != 1.0:
         x.mul_(sigma)

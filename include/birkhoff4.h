@@ -148,6 +148,28 @@ int birkhoff4_forward_backward_bf16(const uint16_t *X, const uint16_t *dP, uint1
                                     uint16_t *dX, int64_t T, birkhoff4_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* Host-resident tokens [mHC s2.1, s2.2; batched as in s2.3]: forward and  */
+/* backward of tokens that live in host memory, streamed through the GPU.  */
+/*                                                                        */
+/* X_h, dP_h: host [T,4,4] inputs; P_h (or NULL) and dX_h: host [T,4,4]    */
+/* outputs; all of dtype `dtype` (B4_F32 or B4_BF16).  Pin them            */
+/* (cudaHostAlloc / cudaHostRegister) for the copies to overlap.           */
+/* workspace: caller-owned device memory of workspace_bytes, split into    */
+/* nstreams slots of four token arrays of `chunk` tokens each, chunk =     */
+/* workspace_bytes / (nstreams * 4 * row bytes) (64 B fp32, 32 B bf16);    */
+/* it must hold at least one token per slot.  streams: nstreams (1..16)    */
+/* caller-owned streams; chunk c runs on streams[c % nstreams]: copy in,   */
+/* the fused forward+backward pass (P recomputed and not copied out when   */
+/* P_h is NULL), copy out.  Copies of one stream overlap the kernels of    */
+/* another.  Returns once everything is enqueued: synchronise every stream */
+/* before reading the outputs or reusing the workspace.                    */
+/* ---------------------------------------------------------------------- */
+int birkhoff4_forward_backward_host(const void *X_h, const void *dP_h, void *P_h, void *dX_h,
+                                    int64_t T, int32_t dtype, void *workspace,
+                                    size_t workspace_bytes, const birkhoff4_stream_t *streams,
+                                    int32_t nstreams);
+
+/* ---------------------------------------------------------------------- */
 /* Reference: fixed-iteration Sinkhorn-Knopp [mHC s1], the scheme current  */
 /* mHC uses (e.g. iters = 20), kept for the accuracy comparison.           */
 /* Log domain, b = 0 start; one iteration is a row normalisation           */

@@ -87,6 +87,23 @@ def test_bad_options_are_einval(L):
     assert f(FAKE, FAKE, None, 4, opts(tol=float("inf")), None) == _lib.B4_EINVAL
 
 
+def test_host_streaming_argument_checks(L):
+    f = L.birkhoff4_forward_backward_host
+    streams = (ctypes.c_void_p * 2)(None, None)
+    ws = FAKE
+    assert f(FAKE, FAKE, FAKE, FAKE, -1, 0, ws, 1 << 20, streams, 2) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 7, ws, 1 << 20, streams, 2) == _lib.B4_EINVAL  # dtype
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 0, ws, 1 << 20, streams, 0) == _lib.B4_EINVAL  # nstreams
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 0, ws, 1 << 20, streams, 17) == _lib.B4_EINVAL
+    assert f(None, FAKE, FAKE, FAKE, 4, 0, ws, 1 << 20, streams, 2) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, FAKE, None, 4, 0, ws, 1 << 20, streams, 2) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 0, None, 1 << 20, streams, 2) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 0, ws, 1 << 20, None, 2) == _lib.B4_EINVAL
+    # a workspace too small for one token per slot (2 slots x 4 x 64 B)
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 0, ws, 511, streams, 2) == _lib.B4_EINVAL
+    assert f(None, None, None, None, 0, 0, None, 0, streams, 2) == _lib.B4_OK
+
+
 def test_negative_iters_is_einval(L):
     assert L.birkhoff4_sinkhorn(FAKE, FAKE, -1, 4, None) == _lib.B4_EINVAL
     assert L.birkhoff4_sinkhorn_bf16(FAKE, FAKE, -3, 4, None) == _lib.B4_EINVAL
