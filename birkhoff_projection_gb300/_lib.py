@@ -14,7 +14,7 @@ from . import _build
 _lock = threading.Lock()
 _lib = None
 
-B4_OK, B4_EINVAL, B4_ECUDA, B4_ENOTIMPL = 0, 1, 2, 3
+B4_OK, B4_EINVAL, B4_ECUDA, B4_ENOTIMPL, B4_ESCRATCH = 0, 1, 2, 3, 4
 B4_F32, B4_BF16 = 0, 1
 
 # Every function the header declares, with its ctypes signature.
@@ -31,6 +31,8 @@ SIGNATURES = {
     "birkhoff4_forward_backward_bf16": (_int, [_vp, _vp, _vp, _vp, _i64, _vp]),
     "birkhoff4_forward_backward_host": (_int, [_vp, _vp, _vp, _vp, _i64, ctypes.c_int32, _vp,
                                                ctypes.c_size_t, _vp, ctypes.c_int32]),
+    "birkhoff4_forward_backward_host_static": (_int, [_vp, _vp, _vp, _vp, _i64, ctypes.c_int32,
+                                                      _i64, _vp, ctypes.c_int32]),
     "birkhoff4_sinkhorn": (_int, [_vp, _vp, _int, _i64, _vp]),
     "birkhoff4_sinkhorn_bf16": (_int, [_vp, _vp, _int, _i64, _vp]),
     "birkhoff4_strerror": (ctypes.c_char_p, [_int]),

@@ -220,6 +220,11 @@ __global__ void selftest_wait_kernel(unsigned int* fault, uint64_t limit_ns) {
 }
 
 }  // namespace
+
+// Records a CUDA error for birkhoff4_last_cuda_error (for other translation
+// units of the library) and returns B4_ECUDA (B4_OK for cudaSuccess).
+int record_cuda_error(cudaError_t e) { return cuda_status(e); }
+
 }  // namespace b4
 
 using namespace b4;
@@ -238,6 +243,8 @@ const char* birkhoff4_strerror(int code) {
       return "CUDA error while preparing or launching a kernel";
     case B4_ENOTIMPL:
       return "not implemented in this build";
+    case B4_ESCRATCH:
+      return "chunk does not fit the library's static scratch (B4_STATIC_SCRATCH_BYTES)";
     default:
       return "unknown status code";
   }

@@ -70,7 +70,8 @@ enum birkhoff4_status {
     B4_OK = 0,
     B4_EINVAL = 1,
     B4_ECUDA = 2,
-    B4_ENOTIMPL = 3
+    B4_ENOTIMPL = 3,
+    B4_ESCRATCH = 4 /* request larger than the static scratch (see below) */
 };
 
 enum birkhoff4_dtype {
@@ -168,6 +169,38 @@ int birkhoff4_forward_backward_host(const void *X_h, const void *dP_h, void *P_h
                                     int64_t T, int32_t dtype, void *workspace,
                                     size_t workspace_bytes, const birkhoff4_stream_t *streams,
                                     int32_t nstreams);
+
+/* ---------------------------------------------------------------------- */
+/* The same host-streaming pass without any device allocation.  The pages  */
+/* have no counterpart: this is a deployment variant for callers that      */
+/* cannot allocate device memory -- code that must not call cudaMalloc     */
+/* because it synchronises the device, code whose device memory is owned   */
+/* by another framework's allocator, plugins or sandboxes where device     */
+/* allocations are not allowed.                                            */
+/*                                                                        */
+/* Arguments and results as birkhoff4_forward_backward_host, except that   */
+/* the staging area is a static device array of B4_STATIC_SCRATCH_BYTES    */
+/* (32 MiB) inside the library, reserved on every GPU the library is       */
+/* loaded on until the process exits.  chunk_tokens: tokens per chunk; 0   */
+/* takes the largest chunk that fits (32 MiB / (nstreams * 4 * row bytes), */
+/* e.g. 65536 fp32 tokens with 2 streams).  A chunk that does not fit      */
+/* returns B4_ESCRATCH; T itself is not limited (the call loops over       */
+/* chunks).  The first call on a device looks up the array's device        */
+/* address (cudaGetSymbolAddress, with that device current): make it       */
+/* before any stream capture.  Apart from that one-time lookup the call    */
+/* only enqueues copies and kernels; it never calls cudaMalloc, cudaFree   */
+/* or any other allocating routine.  Every call uses the same array:       */
+/* calls whose work overlaps on the GPU (concurrent streams, or a second   */
+/* call before the first call's streams have finished) race on it, so      */
+/* order them (for example by reusing the same streams).  Nothing in the   */
+/* array needs to start at zero: every staging slot is filled by a copy    */
+/* before it is read.                                                      */
+/* ---------------------------------------------------------------------- */
+#define B4_STATIC_SCRATCH_BYTES (32ull << 20)
+int birkhoff4_forward_backward_host_static(const void *X_h, const void *dP_h, void *P_h,
+                                           void *dX_h, int64_t T, int32_t dtype,
+                                           int64_t chunk_tokens,
+                                           const birkhoff4_stream_t *streams, int32_t nstreams);
 
 /* ---------------------------------------------------------------------- */
 /* Reference: fixed-iteration Sinkhorn-Knopp [mHC s1], the scheme current  */
