@@ -224,9 +224,15 @@ def main():
     ap.add_argument("--log2-tokens", type=int, default=LOG2_T)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="throughput sweep T = 2^12..2^26, sigma 1 and 10 (one JSON line each)")
+    ap.add_argument("--mhc", action="store_true",
+                    help="bf16 mHC batch [64,32,8192,4,4]: fused and separate passes")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep or args.mhc:
+        return run_extra(args)
 
     import numpy as np
     import torch
@@ -345,6 +351,86 @@ def main():
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def time_device(fn, reps, dev):
+    """Median CUDA-event time (ms) of fn() on the current stream; inputs
+    resident; for sizes below 2x L2 the caller rotates among input sets."""
+    import torch
+
+    s = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        fn(0)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record(s)
+    for i in range(reps):
+        fn(i)
+        ev[i + 1].record(s)
+    torch.cuda.synchronize(dev)
+    t = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
+    return t[len(t) // 2]
+
+
+def run_extra(args):
+    """Extra measurement lines: the throughput sweep and the bf16 mHC batch."""
+    import torch
+
+    import birkhoff_projection_gb300 as b4
+    from birkhoff_projection_gb300 import workloads
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    if args.sweep:
+        for sigma in workloads.SWEEP_SIGMAS:
+            for lg in workloads.SWEEP_LOG2_T:
+                T = 1 << lg
+                # rotate among enough input sets to exceed 2x L2 in total
+                nsets = max(1, -(-2 * l2 // (T * 64 * 2)))
+                sets = []
+                for k in range(min(nsets, 64)):
+                    X, G = workloads.sweep(lg, sigma, device=dev, shard=k)
+                    sets.append((X, G, torch.empty_like(X), torch.empty_like(X)))
+                fw = lambda i: b4.forward(sets[i % len(sets)][0], out=sets[i % len(sets)][2])
+
+                def fb(i):
+                    X, G, P, dX = sets[i % len(sets)]
+                    b4.forward(X, out=P)
+                    b4.backward(G, P=P, out=dX)
+
+                reps = max(20, min(2000, (1 << 27) // T))
+                tf = time_device(fw, reps, dev)
+                tfb = time_device(fb, reps, dev)
+                _, ev, _ = b4.forward(sets[0][0], return_stats=True)
+                print(json.dumps({"sweep": True, "log2_tokens": lg, "sigma": sigma,
+                                  "input_sets": len(sets), "fwd_ms": tf, "fwd_bwd_ms": tfb,
+                                  "fwd_tokens_per_s": T / (tf * 1e-3),
+                                  "fwd_bwd_tokens_per_s": T / (tfb * 1e-3),
+                                  "fwd_gbs": 128 * T / (tf * 1e-3) / 1e9,
+                                  "fwd_bwd_gbs": 320 * T / (tfb * 1e-3) / 1e9,
+                                  "mean_evals": float(ev.float().mean())}), flush=True)
+                del sets
+                torch.cuda.empty_cache()
+    if args.mhc:
+        Xb, Gb = workloads.mhc_batch(device=dev)
+        T = Xb.numel() // 16
+        P = torch.empty_like(Xb)
+        dX = torch.empty_like(Xb)
+        tfused = time_device(lambda i: b4._fused_pass(Xb, Gb, P, dX), 20, dev)
+
+        def sep(i):
+            b4.forward(Xb, out=P)
+            b4.backward(Gb, P=P, out=dX)
+
+        tsep = time_device(sep, 20, dev)
+        tf = time_device(lambda i: b4.forward(Xb, out=P), 20, dev)
+        print(json.dumps({"mhc_bf16": True, "tokens": T, "fused_ms": tfused,
+                          "fused_tokens_per_s": T / (tfused * 1e-3),
+                          "fused_gbs": 128 * T / (tfused * 1e-3) / 1e9,
+                          "separate_ms": tsep, "separate_tokens_per_s": T / (tsep * 1e-3),
+                          "separate_gbs": 160 * T / (tsep * 1e-3) / 1e9,
+                          "fwd_ms": tf, "fwd_gbs": 64 * T / (tf * 1e-3) / 1e9}), flush=True)
 
 
 def ctypes_probe(b4, dev):

@@ -119,6 +119,15 @@ def forward_backward(X: torch.Tensor, dP: torch.Tensor, *, want_P: bool = True):
     return P, dX
 
 
+def _fused_pass(X, dP, P, dX):
+    """The fused pass into preallocated outputs (P may be None)."""
+    T = _check_tokens(X, "X")
+    fn = (lib().birkhoff4_forward_backward if X.dtype == torch.float32
+          else lib().birkhoff4_forward_backward_bf16)
+    with torch.cuda.device(X.device):
+        check(fn(_ptr(X), _ptr(dP), _ptr(P), _ptr(dX), T, _stream(X)), "birkhoff4_forward_backward")
+
+
 def sinkhorn(X: torch.Tensor, iters: int = 20, *, out: torch.Tensor = None) -> torch.Tensor:
     """Fixed-iteration log-domain Sinkhorn-Knopp (the reference scheme)."""
     T = _check_tokens(X, "X")

@@ -100,8 +100,9 @@ typedef struct birkhoff4_opts {
 /* the log domain every 8 evaluations); the gradient is colsum(P) - 1 and  */
 /* the Hessian sum_i diag(p_i) - p_i p_i^T restricted to columns 0..2; the */
 /* 3x3 Newton system is solved by Laplacian elimination; the step is       */
-/* damped by 1/(1+lambda) when the Newton decrement lambda exceeds 1 and   */
-/* clamped to 4 in the max norm.  The loop stops when the residual         */
+/* clamped to 3 (natural-log units) in the max norm and, from the fifth    */
+/* step on, damped by 1/(1+lambda) when the Newton decrement lambda        */
+/* exceeds 1.  The loop stops when the residual                            */
 /* max_j |colsum_j - 1| <= tol (1e-6), when it stagnates below 64*tol, or  */
 /* after max_evals (48) evaluations.  P is the last evaluation (unit row   */
 /* sums up to rounding).                                                   */
