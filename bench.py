@@ -402,6 +402,15 @@ def run_extra(args):
                 reps = max(20, min(2000, (1 << 27) // T))
                 tf = time_device(fw, reps, dev)
                 tfb = time_device(fb, reps, dev)
+                # the same work replayed from a CUDA graph of 16 calls (no
+                # host launch cost between kernels)
+                graphs = {}
+                for key, f in (("fwd", fw), ("fwd_bwd", fb)):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        for i in range(16):
+                            f(i)
+                    graphs[key] = time_device(lambda i, g=g: g.replay(), max(5, reps // 16), dev) / 16
                 _, ev, _ = b4.forward(sets[0][0], return_stats=True)
                 print(json.dumps({"sweep": True, "log2_tokens": lg, "sigma": sigma,
                                   "input_sets": len(sets), "fwd_ms": tf, "fwd_bwd_ms": tfb,
@@ -409,6 +418,9 @@ def run_extra(args):
                                   "fwd_bwd_tokens_per_s": T / (tfb * 1e-3),
                                   "fwd_gbs": 128 * T / (tf * 1e-3) / 1e9,
                                   "fwd_bwd_gbs": 320 * T / (tfb * 1e-3) / 1e9,
+                                  "graph_fwd_ms": graphs["fwd"], "graph_fwd_bwd_ms": graphs["fwd_bwd"],
+                                  "graph_fwd_tokens_per_s": T / (graphs["fwd"] * 1e-3),
+                                  "graph_fwd_bwd_tokens_per_s": T / (graphs["fwd_bwd"] * 1e-3),
                                   "mean_evals": float(ev.float().mean())}), flush=True)
                 del sets
                 torch.cuda.empty_cache()

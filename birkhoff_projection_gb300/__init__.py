@@ -51,6 +51,24 @@ def _stream(t: torch.Tensor):
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
 
+class _on_device:
+    """Make t's device current for the call (a no-op when it already is)."""
+
+    __slots__ = ("ctx",)
+
+    def __init__(self, t: torch.Tensor):
+        idx = t.device.index
+        self.ctx = None if idx is None or idx == torch.cuda.current_device() else torch.cuda.device(idx)
+
+    def __enter__(self):
+        if self.ctx is not None:
+            self.ctx.__enter__()
+
+    def __exit__(self, *exc):
+        if self.ctx is not None:
+            self.ctx.__exit__(*exc)
+
+
 def forward(X: torch.Tensor, *, out: torch.Tensor = None, out_dtype=None, return_dual: bool = False,
             tol: float = 0.0, max_evals: int = 0, return_stats: bool = False):
     """Projection of every token of X ([..., 4, 4], fp32 or bf16).
@@ -74,7 +92,7 @@ def forward(X: torch.Tensor, *, out: torch.Tensor = None, out_dtype=None, return
         nonconv = torch.zeros(1, dtype=torch.int64, device=X.device)
         opts.evals_out = evals.data_ptr()
         opts.nonconv_count = nonconv.data_ptr()
-    with torch.cuda.device(X.device):
+    with _on_device(X):
         check(lib().birkhoff4_forward_ex(_ptr(X), _ptr(out), _ptr(b), T, ctypes.byref(opts),
                                          _stream(X)), "birkhoff4_forward_ex")
     res = (out,)
@@ -99,7 +117,7 @@ def backward(dP: torch.Tensor, *, P: torch.Tensor = None, X: torch.Tensor = None
     if out is None:
         out = torch.empty_like(dP)
     fn = lib().birkhoff4_backward if dP.dtype == torch.float32 else lib().birkhoff4_backward_bf16
-    with torch.cuda.device(dP.device):
+    with _on_device(dP):
         check(fn(_ptr(X), _ptr(P), _ptr(dP), _ptr(out), T, _stream(dP)), "birkhoff4_backward")
     return out
 
@@ -114,7 +132,7 @@ def forward_backward(X: torch.Tensor, dP: torch.Tensor, *, want_P: bool = True):
     dX = torch.empty_like(dP)
     fn = (lib().birkhoff4_forward_backward if X.dtype == torch.float32
           else lib().birkhoff4_forward_backward_bf16)
-    with torch.cuda.device(X.device):
+    with _on_device(X):
         check(fn(_ptr(X), _ptr(dP), _ptr(P), _ptr(dX), T, _stream(X)), "birkhoff4_forward_backward")
     return P, dX
 
@@ -124,7 +142,7 @@ def _fused_pass(X, dP, P, dX):
     T = _check_tokens(X, "X")
     fn = (lib().birkhoff4_forward_backward if X.dtype == torch.float32
           else lib().birkhoff4_forward_backward_bf16)
-    with torch.cuda.device(X.device):
+    with _on_device(X):
         check(fn(_ptr(X), _ptr(dP), _ptr(P), _ptr(dX), T, _stream(X)), "birkhoff4_forward_backward")
 
 
@@ -134,7 +152,7 @@ def sinkhorn(X: torch.Tensor, iters: int = 20, *, out: torch.Tensor = None) -> t
     if out is None:
         out = torch.empty_like(X)
     fn = lib().birkhoff4_sinkhorn if X.dtype == torch.float32 else lib().birkhoff4_sinkhorn_bf16
-    with torch.cuda.device(X.device):
+    with _on_device(X):
         check(fn(_ptr(X), _ptr(out), int(iters), T, _stream(X)), "birkhoff4_sinkhorn")
     return out
 

@@ -144,14 +144,22 @@ cudaError_t launch(const LaunchArgs& la, cudaStream_t stream) {
                          : stream_kernel<M, TIn, TOut, C::TILE, C::NSTAGE, C::NOSTAGE, C::MINB>;
   const int smem_bytes = C::PERWARP ? WS::SMEM_BYTES : S::SMEM_BYTES;
   const int box_rows = C::PERWARP ? 32 : C::TILE;
+  // Persistent grid size (SMs x resident CTAs), worked out once per device
+  // for this kernel: the shared-memory opt-in and the occupancy query are
+  // host calls that would otherwise dominate small launches.
+  static std::atomic<int> cap_cache[64];
   int grid_cap = 0;
   if (aligned) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (err != cudaSuccess) return err;
-    int occ = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::TILE, smem_bytes);
-    if (err != cudaSuccess) return err;
-    grid_cap = nsm * std::max(occ, 1);
+    grid_cap = dev < 64 ? cap_cache[dev].load(std::memory_order_acquire) : 0;
+    if (grid_cap == 0) {
+      err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+      if (err != cudaSuccess) return err;
+      int occ = 0;
+      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::TILE, smem_bytes);
+      if (err != cudaSuccess) return err;
+      grid_cap = nsm * std::max(occ, 1);
+      if (dev < 64) cap_cache[dev].store(grid_cap, std::memory_order_release);
+    }
   }
 
   for (int64_t done = 0; done < la.T; done += kChunkTokens) {

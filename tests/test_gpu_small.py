@@ -272,3 +272,26 @@ def test_host_streaming_api(dtype, nstreams, chunk, with_P):
     if with_P:
         assert torch.equal(Ph, P.cpu())
     assert torch.equal(dXh, dX.cpu())
+
+
+def test_cuda_graph_capture_and_replay():
+    """The passes capture into a CUDA graph (no host synchronisation or
+    allocation on the launch path) and replay on new inputs."""
+    T = 10000
+    X, G = normal(T, seed=30), normal(T, seed=31)
+    P, dX = torch.empty_like(X), torch.empty_like(X)
+    b4.forward(X, out=P)  # one-time per-device set-up happens outside the capture
+    b4.backward(G, P=P, out=dX)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        b4.forward(X, out=P)
+        b4.backward(G, P=P, out=dX)
+    for seed in (32, 34):
+        X.copy_(normal(T, seed=seed))
+        G.copy_(normal(T, seed=seed + 1))
+        g.replay()
+        torch.cuda.synchronize()
+        Pe = b4.forward(X)
+        assert torch.equal(P, Pe)
+        assert torch.equal(dX, b4.backward(G, P=Pe))
