@@ -49,7 +49,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Per-token work of each mode; `valid` is false for the zero-filled rows of
 // a partial last tile (their results are dropped).
-template <Mode M>
+template <Mode M, class TIn>
 __device__ __forceinline__ void token_compute(const KParams& a, int64_t tok, bool valid,
                                               const Tok& in0, const Tok& in1, Tok& out0,
                                               Tok& out1) {
@@ -61,7 +61,17 @@ __device__ __forceinline__ void token_compute(const KParams& a, int64_t tok, boo
     float beta[3];
     int evals;
     Tok& p = (M == Mode::Recompute) ? out1 : out0;  // out1 is scratch there
-    const bool ok = newton_forward(in0, p, beta, evals, a.cfg);
+    // the periodic refresh re-reads X from global memory (the zero rows of a
+    // partial tile converge at once and never refresh)
+    auto reload = [&](Tok& xr) {
+      if (valid) {
+        TileIO<TIn>::gload(a.gin[0], tok, xr.v);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xr.v[k] = make_float2(0.0f, 0.0f);
+      }
+    };
+    const bool ok = newton_forward(in0, p, beta, evals, a.cfg, reload);
     if constexpr (M == Mode::Forward) {
       if (a.b != nullptr && valid) {
         const float b0 = beta[0] * LN2, b1 = beta[1] * LN2, b2 = beta[2] * LN2;
@@ -166,7 +176,7 @@ __global__ void __launch_bounds__(TILE, MINB) stream_kernel(const __grid_constan
     const int64_t tok = static_cast<int64_t>(tile) * TILE + tid;
     const bool valid = tok < a.T;
     Tok out0, out1;
-    token_compute<M>(a, tok, valid, in0, in1, out0, out1);
+    token_compute<M, TIn>(a, tok, valid, in0, in1, out0, out1);
 
     const int os = it % NOSTAGE;
     if (tid == 0) bulk_wait_read<NOSTAGE - 1>();  // the store that used stage os is done
@@ -280,7 +290,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) warp_stream_kernel(const __g
     const int64_t tok = static_cast<int64_t>(sub) * 32 + lane;
     const bool valid = tok < a.T;
     Tok out0, out1;
-    token_compute<M>(a, tok, valid, in0, in1, out0, out1);
+    token_compute<M, TIn>(a, tok, valid, in0, in1, out0, out1);
 
     const int os = it % NOSTAGE;
     if (lane == 0) bulk_wait_read<NOSTAGE - 1>();  // the store that used stage os is done
@@ -323,7 +333,7 @@ __global__ void __launch_bounds__(256) plain_kernel(const __grid_constant__ KPar
 #pragma unroll
       for (int k = 0; k < 8; ++k) in0.v[k] = in1.v[k] = make_float2(0.0f, 0.0f);
     }
-    token_compute<M>(a, tok, valid, in0, in1, out0, out1);
+    token_compute<M, TIn>(a, tok, valid, in0, in1, out0, out1);
     if (valid) {
       TileIO<TOut>::gstore(a.gout[0], tok, out0.v);
       if constexpr (NOUT == 2) TileIO<TOut>::gstore(a.gout[1], tok, out1.v);

@@ -27,7 +27,7 @@ namespace b4 {
 #define B4_FWD_NSTAGE 2
 #endif
 #ifndef B4_FWD_NOSTAGE
-#define B4_FWD_NOSTAGE 2
+#define B4_FWD_NOSTAGE 1
 #endif
 #ifndef B4_FWD_MINB
 #define B4_FWD_MINB 1

@@ -141,8 +141,12 @@ __device__ __forceinline__ void laplacian_solve(const float w[6], const float g[
 
 // Forward solve of one token [s2.1].  Returns true if the residual reached
 // tol (or its stagnation floor); p is the last evaluation, beta the dual.
+// reload(Tok&) fetches X again for the periodic log-domain refresh, so X does
+// not have to stay live in registers through the iteration (no N(0,1) token
+// ever gets that far).
+template <class Reload>
 __device__ __forceinline__ bool newton_forward(const Tok& x, Tok& p, float beta[3], int& evals,
-                                               const NewtonCfg& cfg) {
+                                               const NewtonCfg& cfg, Reload&& reload) {
   // Column-mean start: the exact dual when X_ij = u_i + v_j, and a first-order
   // estimate otherwise: b_j = -(mean_i X_ij - mean_i X_i3).
   const float2 cs01 = add2(add2(x.v[0], x.v[2]), add2(x.v[4], x.v[6]));
@@ -195,10 +199,13 @@ __device__ __forceinline__ bool newton_forward(const Tok& x, Tok& p, float beta[
       d[j] *= scale;  // base-2 units
       beta[j] -= d[j];
     }
-    if ((k & (kRefreshEvery - 1)) == kRefreshEvery - 1)
-      eval_log(x, beta, p);
-    else
+    if ((k & (kRefreshEvery - 1)) == kRefreshEvery - 1) {
+      Tok xr;
+      reload(xr);
+      eval_log(xr, beta, p);
+    } else {
       eval_mul(p, d);
+    }
     ++evals;
   }
 }
