@@ -112,3 +112,24 @@ def fixed_point_family(T: int, seed: int, spread: float = 5.0, floor: float = 1e
     v = (torch.rand(T, 1, 4, generator=g, device=device, dtype=torch.float64) * 2 - 1) * spread
     x = torch.log(q) + u + v
     return x.to(dtype), q
+
+
+def fixed_point_family_n(n: int, T: int, seed: int, spread: float = 5.0, floor: float = 1e-3,
+                         nperm: int = 8, device="cpu", dtype=torch.float64):
+    """(X, Q) for n x n tokens: Q = a random mixture of `nperm` random
+    permutation matrices plus ``floor`` times the uniform matrix
+    (renormalised; strictly positive, doubly stochastic) and
+    X = log Q + u 1^T + 1 v^T, whose projection is Q.  Float64."""
+    g = _gen(seed, device)
+    perms = torch.argsort(torch.rand(T, nperm, n, generator=g, device=device), dim=-1)
+    w = -torch.log(torch.rand(T, nperm, generator=g, device=device, dtype=torch.float64))
+    w = w / w.sum(dim=1, keepdim=True)
+    q = torch.zeros(T, n, n, dtype=torch.float64, device=device)
+    rows = torch.arange(n, device=device)
+    for k in range(nperm):
+        q[torch.arange(T, device=device)[:, None], rows[None, :], perms[:, k, :]] += w[:, k:k + 1]
+    q = (q + floor / n) / (1.0 + floor)
+    u = (torch.rand(T, n, 1, generator=g, device=device, dtype=torch.float64) * 2 - 1) * spread
+    v = (torch.rand(T, 1, n, generator=g, device=device, dtype=torch.float64) * 2 - 1) * spread
+    x = torch.log(q) + u + v
+    return x.to(dtype), q

@@ -76,6 +76,13 @@ def _load():
         lib.oracle_backward64.restype = None
         lib.oracle_laplacian_solve64.argtypes = [dp, dp, dp, i64]
         lib.oracle_laplacian_solve64.restype = i64
+        i32 = ctypes.c_int32
+        lib.oracle_sinkhorn64_n.argtypes = [dp, dp, dp, i32, i64, ctypes.c_double, i32, ip]
+        lib.oracle_sinkhorn64_n.restype = i64
+        lib.oracle_newton64_n.argtypes = [dp, dp, dp, i32, i64, ctypes.c_double, i32, ip]
+        lib.oracle_newton64_n.restype = i64
+        lib.oracle_backward64_n.argtypes = [dp, dp, dp, i32, i64]
+        lib.oracle_backward64_n.restype = None
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_version.restype = ctypes.c_int
         _lib = lib
@@ -213,9 +220,80 @@ def laplacian_solve64(w, r):
     return x
 
 
+# ---------------------------------------------------------------------------
+# General n x n (2 <= n <= 16): the dual reduced to n-1 free variables
+# [mHC s2.1]; same methods as the 4 x 4 functions, written for any n.
+# ---------------------------------------------------------------------------
+def _tokens_n(X):
+    if hasattr(X, "detach"):
+        X = X.detach().to("cpu").double().numpy()
+    a = np.ascontiguousarray(np.asarray(X, dtype=np.float64))
+    n = a.shape[-1]
+    if a.ndim < 2 or a.shape[-2] != n or not (2 <= n <= 16):
+        raise ValueError("expected [..., n, n] with 2 <= n <= 16, got %s" % (a.shape,))
+    return a.reshape(-1, n * n), n
+
+
+def sinkhorn64_n(X, tol: float = 1e-13, max_iters: int = 20000):
+    """Log-domain Sinkhorn-Knopp for n x n tokens: (P, b, iters, nonconverged)."""
+    lib = _load()
+    x, n = _tokens_n(X)
+    T = x.shape[0]
+    P = np.empty_like(x)
+    b = np.empty((T, n))
+    it = np.empty(T, dtype=np.int32)
+    k = lib.oracle_sinkhorn64_n(_ptr(x), _ptr(P), _ptr(b), n, T, float(tol), int(max_iters), _ptr(it))
+    return P.reshape(-1, n, n), b, it, int(k)
+
+
+def newton64_n(X, tol: float = 1e-14, max_iters: int = 200):
+    """Newton on the (n-1)-variable reduced dual: (P, b, iters, nonconverged)."""
+    lib = _load()
+    x, n = _tokens_n(X)
+    T = x.shape[0]
+    P = np.empty_like(x)
+    b = np.empty((T, n))
+    it = np.empty(T, dtype=np.int32)
+    k = lib.oracle_newton64_n(_ptr(x), _ptr(P), _ptr(b), n, T, float(tol), int(max_iters), _ptr(it))
+    return P.reshape(-1, n, n), b, it, int(k)
+
+
+def backward64_n(P, G):
+    """Implicit-function-theorem VJP for n x n tokens."""
+    lib = _load()
+    p, n = _tokens_n(P)
+    g, n2 = _tokens_n(G)
+    if p.shape != g.shape:
+        raise ValueError("P and G shapes differ")
+    dX = np.empty_like(p)
+    lib.oracle_backward64_n(_ptr(p), _ptr(g), _ptr(dX), n, p.shape[0])
+    return dX.reshape(-1, n, n)
+
+
+def fd_backward64_n(X, G, h: float = 1e-3):
+    """Validator: central differences of newton64_n with one Richardson step."""
+    x, n = _tokens_n(X)
+    g, _ = _tokens_n(G)
+    T = x.shape[0]
+    x = x.reshape(T, n, n)
+    g = g.reshape(T, n, n)
+    eye = np.eye(n * n).reshape(n * n, n, n)
+
+    def central(step):
+        plus = (x[:, None] + step * eye[None]).reshape(-1, n, n)
+        minus = (x[:, None] - step * eye[None]).reshape(-1, n, n)
+        Pp = newton64_n(plus, tol=1e-15)[0].reshape(T, n * n, n, n)
+        Pm = newton64_n(minus, tol=1e-15)[0].reshape(T, n * n, n, n)
+        return np.einsum("tij,tkij->tk", g, Pp - Pm) / (2.0 * step)
+
+    return ((4.0 * central(h / 2) - central(h)) / 3.0).reshape(T, n, n)
+
+
 def marginal_residual(P) -> np.ndarray:
-    """Per token max(|P 1 - 1|_inf, |P^T 1 - 1|_inf)."""
-    p = np.asarray(P, dtype=np.float64).reshape(-1, 4, 4)
+    """Per token max(|P 1 - 1|_inf, |P^T 1 - 1|_inf) (any n x n)."""
+    P = np.asarray(P, dtype=np.float64)
+    n = P.shape[-1]
+    p = P.reshape(-1, n, n)
     r = np.abs(p.sum(axis=2) - 1.0).max(axis=1)
     c = np.abs(p.sum(axis=1) - 1.0).max(axis=1)
     return np.maximum(r, c)

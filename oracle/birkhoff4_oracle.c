@@ -492,3 +492,316 @@ void oracle_backward64(const double *P, const double *G, double *dX, int64_t T)
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) backward_token(P + 16 * t, G + 16 * t, dX + 16 * t);
 }
+
+/* ======================================================================== */
+/* General n x n (2 <= n <= 16): the same projection for an n x n logit     */
+/* matrix, the dual reduced to n-1 free variables (b_{n-1} = 0) [mHC s2.1: */
+/* m-1 free variables for m columns].  Written separately from the 4 x 4    */
+/* code above (which it is checked against at n = 4); the Newton system is  */
+/* solved by Cholesky after symmetric diagonal scaling, in long double.     */
+/* ======================================================================== */
+#define NMAX 16
+
+static double lse_n(const double *v, int n, int stride)
+{
+    double m = -INFINITY;
+    for (int k = 0; k < n; ++k)
+        if (v[k * stride] > m) m = v[k * stride];
+    if (isinf(m) && m < 0) return m;
+    double s = 0.0;
+    for (int k = 0; k < n; ++k) s += exp(v[k * stride] - m);
+    return m + log(s);
+}
+
+static double marginal_residual_n(const double *p, int n)
+{
+    double res = 0.0;
+    for (int i = 0; i < n; ++i) {
+        double s = 0.0, c = 0.0;
+        for (int j = 0; j < n; ++j) {
+            s += p[n * i + j];
+            c += p[n * j + i];
+        }
+        double d = fmax(fabs(s - 1.0), fabs(c - 1.0));
+        if (d > res || isnan(d)) res = d;
+    }
+    return res;
+}
+
+static int nonfinite_n(const double *x, double *p, double *b, int n)
+{
+    for (int k = 0; k < n * n; ++k) {
+        if (!isfinite(x[k])) {
+            for (int q = 0; q < n * n; ++q) p[q] = NAN;
+            if (b)
+                for (int q = 0; q < n; ++q) b[q] = NAN;
+            return 1;
+        }
+    }
+    return 0;
+}
+
+/* Log-domain Sinkhorn-Knopp for one n x n token (as sinkhorn_token). */
+static int sinkhorn_token_n(const double *x, double *p, double *bout, int n, double tol,
+                            int32_t max_iters, int32_t *iters)
+{
+    double a[NMAX] = {0}, b[NMAX] = {0}, z[NMAX];
+    if (nonfinite_n(x, p, bout, n)) {
+        if (iters) *iters = 0;
+        return 0;
+    }
+    int converged = 0;
+    int32_t it = 0;
+    while (it < max_iters) {
+        for (int i = 0; i < n; ++i) {
+            for (int j = 0; j < n; ++j) z[j] = x[n * i + j] + b[j];
+            a[i] = -lse_n(z, n, 1);
+        }
+        for (int j = 0; j < n; ++j) {
+            for (int i = 0; i < n; ++i) z[i] = x[n * i + j] + a[i];
+            b[j] = -lse_n(z, n, 1);
+        }
+        ++it;
+        if (tol > 0.0) {
+            double q[NMAX * NMAX];
+            for (int i = 0; i < n; ++i)
+                for (int j = 0; j < n; ++j) q[n * i + j] = exp(x[n * i + j] + a[i] + b[j]);
+            if (marginal_residual_n(q, n) < tol) {
+                converged = 1;
+                break;
+            }
+        }
+    }
+    for (int i = 0; i < n; ++i)
+        for (int j = 0; j < n; ++j) p[n * i + j] = exp(x[n * i + j] + a[i] + b[j]);
+    if (bout)
+        for (int j = 0; j < n; ++j) bout[j] = b[j] - b[n - 1];
+    if (iters) *iters = it;
+    return tol <= 0.0 ? 1 : converged;
+}
+
+int64_t oracle_sinkhorn64_n(const double *X, double *P, double *b, int32_t n, int64_t T,
+                            double tol, int32_t max_iters, int32_t *iters_out)
+{
+    int64_t nonconv = 0;
+    if (T <= 0 || n < 2 || n > NMAX) return 0;
+#pragma omp parallel for schedule(dynamic, 64) reduction(+ : nonconv)
+    for (int64_t t = 0; t < T; ++t) {
+        int32_t it = 0;
+        int ok = sinkhorn_token_n(X + (int64_t)n * n * t, P + (int64_t)n * n * t,
+                                  b ? b + (int64_t)n * t : NULL, n, tol, max_iters, &it);
+        if (!ok) ++nonconv;
+        if (iters_out) iters_out[t] = it;
+    }
+    return nonconv;
+}
+
+/* phi(b), the row softmax p(b) and the gradient colsum(p) - 1, for n x n. */
+static double dual_eval_n(const double *x, const double *b, double *p, double *g, int n)
+{
+    double phi = 0.0;
+    for (int j = 0; j < n; ++j) phi -= b[j];
+    for (int i = 0; i < n; ++i) {
+        double m = -INFINITY;
+        for (int j = 0; j < n; ++j) {
+            double z = x[n * i + j] + b[j];
+            if (z > m) m = z;
+        }
+        double s = 0.0;
+        for (int j = 0; j < n; ++j) {
+            p[n * i + j] = exp(x[n * i + j] + b[j] - m);
+            s += p[n * i + j];
+        }
+        for (int j = 0; j < n; ++j) p[n * i + j] /= s;
+        phi += m + log(s);
+    }
+    for (int j = 0; j < n; ++j) {
+        double c = 0.0;
+        for (int i = 0; i < n; ++i) c += p[n * i + j];
+        g[j] = c - 1.0;
+    }
+    return phi;
+}
+
+/* Hessian of phi on b_0..b_{n-2}: H_jk = sum_i p_ij (delta_jk - p_ik), the
+ * diagonal as p_ij sum_{l != j} p_il (rows of p sum to one). */
+static void dual_hessian_n(const double *p, int n, long double H[NMAX][NMAX])
+{
+    for (int j = 0; j < n - 1; ++j)
+        for (int k = 0; k < n - 1; ++k) {
+            long double h = 0.0L;
+            for (int i = 0; i < n; ++i) {
+                const double *pi = p + n * i;
+                if (j == k) {
+                    long double rest = 0.0L;
+                    for (int l = 0; l < n; ++l)
+                        if (l != j) rest += pi[l];
+                    h += (long double)pi[j] * rest;
+                } else {
+                    h -= (long double)pi[j] * pi[k];
+                }
+            }
+            H[j][k] = h;
+        }
+}
+
+/* Solve H x = r (m = n-1 unknowns) by Cholesky after symmetric diagonal
+ * scaling, in long double.  Returns -1 if H is not numerically positive
+ * definite. */
+static int spd_solve_n(long double H[NMAX][NMAX], const double *r, double *x, int m)
+{
+    long double d[NMAX], L[NMAX][NMAX], y[NMAX], z[NMAX];
+    for (int j = 0; j < m; ++j) {
+        if (!(H[j][j] > 0.0L)) return -1;
+        d[j] = 1.0L / sqrtl(H[j][j]);
+    }
+    for (int j = 0; j < m; ++j) {
+        long double s = d[j] * H[j][j] * d[j];
+        for (int k = 0; k < j; ++k) s -= L[j][k] * L[j][k];
+        if (!(s > 0.0L)) return -1;
+        L[j][j] = sqrtl(s);
+        for (int i = j + 1; i < m; ++i) {
+            long double t = d[i] * H[i][j] * d[j];
+            for (int k = 0; k < j; ++k) t -= L[i][k] * L[j][k];
+            L[i][j] = t / L[j][j];
+        }
+    }
+    for (int j = 0; j < m; ++j) {
+        long double s = d[j] * r[j];
+        for (int k = 0; k < j; ++k) s -= L[j][k] * y[k];
+        y[j] = s / L[j][j];
+    }
+    for (int j = m - 1; j >= 0; --j) {
+        long double s = y[j];
+        for (int k = j + 1; k < m; ++k) s -= L[k][j] * z[k];
+        z[j] = s / L[j][j];
+    }
+    for (int j = 0; j < m; ++j) x[j] = (double)(d[j] * z[j]);
+    return 0;
+}
+
+/* Newton with Armijo backtracking for one n x n token (as newton_token). */
+static int newton_token_n(const double *x, double *pout, double *bout, int n, double tol,
+                          int32_t max_iters, int32_t *iters)
+{
+    double b[NMAX] = {0}, p[NMAX * NMAX], g[NMAX];
+    double best_p[NMAX * NMAX], best_b[NMAX], best_res = INFINITY;
+    int32_t best_k = 0, since_best = 0;
+    if (nonfinite_n(x, pout, bout, n)) {
+        if (iters) *iters = 0;
+        return 0;
+    }
+    double phi = dual_eval_n(x, b, p, g, n);
+    int32_t k = 0;
+    for (;;) {
+        double res = marginal_residual_n(p, n);
+        if (k == 0 || res < best_res) {
+            best_res = res;
+            memcpy(best_p, p, sizeof(double) * n * n);
+            memcpy(best_b, b, sizeof(double) * n);
+            best_k = k;
+            since_best = 0;
+        } else {
+            ++since_best;
+        }
+        if (res <= tol || k >= max_iters || isnan(res)) break;
+        if (since_best >= 8 && best_res < 1e-10) break;
+        long double H[NMAX][NMAX];
+        double step[NMAX];
+        dual_hessian_n(p, n, H);
+        if (spd_solve_n(H, g, step, n - 1) != 0)
+            for (int j = 0; j < n - 1; ++j) step[j] = g[j];
+        double smax = 0.0;
+        for (int j = 0; j < n - 1; ++j) smax = fmax(smax, fabs(step[j]));
+        if (smax > 32.0)
+            for (int j = 0; j < n - 1; ++j) step[j] *= 32.0 / smax;
+        double slope = 0.0;
+        for (int j = 0; j < n - 1; ++j) slope += g[j] * step[j];
+        double t = 1.0, bn[NMAX], pn[NMAX * NMAX], gn[NMAX], phin = phi;
+        int accepted = 0;
+        for (int ls = 0; ls < 60; ++ls) {
+            for (int j = 0; j < n - 1; ++j) bn[j] = b[j] - t * step[j];
+            bn[n - 1] = 0.0;
+            phin = dual_eval_n(x, bn, pn, gn, n);
+            if (phin <= phi - 1e-4 * t * slope) {
+                accepted = 1;
+                break;
+            }
+            if (t * slope <= 1e-12 * (fabs(phi) + 1.0) && marginal_residual_n(pn, n) < res) {
+                accepted = 1;
+                break;
+            }
+            t *= 0.5;
+        }
+        ++k;
+        if (!accepted) break;
+        memcpy(b, bn, sizeof(double) * n);
+        memcpy(p, pn, sizeof(double) * n * n);
+        memcpy(g, gn, sizeof(double) * n);
+        phi = phin;
+    }
+    memcpy(pout, best_p, sizeof(double) * n * n);
+    if (bout) memcpy(bout, best_b, sizeof(double) * n);
+    if (iters) *iters = best_k;
+    return best_res <= tol;
+}
+
+int64_t oracle_newton64_n(const double *X, double *P, double *b, int32_t n, int64_t T, double tol,
+                          int32_t max_iters, int32_t *iters_out)
+{
+    int64_t nonconv = 0;
+    if (T <= 0 || n < 2 || n > NMAX) return 0;
+#pragma omp parallel for schedule(dynamic, 64) reduction(+ : nonconv)
+    for (int64_t t = 0; t < T; ++t) {
+        int32_t it = 0;
+        int ok = newton_token_n(X + (int64_t)n * n * t, P + (int64_t)n * n * t,
+                                b ? b + (int64_t)n * t : NULL, n, tol, max_iters, &it);
+        if (!ok) ++nonconv;
+        if (iters_out) iters_out[t] = it;
+    }
+    return nonconv;
+}
+
+/* Implicit-function-theorem backward for one n x n token (as backward_token,
+ * same difference forms, Cholesky solve). */
+static void backward_token_n(const double *pin, const double *G, double *dX, int n)
+{
+    double p[NMAX * NMAX], D[NMAX * NMAX], v[NMAX], lam[NMAX];
+    for (int k = 0; k < n; ++k) {
+        double s = 0.0;
+        for (int j = 0; j < n; ++j) s += pin[n * k + j];
+        for (int j = 0; j < n; ++j) p[n * k + j] = pin[n * k + j] / s;
+    }
+    for (int k = 0; k < n; ++k)
+        for (int l = 0; l < n; ++l) {
+            double d = 0.0;
+            for (int j = 0; j < n; ++j)
+                if (j != l) d += p[n * k + j] * (G[n * k + l] - G[n * k + j]);
+            D[n * k + l] = d;
+        }
+    for (int l = 0; l < n - 1; ++l) {
+        double s = 0.0;
+        for (int k = 0; k < n; ++k) s += p[n * k + l] * D[n * k + l];
+        v[l] = s;
+    }
+    long double H[NMAX][NMAX];
+    dual_hessian_n(p, n, H);
+    if (spd_solve_n(H, v, lam, n - 1) != 0)
+        for (int l = 0; l < n - 1; ++l) lam[l] = NAN;
+    lam[n - 1] = 0.0;
+    for (int k = 0; k < n; ++k)
+        for (int q = 0; q < n; ++q) {
+            double c = 0.0;
+            for (int l = 0; l < n; ++l)
+                if (l != q) c += p[n * k + l] * (lam[q] - lam[l]);
+            dX[n * k + q] = p[n * k + q] * (D[n * k + q] - c);
+        }
+}
+
+void oracle_backward64_n(const double *P, const double *G, double *dX, int32_t n, int64_t T)
+{
+    if (T <= 0 || n < 2 || n > NMAX) return;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        backward_token_n(P + (int64_t)n * n * t, G + (int64_t)n * n * t, dX + (int64_t)n * n * t, n);
+}
