@@ -228,10 +228,12 @@ def main():
                     help="throughput sweep T = 2^12..2^26, sigma 1 and 10 (one JSON line each)")
     ap.add_argument("--mhc", action="store_true",
                     help="bf16 mHC batch [64,32,8192,4,4]: fused and separate passes")
+    ap.add_argument("--nxn", action="store_true",
+                    help="n x n kernels, n = 2..8, 1 GiB of fp32 X per n (one JSON line each)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
-    if args.sweep or args.mhc:
+    if args.sweep or args.mhc or args.nxn:
         return run_extra(args)
 
     import numpy as np
@@ -373,7 +375,8 @@ def time_device(fn, reps, dev):
 
 
 def run_extra(args):
-    """Extra measurement lines: the throughput sweep and the bf16 mHC batch."""
+    """Extra measurement lines: the throughput sweep, the bf16 mHC batch and
+    the n x n kernels."""
     import torch
 
     import birkhoff_projection_gb300 as b4
@@ -443,6 +446,27 @@ def run_extra(args):
                           "separate_ms": tsep, "separate_tokens_per_s": T / (tsep * 1e-3),
                           "separate_gbs": 160 * T / (tsep * 1e-3) / 1e9,
                           "fwd_ms": tf, "fwd_gbs": 64 * T / (tf * 1e-3) / 1e9}), flush=True)
+    if args.nxn:
+        peak, peak_kind = hbm_peak()
+        for n in range(2, 9):
+            T = (1 << 28) // (n * n)  # 1 GiB of fp32 X
+            g = torch.Generator(device=dev).manual_seed(11 + n)
+            X = torch.randn(T, n, n, device=dev, generator=g)
+            G = torch.randn(T, n, n, device=dev, generator=g)
+            P = torch.empty_like(X)
+            dX = torch.empty_like(X)
+            tf = time_device(lambda i: b4.forward_nxn(X, out=P), 10, dev)
+            tb = time_device(lambda i: b4.backward_nxn(G, P=P, out=dX), 10, dev)
+            fw_gbs = 8 * n * n * T / (tf * 1e-3) / 1e9
+            bw_gbs = 12 * n * n * T / (tb * 1e-3) / 1e9
+            print(json.dumps({"nxn": n, "tokens": T, "sigma": 1.0, "fwd_ms": tf, "bwd_ms": tb,
+                              "fwd_tokens_per_s": T / (tf * 1e-3),
+                              "bwd_tokens_per_s": T / (tb * 1e-3),
+                              "fwd_gbs": fw_gbs, "bwd_gbs": bw_gbs,
+                              "hbm_peak_gbs": peak, "peak_kind": peak_kind,
+                              "fwd_frac": fw_gbs / peak, "bwd_frac": bw_gbs / peak}), flush=True)
+            del X, G, P, dX
+            torch.cuda.empty_cache()
 
 
 def ctypes_probe(b4, dev):

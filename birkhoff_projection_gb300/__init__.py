@@ -24,7 +24,7 @@ from . import _lib
 from ._lib import B4_BF16, B4_F32, Birkhoff4Error, Opts, check, lib
 
 __all__ = ["project", "forward", "backward", "forward_backward", "forward_backward_host",
-           "sinkhorn", "Birkhoff4Error", "lib", "Projection"]
+           "forward_nxn", "backward_nxn", "sinkhorn", "Birkhoff4Error", "lib", "Projection"]
 
 _DT = {torch.float32: B4_F32, torch.bfloat16: B4_BF16}
 
@@ -206,6 +206,45 @@ def host_workspace(device, dtype, chunk_tokens: int = 1 << 22, nstreams: int = 3
     return torch.empty(nstreams * 4 * chunk_tokens * rb, dtype=torch.uint8, device=device)
 
 
+def _check_nxn(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != torch.float32:
+        raise TypeError("%s must be float32 for n x n tokens" % name)
+    if t.dim() < 2 or t.shape[-1] != t.shape[-2] or not (2 <= t.shape[-1] <= 8):
+        raise ValueError("%s must have shape [..., n, n] with 2 <= n <= 8" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    n = t.shape[-1]
+    return n, t.numel() // (n * n)
+
+
+def forward_nxn(X: torch.Tensor, *, out: torch.Tensor = None, return_dual: bool = False):
+    """Projection of n x n tokens X [..., n, n] (fp32, 2 <= n <= 8)."""
+    n, T = _check_nxn(X, "X")
+    if out is None:
+        out = torch.empty_like(X)
+    b = torch.empty(X.shape[:-1], dtype=torch.float32, device=X.device) if return_dual else None
+    with _on_device(X):
+        check(lib().birkhoff4_forward_nxn(_ptr(X), _ptr(out), _ptr(b), n, T, _stream(X)),
+              "birkhoff4_forward_nxn")
+    return (out, b) if return_dual else out
+
+
+def backward_nxn(dP: torch.Tensor, *, P: torch.Tensor, out: torch.Tensor = None) -> torch.Tensor:
+    """Implicit-differentiation backward for n x n tokens."""
+    n, T = _check_nxn(dP, "dP")
+    _check_nxn(P, "P")
+    if P.shape != dP.shape:
+        raise ValueError("P and dP must match")
+    if out is None:
+        out = torch.empty_like(dP)
+    with _on_device(dP):
+        check(lib().birkhoff4_backward_nxn(_ptr(P), _ptr(dP), _ptr(out), n, T, _stream(dP)),
+              "birkhoff4_backward_nxn")
+    return out
+
+
 class Projection(torch.autograd.Function):
     """P = project(X); the backward is the implicit-differentiation kernel
     applied to the saved P (nothing of the forward iteration is stored)."""
@@ -213,16 +252,19 @@ class Projection(torch.autograd.Function):
     @staticmethod
     def forward(ctx, X):
         Xc = X.contiguous()
-        P = forward(Xc)
+        P = forward(Xc) if X.shape[-1] == 4 else forward_nxn(Xc)
         ctx.save_for_backward(P)
         return P
 
     @staticmethod
     def backward(ctx, dP):
         (P,) = ctx.saved_tensors
-        return backward(dP.contiguous().to(P.dtype), P=P)
+        dP = dP.contiguous().to(P.dtype)
+        return backward(dP, P=P) if P.shape[-1] == 4 else backward_nxn(dP, P=P)
 
 
 def project(X: torch.Tensor) -> torch.Tensor:
-    """Differentiable per-token Birkhoff projection of X [..., 4, 4]."""
+    """Differentiable per-token Birkhoff projection of X [..., n, n]
+    (n = 4: fp32 or bf16 through the 4 x 4 kernels; 2 <= n <= 8 fp32 through
+    the n x n kernels)."""
     return Projection.apply(X)

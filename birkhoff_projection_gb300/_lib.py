@@ -33,6 +33,8 @@ SIGNATURES = {
                                                ctypes.c_size_t, _vp, ctypes.c_int32]),
     "birkhoff4_forward_backward_host_static": (_int, [_vp, _vp, _vp, _vp, _i64, ctypes.c_int32,
                                                       _i64, _vp, ctypes.c_int32]),
+    "birkhoff4_forward_nxn": (_int, [_vp, _vp, _vp, ctypes.c_int32, _i64, _vp]),
+    "birkhoff4_backward_nxn": (_int, [_vp, _vp, _vp, ctypes.c_int32, _i64, _vp]),
     "birkhoff4_sinkhorn": (_int, [_vp, _vp, _int, _i64, _vp]),
     "birkhoff4_sinkhorn_bf16": (_int, [_vp, _vp, _int, _i64, _vp]),
     "birkhoff4_strerror": (ctypes.c_char_p, [_int]),

@@ -1,0 +1,319 @@
+// b4_nxn.cuh -- the projection for n x n tokens (2 <= n <= 8), one thread per
+// token: Newton on the dual reduced to n-1 free variables and the
+// implicit-differentiation backward ("Accelerating the Birkhoff Projection
+// for Manifold-Constrained Hyper-Connections", s2.1: m-1 free variables for
+// m columns; s2.2).  The same iteration as the 4 x 4 kernels (column-mean
+// start, row-max-shifted first evaluation, multiplicative re-evaluation with
+// a log-domain refresh every 8 steps, Laplacian-form Hessian and elimination,
+// step clamp 3 with Newton-decrement damping from the fifth step), written
+// for any n.  Tokens are staged through shared memory with plain coalesced
+// loads: n x n rows of n^2 * 4 bytes are not all multiples of 16 bytes, which
+// TMA tiles need.
+#pragma once
+
+#include "b4_device.cuh"
+#include "b4_types.h"
+
+namespace b4 {
+
+template <int N>
+struct NxnShape {
+  static constexpr int NN = N * N;
+  // row stride of a token in shared memory: odd, so that lanes reading the
+  // same element of consecutive tokens hit different banks
+  static constexpr int STRIDE = (NN % 2 == 0) ? NN + 1 : NN;
+};
+
+constexpr float kNxnRidge = 1e-7f;
+constexpr float kNxnClamp = 3.0f;
+constexpr int kNxnDampFrom = 4;
+
+// Row softmax of (x log2e + beta), rows shifted by their maximum; x is the
+// token's row in shared memory.
+template <int N>
+__device__ __forceinline__ void nxn_eval_log(const float* xs, const float beta[N], float p[N * N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float z[N];
+    float m = -3.0e38f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      z[j] = fmaf(xs[N * i + j], LOG2E, beta[j]);
+      m = fmaxf(m, z[j]);
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      z[j] = ex2(z[j] - m);
+      s += z[j];
+    }
+    const float r = rcp(s);
+#pragma unroll
+    for (int j = 0; j < N; ++j) p[N * i + j] = z[j] * r;
+  }
+}
+
+// The row softmax after beta_j -= d_j, from the previous row-normalised p.
+template <int N>
+__device__ __forceinline__ void nxn_eval_mul(float p[N * N], const float d[N - 1]) {
+  float w[N];
+#pragma unroll
+  for (int j = 0; j < N - 1; ++j) w[j] = ex2(-d[j]);
+  w[N - 1] = 1.0f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      p[N * i + j] *= w[j];
+      s += p[N * i + j];
+    }
+    const float r = rcp(s);
+#pragma unroll
+    for (int j = 0; j < N; ++j) p[N * i + j] *= r;
+  }
+}
+
+// Laplacian edge weights w[j][k] = sum_i p_ij p_ik (+ base) for j < k.
+template <int N>
+__device__ __forceinline__ void nxn_weights(const float p[N * N], float w[N][N], float base) {
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+#pragma unroll
+    for (int k = j + 1; k < N; ++k) {
+      float s = base;
+#pragma unroll
+      for (int i = 0; i < N; ++i) s = fmaf(p[N * i + j], p[N * i + k], s);
+      w[j][k] = s;
+    }
+}
+
+// Solve H x = g for the Laplacian of w with column N-1 grounded (N-1
+// unknowns), by elimination in Laplacian form: eliminating column a adds
+// w_aj w_ak / d_a to the remaining weights, so every pivot is a sum of
+// positive terms.  w is overwritten.
+template <int N>
+__device__ __forceinline__ void nxn_solve(float w[N][N], const float g[N - 1], float x[N - 1]) {
+  float gg[N - 1], inv[N - 1];
+#pragma unroll
+  for (int j = 0; j < N - 1; ++j) gg[j] = g[j];
+#pragma unroll
+  for (int a = 0; a < N - 1; ++a) {
+    float d = 0.0f;
+#pragma unroll
+    for (int k = a + 1; k < N; ++k) d += w[a][k];
+    inv[a] = rcp(fmaxf(d, 1e-30f));
+#pragma unroll
+    for (int j = a + 1; j < N; ++j) {
+      const float t = w[a][j] * inv[a];
+      if (j < N - 1) gg[j] = fmaf(t, gg[a], gg[j]);
+#pragma unroll
+      for (int k = j + 1; k < N; ++k) w[j][k] = fmaf(t, w[a][k], w[j][k]);
+    }
+  }
+#pragma unroll
+  for (int a = N - 2; a >= 0; --a) {
+    float s = gg[a];
+#pragma unroll
+    for (int j = a + 1; j < N - 1; ++j) s = fmaf(w[a][j], x[j], s);
+    x[a] = s * inv[a];
+  }
+}
+
+// Forward solve of one n x n token; xs is its row in shared memory (read at
+// the start and by the periodic refresh).  beta[N-1] = 0 (base 2).
+template <int N>
+__device__ __forceinline__ bool nxn_newton(const float* xs, float p[N * N], float beta[N],
+                                           int& evals, const NewtonCfg& cfg) {
+  float cs[N];
+  float all = 0.0f;
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) s += xs[N * i + j];
+    cs[j] = s;
+    all += s;
+  }
+  if (!isfinite(all)) {
+    const float nan = __int_as_float(0x7fffffff);
+#pragma unroll
+    for (int k = 0; k < N * N; ++k) p[k] = nan;
+#pragma unroll
+    for (int j = 0; j < N; ++j) beta[j] = nan;
+    evals = 0;
+    return false;
+  }
+  // column-mean start b_j = -(mean_i X_ij - mean_i X_i,N-1)
+#pragma unroll
+  for (int j = 0; j < N; ++j) beta[j] = (cs[N - 1] - cs[j]) * (LOG2E / N);
+  nxn_eval_log<N>(xs, beta, p);
+  evals = 1;
+  float prev = 3.0e38f;
+  for (int k = 0;; ++k) {
+    float g[N];
+    float res = 0.0f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      float s = 0.0f;
+#pragma unroll
+      for (int i = 0; i < N; ++i) s += p[N * i + j];
+      g[j] = s - 1.0f;
+      res = fmaxf(res, fabsf(g[j]));
+    }
+    const bool stop = (res <= cfg.tol) || (res <= 64.0f * cfg.tol && res > 0.5f * prev);
+    if (stop) return true;
+    if (evals >= cfg.max_evals) return false;
+    prev = res;
+    float w[N][N], d[N - 1];
+    nxn_weights<N>(p, w, kNxnRidge);
+    nxn_solve<N>(w, g, d);
+    float lim = 1.0f;
+    if (k >= kNxnDampFrom) {
+      float lam2 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < N - 1; ++j) lam2 = fmaf(g[j], d[j], lam2);
+      if (lam2 > 1.0f) lim = rcp(1.0f + lam2 * rsqrt(lam2));
+    }
+    float dmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < N - 1; ++j) dmax = fmaxf(dmax, fabsf(d[j]));
+    const float scale = LOG2E * fminf(lim, kNxnClamp * rcp(dmax));
+#pragma unroll
+    for (int j = 0; j < N - 1; ++j) {
+      d[j] *= scale;
+      beta[j] -= d[j];
+    }
+    if ((k & 7) == 7)
+      nxn_eval_log<N>(xs, beta, p);
+    else
+      nxn_eval_mul<N>(p, d);
+    ++evals;
+  }
+}
+
+// Backward of one n x n token [s2.2], the difference forms of the 4 x 4
+// kernel: D_kl = sum_j p_kj (G_kl - G_kj), v_l = sum_k p_kl D_kl,
+// H lambda = v (lambda_{N-1} = 0, ridge 1e-7 max w),
+// dX_kq = p_kq (D_kq - sum_l p_kl (lambda_q - lambda_l)).  G is the token's
+// row in shared memory; dx may alias nothing else.
+template <int N>
+__device__ __forceinline__ void nxn_backward(const float pin[N * N], const float* Gs, float dx[N * N]) {
+  float p[N * N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) s += pin[N * k + j];
+    const float r = rcp(s);
+#pragma unroll
+    for (int j = 0; j < N; ++j) p[N * k + j] = pin[N * k + j] * r;
+  }
+  // D in dx
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+#pragma unroll
+    for (int l = 0; l < N; ++l) {
+      float s = 0.0f;
+#pragma unroll
+      for (int j = 0; j < N; ++j)
+        if (j != l) s = fmaf(p[N * k + j], Gs[N * k + l] - Gs[N * k + j], s);
+      dx[N * k + l] = s;
+    }
+  float v[N - 1];
+#pragma unroll
+  for (int l = 0; l < N - 1; ++l) {
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < N; ++k) s = fmaf(p[N * k + l], dx[N * k + l], s);
+    v[l] = s;
+  }
+  float w[N][N];
+  nxn_weights<N>(p, w, 0.0f);
+  float wmax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+#pragma unroll
+    for (int k = j + 1; k < N; ++k) wmax = fmaxf(wmax, w[j][k]);
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+#pragma unroll
+    for (int k = j + 1; k < N; ++k) w[j][k] = fmaf(1e-7f, wmax, w[j][k]);
+  float lam[N];
+  nxn_solve<N>(w, v, lam);
+  lam[N - 1] = 0.0f;
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+      float c = 0.0f;
+#pragma unroll
+      for (int l = 0; l < N; ++l)
+        if (l != q) c = fmaf(p[N * k + l], lam[q] - lam[l], c);
+      dx[N * k + q] = p[N * k + q] * (dx[N * k + q] - c);
+    }
+}
+
+struct NxnParams {
+  const float* in0;  // X (forward) or P (backward)
+  const float* in1;  // dP (backward)
+  float* out;        // P (forward) or dX (backward)
+  float* b;          // forward: optional [T, N] dual
+  int64_t T;
+  NewtonCfg cfg;
+};
+
+// Persistent kernel over tiles of TILE tokens: coalesced copy into shared
+// memory, per-token compute, coalesced copy out.
+template <int N, int TILE, bool FWD>
+__global__ void __launch_bounds__(TILE) nxn_kernel(const NxnParams a) {
+  using S = NxnShape<N>;
+  extern __shared__ float sm[];
+  float* s0 = sm;                     // X or P tile, reused for the output
+  float* s1 = sm + TILE * S::STRIDE;  // dP tile (backward)
+  const int tid = threadIdx.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * TILE; base < a.T;
+       base += static_cast<int64_t>(gridDim.x) * TILE) {
+    const int64_t left = a.T - base;
+    const int ntok = left < TILE ? static_cast<int>(left) : TILE;
+    const int nel = ntok * S::NN;
+    const float* g0 = a.in0 + base * S::NN;
+    for (int i = tid; i < nel; i += TILE) s0[(i / S::NN) * S::STRIDE + i % S::NN] = __ldg(g0 + i);
+    if constexpr (!FWD) {
+      const float* g1 = a.in1 + base * S::NN;
+      for (int i = tid; i < nel; i += TILE) s1[(i / S::NN) * S::STRIDE + i % S::NN] = __ldg(g1 + i);
+    }
+    __syncthreads();
+    float out[S::NN];
+    const bool valid = tid < ntok;
+    if (valid) {
+      if constexpr (FWD) {
+        float beta[N];
+        int evals = 0;
+        nxn_newton<N>(s0 + tid * S::STRIDE, out, beta, evals, a.cfg);
+        if (a.b != nullptr) {
+          float* bp = a.b + (base + tid) * N;
+#pragma unroll
+          for (int j = 0; j < N - 1; ++j) bp[j] = beta[j] * LN2;
+          bp[N - 1] = 0.0f;
+        }
+      } else {
+        float pin[S::NN];
+#pragma unroll
+        for (int e = 0; e < S::NN; ++e) pin[e] = s0[tid * S::STRIDE + e];
+        nxn_backward<N>(pin, s1 + tid * S::STRIDE, out);
+      }
+    }
+    __syncthreads();  // every token's inputs have been read
+    if (valid) {
+#pragma unroll
+      for (int e = 0; e < S::NN; ++e) s0[tid * S::STRIDE + e] = out[e];
+    }
+    __syncthreads();
+    float* go = a.out + base * S::NN;
+    for (int i = tid; i < nel; i += TILE) go[i] = s0[(i / S::NN) * S::STRIDE + i % S::NN];
+    __syncthreads();  // the tile is free for the next load
+  }
+}
+
+}  // namespace b4

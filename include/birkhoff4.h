@@ -150,6 +150,21 @@ int birkhoff4_forward_backward_bf16(const uint16_t *X, const uint16_t *dP, uint1
                                     uint16_t *dX, int64_t T, birkhoff4_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* General n x n tokens, 2 <= n <= 8 [mHC s2.1: the dual reduces to m-1    */
+/* free variables for m columns; s2.2].  The same forward iteration (b     */
+/* gauge b[n-1] = 0, tolerance 1e-6, cap 48) and backward as above, for    */
+/* [T, n, n] row-major fp32 arrays (element (t,i,j) at n*n*t + n*i + j);  */
+/* b: NULL or [T, n].  Tokens are staged through shared memory with plain  */
+/* loads (n^2 * 4-byte rows are not all TMA-aligned); no alignment         */
+/* requirement beyond 4 bytes.  In place (P == X, dX == dP) is allowed.    */
+/* n outside 2..8 returns B4_EINVAL.                                       */
+/* ---------------------------------------------------------------------- */
+int birkhoff4_forward_nxn(const float *X, float *P, float *b, int32_t n, int64_t T,
+                          birkhoff4_stream_t stream);
+int birkhoff4_backward_nxn(const float *P, const float *dP, float *dX, int32_t n, int64_t T,
+                           birkhoff4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* Host-resident tokens [mHC s2.1, s2.2; batched as in s2.3]: forward and  */
 /* backward of tokens that live in host memory, streamed through the GPU.  */
 /*                                                                        */

@@ -19,20 +19,22 @@ TOL_DX_REL = 1e-4
 
 
 def np64(t) -> np.ndarray:
-    """Tensor (any device/dtype) -> float64 numpy [..., 4, 4] copy."""
+    """Tensor (any device/dtype) -> float64 numpy copy of the same shape."""
     return t.detach().to("cpu", torch.float64).numpy()
 
 
 def residual(P) -> np.ndarray:
-    """Per-token max(|P 1 - 1|_inf, |P^T 1 - 1|_inf), float64."""
-    p = np.asarray(P, dtype=np.float64).reshape(-1, 4, 4)
+    """Per-token max(|P 1 - 1|_inf, |P^T 1 - 1|_inf) of [..., n, n] tokens,
+    float64."""
+    p = np.asarray(P, dtype=np.float64)
+    p = p.reshape(-1, p.shape[-1], p.shape[-1])
     return np.maximum(np.abs(p.sum(2) - 1).max(1), np.abs(p.sum(1) - 1).max(1))
 
 
 def residual_gpu(P: torch.Tensor) -> torch.Tensor:
     """The same residual computed on the device in float64 (for arrays too
     large to copy back)."""
-    p = P.reshape(-1, 4, 4).double()
+    p = P.reshape(-1, P.shape[-1], P.shape[-1]).double()
     return torch.maximum((p.sum(2) - 1).abs().amax(1), (p.sum(1) - 1).abs().amax(1))
 
 

@@ -69,6 +69,20 @@ def test_null_pointers_are_einval(L):
     assert L.birkhoff4_sinkhorn_bf16(FAKE, None, 20, 4, None) == _lib.B4_EINVAL
 
 
+def test_nxn_arguments_are_checked(L):
+    for n in (1, 9, 0, -3):
+        assert L.birkhoff4_forward_nxn(FAKE, FAKE, None, n, 4, None) == _lib.B4_EINVAL
+        assert L.birkhoff4_backward_nxn(FAKE, FAKE, FAKE, n, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_forward_nxn(FAKE, FAKE, None, 5, -1, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_forward_nxn(None, FAKE, None, 5, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_forward_nxn(FAKE, None, None, 5, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_backward_nxn(None, FAKE, FAKE, 5, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_backward_nxn(FAKE, None, FAKE, 5, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_backward_nxn(FAKE, FAKE, None, 5, 4, None) == _lib.B4_EINVAL
+    assert L.birkhoff4_forward_nxn(None, None, None, 5, 0, None) == _lib.B4_OK
+    assert L.birkhoff4_backward_nxn(None, None, None, 8, 0, None) == _lib.B4_OK
+
+
 def test_bad_options_are_einval(L):
     def opts(**kw):
         o = _lib.Opts(in_dtype=0, out_dtype=0, max_evals=0, tol=0.0)
