@@ -15,6 +15,12 @@ Workloads (all tokens are [4,4] row-major; T = number of tokens):
                    s ~ N(0,1) per token (diagonal bias); dP bf16 N(0,1), seed 3
   sweep            T = 2^12 ... 2^26, X fp32 iid N(0, sigma^2),
                    sigma in {1, 10}, seed 4
+
+Point clouds for streaming entropic OT (n x d and m x d, fp32):
+  eot_clouds       X rows iid N(0, I_d / d); Y rows iid N(0, I_d / d) shifted
+                   by 0.5 along the first axis (so ||x - y||^2 is about 2.25
+                   for any d); weights uniform, or with random=True drawn
+                   U[0.2, 1] and normalised; seed 100 + seed
 """
 from __future__ import annotations
 
@@ -133,3 +139,26 @@ def fixed_point_family_n(n: int, T: int, seed: int, spread: float = 5.0, floor: 
     v = (torch.rand(T, 1, n, generator=g, device=device, dtype=torch.float64) * 2 - 1) * spread
     x = torch.log(q) + u + v
     return x.to(dtype), q
+
+
+EOT_SIZES = {"small": (1000, 1500), "bench": (65536, 65536)}
+EOT_DIMS = (64, 512)
+EOT_EPS = 0.1
+
+
+def eot_clouds(n: int, m: int, d: int, seed: int = 0, device="cpu", random_weights: bool = False):
+    """(X [n,d], Y [m,d], log_a [n], log_b [m]) fp32 point clouds and log
+    weights (see the module docstring)."""
+    g = _gen(100 + seed, device)
+    X = torch.randn(n, d, generator=g, device=device) * (1.0 / d ** 0.5)
+    Y = torch.randn(m, d, generator=g, device=device) * (1.0 / d ** 0.5)
+    Y[:, 0] += 0.5
+    if random_weights:
+        a = torch.rand(n, generator=g, device=device) * 0.8 + 0.2
+        b = torch.rand(m, generator=g, device=device) * 0.8 + 0.2
+        log_a = torch.log(a / a.sum())
+        log_b = torch.log(b / b.sum())
+    else:
+        log_a = torch.full((n,), -float(torch.log(torch.tensor(float(n)))), device=device)
+        log_b = torch.full((m,), -float(torch.log(torch.tensor(float(m)))), device=device)
+    return X.contiguous(), Y.contiguous(), log_a, log_b
