@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libbirkhoff4.so")
 
 SOURCES = ["birkhoff4_api.cu", "k_forward.cu", "k_backward.cu", "k_fused.cu", "k_sinkhorn.cu",
-           "birkhoff4_noalloc.cu", "k_nxn.cu"]
+           "birkhoff4_noalloc.cu", "k_nxn.cu", "eot_stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I", CSRC, "-I", INCLUDE]
@@ -33,7 +33,7 @@ def nvcc() -> str:
 
 def _inputs():
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    deps += [os.path.join(INCLUDE, "birkhoff4.h"), os.path.abspath(__file__)]
+    deps += [os.path.join(INCLUDE, h) for h in os.listdir(INCLUDE)] + [os.path.abspath(__file__)]
     return deps
 
 

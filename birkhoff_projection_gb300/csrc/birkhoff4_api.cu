@@ -225,6 +225,10 @@ __global__ void selftest_wait_kernel(unsigned int* fault, uint64_t limit_ns) {
 // units of the library) and returns B4_ECUDA (B4_OK for cudaSuccess).
 int record_cuda_error(cudaError_t e) { return cuda_status(e); }
 
+// The fault latch's device address for kernels launched from other
+// translation units (bounded waits that run out set bits in it).
+unsigned int* device_fault_latch(cudaError_t* err) { return fault_latch(err); }
+
 }  // namespace b4
 
 using namespace b4;

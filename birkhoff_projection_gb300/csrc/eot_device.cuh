@@ -1,0 +1,126 @@
+// eot_device.cuh -- inline PTX for the 5th-generation tensor cores (tcgen05:
+// tensor-memory allocation, MMA issue and commit, tensor-memory loads) and
+// the shared-memory matrix descriptors used by the streaming entropic-OT
+// kernel.  Written from the PTX ISA's description of tcgen05.
+#pragma once
+
+#include <cstdint>
+
+#include "b4_device.cuh"
+
+namespace eot {
+
+// ---------------------------------------------------------------------------
+// Tensor memory (TMEM): 128 lanes x 512 columns of 32 bits per SM.
+// alloc / relinquish / dealloc are executed by all 32 lanes of one warp.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   b4::smem_addr(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Order tcgen05 operations against thread synchronisation (barriers,
+// mbarrier arrive/wait) in the issuing thread.
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// MMA: D[tmem] = A * B^T (+ D if accumulate), A = M x K and B = N x K, both
+// read from shared memory through matrix descriptors; kind::tf32 (fp32
+// storage, tf32 multiply, fp32 accumulate).  Issued by a single thread.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive (once) on `bar` when every MMA issued so far by this thread has
+// completed (its shared-memory operands read, its TMEM result written).
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          b4::smem_addr(bar))
+      : "memory");
+}
+
+// Instruction descriptor of a kind::tf32 MMA with fp32 accumulation, both
+// operands K-major, shape M x N (M = 128: TMEM lane i holds row i of D).
+template <int M, int N>
+__host__ __device__ constexpr uint32_t idesc_tf32() {
+  static_assert(M == 128, "one-CTA MMA with M = 128 rows");
+  static_assert(N % 16 == 0 && N >= 16 && N <= 256, "N in 16..256, multiple of 16");
+  return (1u << 4)                                  // D format: f32
+         | (2u << 7)                                // A format: tf32
+         | (2u << 10)                               // B format: tf32
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Shared-memory matrix descriptor for a K-major operand stored as rows of
+// 128 bytes (32 fp32) in the 128-byte swizzle pattern that a TMA box of
+// {32 elements, rows} with SWIZZLE_128B writes: 8-row groups of 1024 bytes
+// (the stride between groups), the tile base 1024-byte aligned.  The
+// leading-dimension offset is unused for this layout (one MMA's K extent,
+// 32 bytes, lies inside the 128-byte swizzle row).  Advancing K by 8 tf32
+// elements adds 32 bytes to the start address (2 in the encoded field).
+__device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)     // start address
+         | (static_cast<uint64_t>(1) << 16)                  // leading byte offset (unused)
+         | (static_cast<uint64_t>(1024 >> 4) << 32)          // stride byte offset
+         | (static_cast<uint64_t>(1) << 46)                  // descriptor version
+         | (static_cast<uint64_t>(2) << 61);                 // 128-byte swizzle
+}
+
+// ---------------------------------------------------------------------------
+// TMEM -> registers: this warp's 32 lanes (lane quarter warp % 4) x 32
+// consecutive 32-bit columns starting at taddr; thread t receives lane
+// (32 * (warp % 4) + t).  The wait is in the same statement, so the values
+// are complete when the statement ends.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Round fp32 to the nearest tf32 value (ties away from zero); the 13 low
+// mantissa bits of the result are zero.
+__device__ __forceinline__ float tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b4::smem_addr(bar)) : "memory");
+}
+
+}  // namespace eot

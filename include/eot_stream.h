@@ -1,0 +1,84 @@
+/* eot_stream.h -- streaming entropic optimal transport between point clouds
+ * on one GB300 (part of libbirkhoff4.so).
+ *
+ * Follows "FlashSinkhorn: IO-Aware Entropic OT on GPU", Methodik s1-s2:
+ * the log-domain Sinkhorn update for the quadratic Euclidean cost
+ *
+ *     f_i <- -eps LSE_j[ (g_j - ||x_i - y_j||^2) / eps + log b_j ]
+ *
+ * computed in the pages' attention form (s1, Proposition 1): with
+ * ||x - y||^2 = ||x||^2 + ||y||^2 - 2 x.y the update is
+ *     f_i = ||x_i||^2 - eps LSE_j[ (2 x_i.y_j + g_j - ||y_j||^2) / eps + log b_j ],
+ * a row-wise log-sum-exp of a biased dot-product score matrix.  The n x m
+ * cost matrix is never stored (s2): a CTA keeps 128 query rows and streams
+ * every key tile through shared memory (TMA), the dot products run on the
+ * tensor cores (tcgen05, accumulators in tensor memory), and a running
+ * maximum and sum of exponentials per row stay in registers (online LSE,
+ * row-stationary traversal).
+ *
+ * Arithmetic: point coordinates are rounded to TF32 for the products and
+ * accumulated in fp32 (EOT_TF32), or split x = hi + lo into two TF32 parts
+ * with the products hi.hi + hi.lo + lo.hi (EOT_TF32X3, near-fp32 accuracy,
+ * three MMAs per step).  Norms, biases and the log-sum-exp are fp32.
+ *
+ * Layout: X [n, d], Y [m, d] row-major fp32 (point i at X + i*d); log_a [n],
+ * log_b [m], f [n], g [m] fp32.  All pointers are device memory owned by the
+ * caller; the library allocates nothing.  Work is asynchronous on `stream`.
+ *
+ * Workspace: the clouds are repacked once per call into the workspace (rows
+ * padded to a multiple of 256, coordinates padded with zeros to a multiple of
+ * 32, rounded to TF32), with their squared norms and one bias vector;
+ * eot_workspace_bytes gives the size.  It must be 256-byte aligned.
+ *
+ * Errors (return values, from birkhoff4.h): B4_EINVAL for a NULL pointer with
+ * work to do, n < 0, m < 0, m == 0 < n, d < 1 or d > 16384, eps not a positive
+ * finite number, iters < 0, passes not 1 or 3, more than 2^31 - 512 points,
+ * or a workspace that is too small or misaligned; B4_ECUDA for a launch
+ * error (birkhoff4_last_cuda_error has the code).  n == 0 does nothing.  A
+ * tensor-pipeline wait that runs out (2 s) sets bit 2 of the fault latch
+ * (birkhoff4_device_status) and the kernel returns; it never traps.
+ */
+#ifndef EOT_STREAM_H
+#define EOT_STREAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "birkhoff4.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EOT_TF32 1   /* one TF32 product per coordinate pair */
+#define EOT_TF32X3 3 /* split hi + lo, three TF32 products (near fp32) */
+
+/* Bytes of workspace that eot_sinkhorn / eot_update need for n points
+ * against m points in d dimensions (0 for invalid sizes or passes). */
+size_t eot_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t passes);
+
+/* One potential update [FlashSinkhorn, Methodik s1]:
+ *     out_i = -eps LSE_j[ (h_j - ||xq_i - xk_j||^2) / eps + log_w_j ],
+ * i < nq, j < nk.  Xq [nq, d] are the query points (the side whose potential
+ * is written), Xk [nk, d] the key points, h [nk] the key-side potential,
+ * log_w [nk] the key-side log weights.  The f update is (X, Y, g, log_b);
+ * the g update is (Y, X, f, log_a).  out may not alias the other inputs. */
+int eot_update(const float *Xq, const float *Xk, const float *h, const float *log_w, float *out,
+               int64_t nq, int64_t nk, int32_t d, float eps, int32_t passes, void *workspace,
+               size_t workspace_bytes, birkhoff4_stream_t stream);
+
+/* `iters` alternating Sinkhorn iterations [FlashSinkhorn, Methodik s1]:
+ * each iteration updates f from g (keys Y, weights b), then g from the new f
+ * (keys X, weights a).  f [n] and g [m] hold the starting potentials on
+ * entry (zeros for a cold start) and the result on return.  The clouds are
+ * repacked once per call, not per iteration. */
+int eot_sinkhorn(const float *X, const float *Y, const float *log_a, const float *log_b, float *f,
+                 float *g, int64_t n, int64_t m, int32_t d, float eps, int32_t iters,
+                 int32_t passes, void *workspace, size_t workspace_bytes,
+                 birkhoff4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EOT_STREAM_H */

@@ -1,7 +1,7 @@
 """The C ABI boundary on the host (no GPU needed).
 
-libbirkhoff4.so must load, export every function include/birkhoff4.h
-declares, and reject invalid arguments on the host before any CUDA call
+libbirkhoff4.so must load, export every function include/birkhoff4.h and
+include/eot_stream.h declare, and reject invalid arguments on the host before any CUDA call
 (these checks never touch a device, so they run on a CPU-only machine).
 """
 import ctypes
@@ -13,13 +13,15 @@ import pytest
 from birkhoff_projection_gb300 import _lib
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "birkhoff4.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("birkhoff4.h", "eot_stream.h")]
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(birkhoff4_\w+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:birkhoff4|eot)_\w+)\s*\(", text))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -81,6 +83,42 @@ def test_nxn_arguments_are_checked(L):
     assert L.birkhoff4_backward_nxn(FAKE, FAKE, None, 5, 4, None) == _lib.B4_EINVAL
     assert L.birkhoff4_forward_nxn(None, None, None, 5, 0, None) == _lib.B4_OK
     assert L.birkhoff4_backward_nxn(None, None, None, 8, 0, None) == _lib.B4_OK
+
+
+def test_eot_arguments_are_checked(L):
+    f32 = ctypes.c_float
+    ws = ctypes.c_void_p(0x100000)
+    need = L.eot_workspace_bytes(100, 200, 64, 1)
+    assert need > 0 and L.eot_workspace_bytes(100, 200, 64, 3) > need
+    assert L.eot_workspace_bytes(100, 200, 0, 1) == 0
+    assert L.eot_workspace_bytes(100, 200, 64, 2) == 0
+    assert L.eot_workspace_bytes(-1, 200, 64, 1) == 0
+
+    def upd(nq=100, nk=200, d=64, eps=0.1, passes=1, w=ws, wb=need, ptr=FAKE):
+        return L.eot_update(ptr, FAKE, FAKE, FAKE, FAKE, nq, nk, d, f32(eps), passes, w, wb, None)
+
+    assert upd(eps=0.0) == _lib.B4_EINVAL
+    assert upd(eps=-1.0) == _lib.B4_EINVAL
+    assert upd(eps=float("nan")) == _lib.B4_EINVAL
+    assert upd(eps=float("inf")) == _lib.B4_EINVAL
+    assert upd(passes=2) == _lib.B4_EINVAL
+    assert upd(d=0) == _lib.B4_EINVAL
+    assert upd(nk=0) == _lib.B4_EINVAL
+    assert upd(ptr=None) == _lib.B4_EINVAL
+    assert upd(w=None) == _lib.B4_EINVAL
+    assert upd(w=ctypes.c_void_p(0x100001)) == _lib.B4_EINVAL
+    assert upd(wb=need - 1) == _lib.B4_EINVAL
+    assert upd(nq=0, ptr=None, w=None) == _lib.B4_OK
+
+    def sk(n=100, m=200, iters=3, w=ws, wb=need):
+        return L.eot_sinkhorn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, n, m, 64, f32(0.1), iters, 1,
+                              w, wb, None)
+
+    assert sk(iters=-1) == _lib.B4_EINVAL
+    assert sk(m=0) == _lib.B4_EINVAL
+    assert sk(wb=0) == _lib.B4_EINVAL
+    assert sk(iters=0) == _lib.B4_OK
+    assert sk(n=0, m=0) == _lib.B4_OK
 
 
 def test_bad_options_are_einval(L):

@@ -1,0 +1,141 @@
+"""GPU parity of the streaming entropic-OT kernels (eot_update, eot_sinkhorn)
+against the float64 oracle (oracle/eot.py), through the C ABI.
+
+Tolerance: a per-row bound derived from the kernel's arithmetic.  With
+A_i = max_j sum_k |x_ik y_jk|, N_i = ||x_i||^2, B = max_j ||y_j||^2:
+  * dot products: each coordinate rounded to TF32 (relative 2^-11, so 2^-10
+    per product) for one pass, or represented as hi + lo to 2^-22 with the
+    lo.lo product dropped (2^-20 per product) for the split form; fp32
+    accumulation over d_pad terms (d_pad 2^-23);
+  * squared norms in fp32 (d 2^-23 relative);
+  * biases, the running maximum, ex2 / lg2 and the final combination in fp32
+    (2^-21 relative to every magnitude involved, plus eps 2^-18);
+the log-sum-exp is 1-Lipschitz in the max norm of its arguments, so the
+error of f_i is at most the largest error of an argument in row i, and a
+sequence of updates adds the bounds of its steps.  The tests assert twice
+that bound.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from birkhoff_projection_gb300 import eot, workloads
+from oracle import eot as oeot
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def np64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def row_bound(X, Y, h, log_w, f_ref, eps, passes):
+    """Per-row error bound of one update of the X side against keys Y."""
+    X = np.asarray(X, np.float64)
+    Y = np.asarray(Y, np.float64)
+    d = X.shape[1]
+    d_pad = -(-d // 32) * 32
+    A = (np.abs(X) @ np.abs(Y).T).max(1)
+    N = (X * X).sum(1)
+    B = (Y * Y).sum(1).max()
+    H = np.abs(h).max()
+    W = eps * np.abs(log_w).max()
+    u = 2.0 ** -10 if passes == 1 else 2.0 ** -20
+    t = (2 * (u + d_pad * 2.0 ** -23) * A + d * 2.0 ** -23 * (N + B)
+         + 2.0 ** -21 * (2 * A + H + B + W + np.abs(f_ref) + N) + eps * 2.0 ** -18)
+    return 2.0 * t
+
+
+CASES = [
+    (1000, 1500, 64),
+    (777, 300, 3),
+    (300, 1000, 100),
+    (1, 1, 1),
+    (129, 257, 32),
+    (20000, 300, 8),  # more row blocks than SMs
+    (64, 3000, 520),  # d past one 512-wide span, ragged
+]
+
+
+@pytest.mark.parametrize("passes", [eot.TF32, eot.TF32X3])
+@pytest.mark.parametrize("nq,nk,d", CASES)
+def test_update_parity(nq, nk, d, passes):
+    X, Y, _, log_b = workloads.eot_clouds(nq, nk, d, seed=nq + nk + d, device=DEV, random_weights=True)
+    gen = torch.Generator(device="cpu").manual_seed(d)
+    h = (torch.randn(nk, generator=gen) * 0.3).to(DEV)
+    eps = workloads.EOT_EPS
+    f = eot.update(X, Y, h, log_b, eps, passes=passes)
+    ref = oeot.f_update64(np64(X), np64(Y), np64(h), np64(log_b), eps)
+    err = np.abs(np64(f) - ref)
+    tol = row_bound(np64(X), np64(Y), np64(h), np64(log_b), ref, eps, passes)
+    assert np.all(np.isfinite(np64(f)))
+    assert np.all(err <= tol), (err.max(), tol[err.argmax()])
+
+
+@pytest.mark.parametrize("passes", [eot.TF32, eot.TF32X3])
+def test_split_form_is_near_fp32(passes):
+    """The split form must be far more accurate than one TF32 pass."""
+    X, Y, _, log_b = workloads.eot_clouds(1000, 1500, 256, seed=5, device=DEV)
+    h = torch.zeros(1500, device=DEV)
+    f = eot.update(X, Y, h, log_b, 0.1, passes=passes)
+    ref = oeot.f_update64(np64(X), np64(Y), np64(h), np64(log_b), 0.1)
+    err = np.abs(np64(f) - ref).max()
+    assert err <= (2e-3 if passes == eot.TF32 else 2e-5)
+
+
+@pytest.mark.parametrize("passes", [eot.TF32, eot.TF32X3])
+def test_sinkhorn_parity(passes):
+    n, m, d, K = 500, 700, 16, 5
+    eps = 0.1
+    X, Y, log_a, log_b = workloads.eot_clouds(n, m, d, seed=1, device=DEV, random_weights=True)
+    f, g = eot.sinkhorn(X, Y, log_a, log_b, eps, K, passes=passes)
+    fr, gr = oeot.sinkhorn64(np64(X), np64(Y), np64(log_a), np64(log_b), eps, K)
+    mag = max(np.abs(fr).max(), np.abs(gr).max())
+    tf = row_bound(np64(X), np64(Y), np.full(m, mag), np64(log_b), np.full(n, mag), eps, passes)
+    tg = row_bound(np64(Y), np64(X), np.full(n, mag), np64(log_a), np.full(m, mag), eps, passes)
+    total = 2 * K * max(tf.max(), tg.max())
+    assert np.abs(np64(f) - fr).max() <= total
+    assert np.abs(np64(g) - gr).max() <= total
+
+
+def test_sinkhorn_warm_start_and_zero_iters():
+    X, Y, log_a, log_b = workloads.eot_clouds(300, 400, 8, seed=2, device=DEV)
+    f, g = eot.sinkhorn(X, Y, log_a, log_b, 0.1, 3)
+    f2, g2 = eot.sinkhorn(X, Y, log_a, log_b, 0.1, 0, f=f.clone(), g=g.clone())
+    assert torch.equal(f2, f) and torch.equal(g2, g)
+    # 3 + 2 iterations from a warm start == 5 from cold, up to rounding
+    fa, ga = eot.sinkhorn(X, Y, log_a, log_b, 0.1, 2, f=f.clone(), g=g.clone())
+    fb, gb = eot.sinkhorn(X, Y, log_a, log_b, 0.1, 5)
+    assert torch.allclose(fa, fb, atol=1e-5) and torch.allclose(ga, gb, atol=1e-5)
+
+
+def test_converged_plan_marginals():
+    n, m, d, eps = 600, 800, 4, 0.1
+    X, Y, log_a, log_b = workloads.eot_clouds(n, m, d, seed=3, device=DEV, random_weights=True)
+    f, g = eot.sinkhorn(X, Y, log_a, log_b, eps, 300, passes=eot.TF32X3)
+    P = oeot.plan64(np64(X), np64(Y), np64(f), np64(g), np64(log_a), np64(log_b), eps)
+    a, b = np.exp(np64(log_a)), np.exp(np64(log_b))
+    # columns are exact after a g update up to the fp32 rounding of g / eps
+    assert np.abs(P.sum(0) / b - 1).max() <= 2e-3
+    assert np.abs(P.sum(1) / a - 1).max() <= 2e-2
+
+
+def test_full_size_sampled_rows():
+    """The benchmark's size (65536 x 65536 points, d = 512): sampled rows
+    of one f update against the oracle evaluated row by row."""
+    n = m = 65536
+    d = 512
+    X, Y, _, log_b = workloads.eot_clouds(n, m, d, seed=0, device=DEV)
+    h = torch.zeros(m, device=DEV)
+    for passes in (eot.TF32, eot.TF32X3):
+        f = eot.update(X, Y, h, log_b, workloads.EOT_EPS, passes=passes)
+        rows = np.r_[0, 1, 127, 128, 40000, n - 129, n - 1, np.random.default_rng(0).integers(0, n, 9)]
+        Xs = np64(X[torch.as_tensor(rows, device=DEV)])
+        Yn = np64(Y)
+        ref = oeot.f_update64(Xs, Yn, np.zeros(m), np64(log_b), workloads.EOT_EPS)
+        tol = row_bound(Xs, Yn, np.zeros(m), np64(log_b), ref, workloads.EOT_EPS, passes)
+        assert np.all(np.abs(np64(f)[rows] - ref) <= tol)
+        assert np.all(np.isfinite(np64(f)))
