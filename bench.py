@@ -228,12 +228,14 @@ def main():
                     help="throughput sweep T = 2^12..2^26, sigma 1 and 10 (one JSON line each)")
     ap.add_argument("--mhc", action="store_true",
                     help="bf16 mHC batch [64,32,8192,4,4]: fused and separate passes")
+    ap.add_argument("--eot", action="store_true",
+                    help="streaming entropic OT: n = m = 65536 points, d = 64 and 512, both precisions")
     ap.add_argument("--nxn", action="store_true",
                     help="n x n kernels, n = 2..8, 1 GiB of fp32 X per n (one JSON line each)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
-    if args.sweep or args.mhc or args.nxn:
+    if args.sweep or args.mhc or args.nxn or args.eot:
         return run_extra(args)
 
     import numpy as np
@@ -376,7 +378,7 @@ def time_device(fn, reps, dev):
 
 def run_extra(args):
     """Extra measurement lines: the throughput sweep, the bf16 mHC batch and
-    the n x n kernels."""
+    the n x n kernels, streaming entropic OT."""
     import torch
 
     import birkhoff_projection_gb300 as b4
@@ -446,6 +448,8 @@ def run_extra(args):
                           "separate_ms": tsep, "separate_tokens_per_s": T / (tsep * 1e-3),
                           "separate_gbs": 160 * T / (tsep * 1e-3) / 1e9,
                           "fwd_ms": tf, "fwd_gbs": 64 * T / (tf * 1e-3) / 1e9}), flush=True)
+    if args.eot:
+        run_eot(dev)
     if args.nxn:
         peak, peak_kind = hbm_peak()
         for n in range(2, 9):
@@ -467,6 +471,52 @@ def run_extra(args):
                               "fwd_frac": fw_gbs / peak, "bwd_frac": bw_gbs / peak}), flush=True)
             del X, G, P, dX
             torch.cuda.empty_cache()
+
+
+def tf32_peak():
+    """Dense TF32 tensor peak: the measured bf16 burst peak times the nominal
+    TF32 / BF16 ratio (1.1 / 2.25 PFLOP/s)."""
+    try:
+        with open(PEAKS_PATH) as f:
+            return float(json.load(f)["bf16_tflops"]) * 1.1 / 2.25, "measured bf16 x 1.1/2.25"
+    except (OSError, KeyError, ValueError):
+        return 1900.0 * 1.1 / 2.25, "fallback bf16 x 1.1/2.25"
+
+
+def run_eot(dev):
+    """Streaming EOT lines: time per Sinkhorn iteration (two potential
+    updates) at n = m = 65536, from the difference of 1 + K and 1 iterations
+    (the one-off repacking of the clouds cancels)."""
+    import torch
+
+    from birkhoff_projection_gb300 import eot, workloads
+
+    n, m = workloads.EOT_SIZES["bench"]
+    eps = workloads.EOT_EPS
+    peak, peak_kind = tf32_peak()
+    for d in workloads.EOT_DIMS:
+        X, Y, la, lb = workloads.eot_clouds(n, m, d, seed=0, device=dev)
+        for passes in (eot.TF32, eot.TF32X3):
+            ws = torch.empty(eot.workspace_bytes(n, m, d, passes), dtype=torch.uint8, device=dev)
+            K = 10 if d <= 128 else 4
+            f = torch.zeros(n, device=dev)
+            g = torch.zeros(m, device=dev)
+            t1 = time_device(lambda i: eot.sinkhorn(X, Y, la, lb, eps, 1, passes, f, g, ws), 5, dev)
+            tk = time_device(lambda i: eot.sinkhorn(X, Y, la, lb, eps, 1 + K, passes, f, g, ws), 5, dev)
+            it_ms = (tk - t1) / K
+            upd_ms = it_ms / 2
+            alg = 2.0 * n * m * d / (upd_ms * 1e-3) / 1e12
+            tensor = alg * passes * (-(-d // 32) * 32) / d
+            print(json.dumps({"eot": True, "n": n, "m": m, "d": d, "passes": passes, "eps": eps,
+                              "ms_per_iteration": it_ms, "ms_per_update": upd_ms,
+                              "algorithmic_tflops": alg, "tensor_tflops": tensor,
+                              "tf32_peak_tflops": peak, "peak_kind": peak_kind,
+                              "frac_of_tensor_peak": tensor / peak,
+                              "ex2_per_update": n * m,
+                              "f_finite": bool(torch.isfinite(f).all())}), flush=True)
+            del ws
+        del X, Y
+        torch.cuda.empty_cache()
 
 
 def ctypes_probe(b4, dev):

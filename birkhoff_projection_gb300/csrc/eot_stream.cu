@@ -27,6 +27,8 @@ constexpr int BM = 128;        // query rows per CTA tile = MMA M = TMEM lanes
 constexpr int KC = 32;         // fp32 coordinates per K chunk (one 128-byte swizzle row)
 constexpr int ROW_PAD = 256;   // point counts are padded to this multiple
 constexpr int KSTEP = 8;       // K of one kind::tf32 MMA
+constexpr int NEPI = 8;        // epilogue warps: two per TMEM lane quarter
+constexpr int NTHREADS = 64 + 32 * NEPI;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr unsigned int kFaultEot = 4u;
 
@@ -82,15 +84,57 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
+// One 32-column chunk of a row: scores s_j = acc_j c1 + bias_j (log2
+// units), then the running maximum and sum of 2^(s - max) updated.
+// Packed pair arithmetic, a tree maximum and four partial sums keep the
+// dependency chains short.
+__device__ __forceinline__ void lse_chunk(const uint32_t (&r)[32], const float4* kb, float c1,
+                                          float& m_run, float& s_run) {
+  float2 sc[16];
+  const float2 cc = make_float2(c1, c1);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 b = __ldg(kb + i);
+    sc[2 * i] = __ffma2_rn(make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])),
+                           cc, make_float2(b.x, b.y));
+    sc[2 * i + 1] =
+        __ffma2_rn(make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), cc,
+                   make_float2(b.z, b.w));
+  }
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    mx[i] = b4::max3(sc[2 * i].x, sc[2 * i].y, fmaxf(sc[2 * i + 1].x, sc[2 * i + 1].y));
+  const float cm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  const float mn = fmaxf(m_run, cm);
+  const float ms = mn == -INFINITY ? 0.0f : mn;
+  const float2 neg = make_float2(-ms, -ms);
+  float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                   make_float2(0.0f, 0.0f)};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float2 e = __fadd2_rn(sc[i], neg);
+    e.x = b4::ex2(e.x);
+    e.y = b4::ex2(e.y);
+    acc[i & 3] = __fadd2_rn(acc[i & 3], e);
+  }
+  const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  s_run = fmaf(s_run, b4::ex2(m_run - ms), t.x + t.y);
+  m_run = mn;
+}
+
 // Online log-sum-exp over the score matrix S = (2 Q K^T) log2(e)/eps + bias,
 // row-stationary: each CTA takes 128 query rows at a time and streams every
 // key tile.  Warp roles: 0 = TMA producer, 1 = TMEM owner and MMA issuer,
-// 2..5 = epilogue (TMEM -> registers -> running max / sum per row; thread t
-// of warp w owns row 32 (w % 4) + t, the TMEM lane quarter that warp may
-// read).  Two TMEM accumulators let the MMAs of key tile t + 1 run while
-// the epilogue reduces tile t.
+// 2..9 = epilogue (TMEM -> registers -> running max / sum per row).  Thread
+// t of epilogue warp w owns row 32 (w % 4) + t (the TMEM lane quarter that
+// warp may read) for one half of each tile's columns; the two halves of a
+// row are merged through shared memory when the row block is done.  Two TMEM
+// accumulators let the MMAs of key tile t + 1 run while the epilogue reduces
+// tile t.
 template <int BN, int PASSES>
-__global__ void __launch_bounds__(192, 1) lse_kernel(const __grid_constant__ LseParams p) {
+__global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant__ LseParams p) {
   using C = Cfg<BN, PASSES>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -98,6 +142,7 @@ __global__ void __launch_bounds__(192, 1) lse_kernel(const __grid_constant__ Lse
   __shared__ uint64_t full[C::NSTAGE], empty[C::NSTAGE], acc_full[2], acc_empty[2], mma_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ float2 merge_sh[BM];
   volatile int* abort_flag = &abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -108,7 +153,7 @@ __global__ void __launch_bounds__(192, 1) lse_kernel(const __grid_constant__ Lse
     }
     for (int b = 0; b < 2; ++b) {
       b4::mbar_init(&acc_full[b], 1);
-      b4::mbar_init(&acc_empty[b], 128);
+      b4::mbar_init(&acc_empty[b], 32 * NEPI);
     }
     b4::mbar_init(&mma_done, 1);
     abort_sh = 0;
@@ -204,14 +249,16 @@ __global__ void __launch_bounds__(192, 1) lse_kernel(const __grid_constant__ Lse
     __syncwarp();
   } else {
     // ---------------- epilogue: online LSE per row ----------------
+    constexpr int HALF = BN / 2;
+    constexpr int NCH = HALF / 32;
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    const float ninf = -INFINITY;
     uint32_t tc = 0;
-    bool ok = true;
-    for (int rb = blockIdx.x; rb < p.n_rb && ok; rb += gridDim.x) {
-      float m_run = ninf, s_run = 0.0f;
+    for (int rb = blockIdx.x; rb < p.n_rb; rb += gridDim.x) {
+      float m_run = -INFINITY, s_run = 0.0f;
+      bool ok = true;
       for (int kt = 0; kt < p.n_kt; ++kt, ++tc) {
         const int buf = static_cast<int>(tc & 1u);
         const uint32_t use = tc >> 1;
@@ -219,35 +266,39 @@ __global__ void __launch_bounds__(192, 1) lse_kernel(const __grid_constant__ Lse
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const float4* kb = reinterpret_cast<const float4*>(p.kbias + static_cast<int64_t>(kt) * BN);
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(buf * BN + c * 32), v);
-          float cm = ninf;
+        const int col0 = buf * BN + half * HALF;
+        const float4* kb =
+            reinterpret_cast<const float4*>(p.kbias + static_cast<int64_t>(kt) * BN + half * HALF);
+        uint32_t ra[32], rn[32];
+        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(col0), ra);
+        tmem_wait32(ra);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 b = __ldg(kb + c * 8 + i);
-            v[4 * i + 0] = fmaf(v[4 * i + 0], p.c1, b.x);
-            v[4 * i + 1] = fmaf(v[4 * i + 1], p.c1, b.y);
-            v[4 * i + 2] = fmaf(v[4 * i + 2], p.c1, b.z);
-            v[4 * i + 3] = fmaf(v[4 * i + 3], p.c1, b.w);
-            cm = fmaxf(cm, b4::max3(v[4 * i + 0], v[4 * i + 1], fmaxf(v[4 * i + 2], v[4 * i + 3])));
+        for (int c = 0; c < NCH; ++c) {
+          if (c + 1 < NCH) tmem_ld32(tmem + lane_base + static_cast<uint32_t>(col0 + 32 * (c + 1)), rn);
+          lse_chunk(ra, kb + 8 * c, p.c1, m_run, s_run);
+          if (c + 1 < NCH) {
+            tmem_wait32(rn);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ra[i] = rn[i];
           }
-          const float mn = fmaxf(m_run, cm);
-          const float ms = mn == ninf ? 0.0f : mn;
-          float acc = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) acc += b4::ex2(v[i] - ms);
-          s_run = fmaf(s_run, b4::ex2(m_run - ms), acc);
-          m_run = mn;
         }
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
       }
-      if (!ok) break;
-      const int64_t r = static_cast<int64_t>(rb) * BM + row;
-      if (r < p.nq) p.out[r] = p.qnorm[r] - p.out_scale * (m_run + b4::lg2(s_run));
+      // merge the two column halves of each row (all epilogue warps reach
+      // both barriers; an abort is seen by all of them after the first)
+      if (half == 1) merge_sh[row] = make_float2(m_run, s_run);
+      named_bar_sync(1, 32 * NEPI);
+      if (half == 0 && ok && !*abort_flag) {
+        const float2 o = merge_sh[row];
+        const float mn = fmaxf(m_run, o.x);
+        const float ms = mn == -INFINITY ? 0.0f : mn;
+        const float st = s_run * b4::ex2(m_run - ms) + o.y * b4::ex2(o.x - ms);
+        const int64_t r = static_cast<int64_t>(rb) * BM + row;
+        if (r < p.nq) p.out[r] = p.qnorm[r] - p.out_scale * (mn + b4::lg2(st));
+      }
+      named_bar_sync(1, 32 * NEPI);
+      if (*abort_flag) break;
     }
   }
   tc_fence_before();
@@ -399,7 +450,7 @@ cudaError_t launch_lse(const Side& qs, const Side& ks, int32_t d_pad, const floa
   p.out_scale = static_cast<float>(eps * 0.6931471805599453);
   p.fault = fault;
   const int grid = static_cast<int>(std::min<int64_t>(p.n_rb, nsm));
-  lse_kernel<BN, PASSES><<<grid, 192, C::SMEM, stream>>>(p);
+  lse_kernel<BN, PASSES><<<grid, NTHREADS, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
