@@ -27,8 +27,14 @@ constexpr int BM = 128;        // query rows per CTA tile = MMA M = TMEM lanes
 constexpr int KC = 32;         // fp32 coordinates per K chunk (one 128-byte swizzle row)
 constexpr int ROW_PAD = 256;   // point counts are padded to this multiple
 constexpr int KSTEP = 8;       // K of one kind::tf32 MMA
-constexpr int NEPI = 8;        // epilogue warps: two per TMEM lane quarter
+#ifndef EOT_NEPI
+#define EOT_NEPI 16
+#endif
+constexpr int NEPI = EOT_NEPI;  // epilogue warps: NEPI / 4 column groups per TMEM lane quarter
+constexpr int GROUPS = NEPI / 4;
+static_assert(NEPI % 4 == 0 && NEPI >= 4, "whole lane quarters");
 constexpr int NTHREADS = 64 + 32 * NEPI;
+constexpr int NBIAS = 4;       // key-tile bias buffers in shared memory
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr unsigned int kFaultEot = 4u;
 
@@ -85,30 +91,17 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 }
 
 // One 32-column chunk of a row: scores s_j = acc_j c1 + bias_j (log2
-// units), then the running maximum and sum of 2^(s - max) updated.
-// Packed pair arithmetic, a tree maximum and four partial sums keep the
-// dependency chains short.
-__device__ __forceinline__ void lse_chunk(const uint32_t (&r)[32], const float4* kb, float c1,
-                                          float& m_run, float& s_run) {
-  float2 sc[16];
-  const float2 cc = make_float2(c1, c1);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 b = __ldg(kb + i);
-    sc[2 * i] = __ffma2_rn(make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])),
-                           cc, make_float2(b.x, b.y));
-    sc[2 * i + 1] =
-        __ffma2_rn(make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), cc,
-                   make_float2(b.z, b.w));
-  }
-  float mx[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    mx[i] = b4::max3(sc[2 * i].x, sc[2 * i].y, fmaxf(sc[2 * i + 1].x, sc[2 * i + 1].y));
-  const float cm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-  const float mn = fmaxf(m_run, cm);
-  const float ms = mn == -INFINITY ? 0.0f : mn;
+// units; the biases come from shared memory, the same for every lane), then
+// the running sum of 2^(s - m) against the row's reference m.  The
+// reference lags behind the true maximum: a chunk is first summed against
+// the current m, and only when that sum leaves [0, 2^64] (which includes
+// the first chunk of a row, m = -inf) is the exact maximum taken, the
+// running sum rescaled and the chunk summed again.  Every term is then at
+// most 2^64 and a row's sum at most 2^95, so nothing overflows and fp32
+// keeps its relative accuracy, while most chunks skip the maximum entirely.
+// Packed pair arithmetic and four partial sums keep the dependency chains
+// short.
+__device__ __forceinline__ float chunk_sum(const float2 (&sc)[16], float ms) {
   const float2 neg = make_float2(-ms, -ms);
   float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
                    make_float2(0.0f, 0.0f)};
@@ -120,19 +113,48 @@ __device__ __forceinline__ void lse_chunk(const uint32_t (&r)[32], const float4*
     acc[i & 3] = __fadd2_rn(acc[i & 3], e);
   }
   const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-  s_run = fmaf(s_run, b4::ex2(m_run - ms), t.x + t.y);
+  return t.x + t.y;
+}
+
+__device__ __forceinline__ void lse_chunk(const uint32_t (&r)[32], const float4* kb, float c1,
+                                          float& m_run, float& s_run) {
+  float2 sc[16];
+  const float2 cc = make_float2(c1, c1);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 b = kb[i];
+    sc[2 * i] = __ffma2_rn(make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])),
+                           cc, make_float2(b.x, b.y));
+    sc[2 * i + 1] =
+        __ffma2_rn(make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), cc,
+                   make_float2(b.z, b.w));
+  }
+  const float t = chunk_sum(sc, m_run);
+  if (t <= 0x1p64f) {
+    s_run += t;
+    return;
+  }
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    mx[i] = b4::max3(sc[2 * i].x, sc[2 * i].y, fmaxf(sc[2 * i + 1].x, sc[2 * i + 1].y));
+  const float cm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  const float mn = fmaxf(m_run, cm);
+  const float ms = mn == -INFINITY ? 0.0f : mn;
+  s_run = fmaf(s_run, b4::ex2(m_run - ms), chunk_sum(sc, ms));
   m_run = mn;
 }
 
 // Online log-sum-exp over the score matrix S = (2 Q K^T) log2(e)/eps + bias,
 // row-stationary: each CTA takes 128 query rows at a time and streams every
 // key tile.  Warp roles: 0 = TMA producer, 1 = TMEM owner and MMA issuer,
-// 2..9 = epilogue (TMEM -> registers -> running max / sum per row).  Thread
+// 2.. = epilogue (TMEM -> registers -> running max / sum per row).  Thread
 // t of epilogue warp w owns row 32 (w % 4) + t (the TMEM lane quarter that
-// warp may read) for one half of each tile's columns; the two halves of a
-// row are merged through shared memory when the row block is done.  Two TMEM
-// accumulators let the MMAs of key tile t + 1 run while the epilogue reduces
-// tile t.
+// warp may read) for one column group (a contiguous 1 / GROUPS of each
+// tile's columns); the groups of a row are merged through shared memory
+// when the row block is done.  Two TMEM accumulators let the MMAs of key
+// tile t + 1 run while the epilogue reduces tile t.
 template <int BN, int PASSES>
 __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant__ LseParams p) {
   using C = Cfg<BN, PASSES>;
@@ -140,9 +162,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t full[C::NSTAGE], empty[C::NSTAGE], acc_full[2], acc_empty[2], mma_done;
+  __shared__ uint64_t bias_full[NBIAS], bias_empty[NBIAS];
+  __shared__ __align__(16) float bias_sm[NBIAS][BN];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ float2 merge_sh[BM];
+  __shared__ float2 merge_sh[GROUPS > 1 ? GROUPS - 1 : 1][BM];
   volatile int* abort_flag = &abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -153,7 +177,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) {
       b4::mbar_init(&acc_full[b], 1);
-      b4::mbar_init(&acc_empty[b], 32 * NEPI);
+      b4::mbar_init(&acc_empty[b], NEPI);
+    }
+    for (int b = 0; b < NBIAS; ++b) {
+      b4::mbar_init(&bias_full[b], 1);
+      b4::mbar_init(&bias_empty[b], NEPI);
     }
     b4::mbar_init(&mma_done, 1);
     abort_sh = 0;
@@ -179,9 +207,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = 0, tt = 0;
       for (int rb = blockIdx.x; rb < p.n_rb && !*abort_flag; rb += gridDim.x)
-        for (int kt = 0; kt < p.n_kt && !*abort_flag; ++kt)
+        for (int kt = 0; kt < p.n_kt && !*abort_flag; ++kt) {
+          // the key tile's biases into the shared ring
+          const int slot = static_cast<int>(tt % NBIAS);
+          if (!wait_bar(&bias_empty[slot], ((tt / NBIAS) & 1u) ^ 1u, abort_flag, p.fault)) break;
+          b4::mbar_arrive_expect_tx(&bias_full[slot], BN * 4);
+          bulk_load_1d(bias_sm[slot], p.kbias + static_cast<int64_t>(kt) * BN, BN * 4,
+                       &bias_full[slot]);
+          ++tt;
           for (int kc = 0; kc < p.n_kc; ++kc) {
             const int s = static_cast<int>(it % C::NSTAGE);
             const uint32_t ph = (it / C::NSTAGE) & 1u;
@@ -197,11 +232,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
             }
             ++it;
           }
+        }
       // Every issued copy must land before the CTA may exit: wait for the
-      // last use of each stage (already consumed on the normal path).
+      // last use of each stage and bias slot (already consumed on the normal
+      // path).
       const uint32_t first = it > static_cast<uint32_t>(C::NSTAGE) ? it - C::NSTAGE : 0u;
       for (uint32_t j = first; j < it; ++j)
         b4::mbar_wait(&full[j % C::NSTAGE], (j / C::NSTAGE) & 1u, kWaitLimitNs);
+      const uint32_t tfirst = tt > static_cast<uint32_t>(NBIAS) ? tt - NBIAS : 0u;
+      for (uint32_t j = tfirst; j < tt; ++j)
+        b4::mbar_wait(&bias_full[j % NBIAS], (j / NBIAS) & 1u, kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -249,10 +289,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
     __syncwarp();
   } else {
     // ---------------- epilogue: online LSE per row ----------------
-    constexpr int HALF = BN / 2;
-    constexpr int NCH = HALF / 32;
+    constexpr int COLS = BN / GROUPS;
+    constexpr int NCH = COLS / 32;
+    static_assert(COLS % 32 == 0 && NCH >= 1, "whole 32-column chunks per group");
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int grp = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t tc = 0;
@@ -262,13 +303,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
       for (int kt = 0; kt < p.n_kt; ++kt, ++tc) {
         const int buf = static_cast<int>(tc & 1u);
         const uint32_t use = tc >> 1;
-        ok = wait_bar(&acc_full[buf], use & 1u, abort_flag, p.fault);
+        const int slot = static_cast<int>(tc % NBIAS);
+        ok = wait_bar(&acc_full[buf], use & 1u, abort_flag, p.fault) &&
+             wait_bar(&bias_full[slot], (tc / NBIAS) & 1u, abort_flag, p.fault);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const int col0 = buf * BN + half * HALF;
-        const float4* kb =
-            reinterpret_cast<const float4*>(p.kbias + static_cast<int64_t>(kt) * BN + half * HALF);
+        const int col0 = buf * BN + grp * COLS;
+        const float4* kb = reinterpret_cast<const float4*>(&bias_sm[slot][grp * COLS]);
         uint32_t ra[32], rn[32];
         tmem_ld32(tmem + lane_base + static_cast<uint32_t>(col0), ra);
         tmem_wait32(ra);
@@ -283,17 +325,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
           }
         }
         tc_fence_before();
-        mbar_arrive(&acc_empty[buf]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[buf]);
+          mbar_arrive(&bias_empty[slot]);
+        }
       }
-      // merge the two column halves of each row (all epilogue warps reach
-      // both barriers; an abort is seen by all of them after the first)
-      if (half == 1) merge_sh[row] = make_float2(m_run, s_run);
+      // merge the column groups of each row (all epilogue warps reach both
+      // barriers; an abort is seen by all of them after the first)
+      if (grp > 0) merge_sh[grp - 1][row] = make_float2(m_run, s_run);
       named_bar_sync(1, 32 * NEPI);
-      if (half == 0 && ok && !*abort_flag) {
-        const float2 o = merge_sh[row];
-        const float mn = fmaxf(m_run, o.x);
+      if (grp == 0 && ok && !*abort_flag) {
+        float mn = m_run;
+#pragma unroll
+        for (int g = 0; g < GROUPS - 1; ++g) mn = fmaxf(mn, merge_sh[g][row].x);
         const float ms = mn == -INFINITY ? 0.0f : mn;
-        const float st = s_run * b4::ex2(m_run - ms) + o.y * b4::ex2(o.x - ms);
+        float st = s_run * b4::ex2(m_run - ms);
+#pragma unroll
+        for (int g = 0; g < GROUPS - 1; ++g) {
+          const float2 o = merge_sh[g][row];
+          st = fmaf(o.y, b4::ex2(o.x - ms), st);
+        }
         const int64_t r = static_cast<int64_t>(rb) * BM + row;
         if (r < p.nq) p.out[r] = p.qnorm[r] - p.out_scale * (mn + b4::lg2(st));
       }
