@@ -64,14 +64,21 @@ struct LseParams {
   const float* qnorm;   // [nq_pad] squared norms of the query points
   const float* kbias;   // [nk_pad] (h_j - ||y_j||^2) log2(e)/eps + log2(w_j); -inf past nk
   float* out;           // [nq]
-  int64_t nq;
+  float2* part;         // [n_seg][nq_pad] partial (max, sum) per row when n_seg > 1
+  int64_t nq, nq_pad;
   int32_t n_rb;         // query row blocks (nq_pad / 128)
+  int32_t n_seg;        // key segments per row block (work items = n_rb * n_seg)
   int32_t n_kt;         // key tiles (nk_pad / BN)
   int32_t n_kc;         // K chunks (d_pad / 32)
   float c1;             // 2 log2(e) / eps
   float out_scale;      // eps ln 2
   unsigned int* fault;
 };
+
+// First key tile of segment `seg` of `n_seg`.
+__device__ __forceinline__ int seg_begin(int seg, int n_seg, int n_kt) {
+  return static_cast<int>(static_cast<int64_t>(seg) * n_kt / n_seg);
+}
 
 // mbarrier wait bounded in time and abandoned when another role of the CTA
 // has given up (shared abort flag).
@@ -208,8 +215,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       uint32_t it = 0, tt = 0;
-      for (int rb = blockIdx.x; rb < p.n_rb && !*abort_flag; rb += gridDim.x)
-        for (int kt = 0; kt < p.n_kt && !*abort_flag; ++kt) {
+      const int n_items = p.n_rb * p.n_seg;
+      for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
+        const int rb = item % p.n_rb, seg = item / p.n_rb;
+        const int kt1 = seg_begin(seg + 1, p.n_seg, p.n_kt);
+        for (int kt = seg_begin(seg, p.n_seg, p.n_kt); kt < kt1 && !*abort_flag; ++kt) {
           // the key tile's biases into the shared ring
           const int slot = static_cast<int>(tt % NBIAS);
           if (!wait_bar(&bias_empty[slot], ((tt / NBIAS) & 1u) ^ 1u, abort_flag, p.fault)) break;
@@ -233,6 +243,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
             ++it;
           }
         }
+      }
       // Every issued copy must land before the CTA may exit: wait for the
       // last use of each stage and bias slot (already consumed on the normal
       // path).
@@ -250,8 +261,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
       constexpr uint32_t idesc = idesc_tf32<BM, BN>();
       uint32_t it = 0, tc = 0;
       bool ok = true;
-      for (int rb = blockIdx.x; rb < p.n_rb && ok; rb += gridDim.x)
-        for (int kt = 0; kt < p.n_kt && ok; ++kt, ++tc) {
+      const int n_items = p.n_rb * p.n_seg;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int seg = item / p.n_rb;
+        const int kt1 = seg_begin(seg + 1, p.n_seg, p.n_kt);
+        for (int kt = seg_begin(seg, p.n_seg, p.n_kt); kt < kt1 && ok; ++kt, ++tc) {
           const int buf = static_cast<int>(tc & 1u);
           const uint32_t use = tc >> 1;
           if (!(ok = wait_bar(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.fault))) break;
@@ -282,6 +296,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
           if (!ok) break;
           mma_commit(&acc_full[buf]);
         }
+      }
       // all MMAs issued by this thread complete before TMEM is released
       mma_commit(&mma_done);
       b4::mbar_wait(&mma_done, 0, kWaitLimitNs);
@@ -297,10 +312,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t tc = 0;
-    for (int rb = blockIdx.x; rb < p.n_rb; rb += gridDim.x) {
+    const int n_items = p.n_rb * p.n_seg;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const int rb = item % p.n_rb, seg = item / p.n_rb;
+      const int kt1 = seg_begin(seg + 1, p.n_seg, p.n_kt);
       float m_run = -INFINITY, s_run = 0.0f;
       bool ok = true;
-      for (int kt = 0; kt < p.n_kt; ++kt, ++tc) {
+      for (int kt = seg_begin(seg, p.n_seg, p.n_kt); kt < kt1; ++kt, ++tc) {
         const int buf = static_cast<int>(tc & 1u);
         const uint32_t use = tc >> 1;
         const int slot = static_cast<int>(tc % NBIAS);
@@ -347,7 +365,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) lse_kernel(const __grid_constant_
           st = fmaf(o.y, b4::ex2(o.x - ms), st);
         }
         const int64_t r = static_cast<int64_t>(rb) * BM + row;
-        if (r < p.nq) p.out[r] = p.qnorm[r] - p.out_scale * (mn + b4::lg2(st));
+        if (p.n_seg > 1)
+          p.part[static_cast<int64_t>(seg) * p.nq_pad + r] = make_float2(mn, st);
+        else if (r < p.nq)
+          p.out[r] = p.qnorm[r] - p.out_scale * (mn + b4::lg2(st));
       }
       named_bar_sync(1, 32 * NEPI);
       if (*abort_flag) break;
@@ -393,12 +414,52 @@ __global__ void bias_kernel(const float* __restrict__ h, const float* __restrict
   kb[j] = j < nk ? fmaf(h[j] - knorm[j], scale, log_w[j] * b4::LOG2E) : -INFINITY;
 }
 
+// Combine the key segments' partial (max, sum) of each row into the
+// potential: out_r = qnorm_r - eps ln2 (M + log2 sum_k s_k 2^(m_k - M)).
+__global__ void merge_kernel(const float2* __restrict__ part, int n_seg, int64_t nq, int64_t nq_pad,
+                             const float* __restrict__ qnorm, float out_scale,
+                             float* __restrict__ out) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r >= nq) return;
+  float mx = -INFINITY;
+  for (int k = 0; k < n_seg; ++k) mx = fmaxf(mx, part[k * nq_pad + r].x);
+  const float ms = mx == -INFINITY ? 0.0f : mx;
+  float st = 0.0f;
+  for (int k = 0; k < n_seg; ++k) {
+    const float2 v = part[k * nq_pad + r];
+    st = fmaf(v.y, b4::ex2(v.x - ms), st);
+  }
+  out[r] = qnorm[r] - out_scale * (mx + b4::lg2(st));
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 namespace {
 
 constexpr int64_t kMaxPoints = (int64_t(1) << 31) - 512;
+constexpr int kMaxSegments = 32;
+
+// Key segments per row block: the count (1..32, at least 4 key tiles each)
+// whose work items fill the last wave of `slots` resident CTAs best;
+// another split is taken only when it fills at least 2% more.
+int choose_segments(int64_t n_rb, int n_kt, int slots) {
+  auto fill = [&](int S) {
+    const int64_t items = n_rb * S;
+    const int64_t waves = (items + slots - 1) / slots;
+    return static_cast<double>(items) / static_cast<double>(waves * slots);
+  };
+  int best = 1;
+  double best_fill = fill(1);
+  for (int S = 2; S <= kMaxSegments && n_kt / S >= 4; ++S) {
+    const double f = fill(S);
+    if (f > best_fill + 0.02) {
+      best = S;
+      best_fill = f;
+    }
+  }
+  return best;
+}
 
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 size_t align_bytes(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
@@ -406,7 +467,7 @@ size_t align_bytes(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
 struct Layout {
   int64_t n_pad, m_pad;
   int32_t d_pad;
-  size_t x_hi, x_lo, y_hi, y_lo, x_norm, y_norm, bias, total;  // byte offsets
+  size_t x_hi, x_lo, y_hi, y_lo, x_norm, y_norm, bias, part, total;  // byte offsets
 };
 
 Layout layout(int64_t n, int64_t m, int32_t d, int32_t passes) {
@@ -434,6 +495,8 @@ Layout layout(int64_t n, int64_t m, int32_t d, int32_t passes) {
   o += align_bytes(static_cast<size_t>(L.m_pad) * 4);
   L.bias = o;
   o += align_bytes(static_cast<size_t>(std::max(L.n_pad, L.m_pad)) * 4);
+  L.part = o;
+  o += align_bytes(static_cast<size_t>(std::max(L.n_pad, L.m_pad)) * 8 * kMaxSegments);
   L.total = o;
   return L;
 }
@@ -465,7 +528,8 @@ struct Side {
 
 template <int BN, int PASSES>
 cudaError_t launch_lse(const Side& qs, const Side& ks, int32_t d_pad, const float* kbias,
-                       float* out, float eps, unsigned int* fault, cudaStream_t stream) {
+                       float2* part, float* out, float eps, unsigned int* fault,
+                       cudaStream_t stream) {
   using C = Cfg<BN, PASSES>;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -494,15 +558,23 @@ cudaError_t launch_lse(const Side& qs, const Side& ks, int32_t d_pad, const floa
   p.qnorm = qs.norm;
   p.kbias = kbias;
   p.out = out;
+  p.part = part;
   p.nq = qs.n;
+  p.nq_pad = qs.n_pad;
   p.n_rb = static_cast<int32_t>(qs.n_pad / BM);
   p.n_kt = static_cast<int32_t>(ks.n_pad / BN);
+  p.n_seg = choose_segments(p.n_rb, p.n_kt, nsm);
   p.n_kc = d_pad / KC;
   p.c1 = static_cast<float>(2.0 * 1.4426950408889634 / eps);
   p.out_scale = static_cast<float>(eps * 0.6931471805599453);
   p.fault = fault;
-  const int grid = static_cast<int>(std::min<int64_t>(p.n_rb, nsm));
+  const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(p.n_rb) * p.n_seg, nsm));
   lse_kernel<BN, PASSES><<<grid, NTHREADS, C::SMEM, stream>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess || p.n_seg == 1) return err;
+  const int64_t blocks = (qs.n + 255) / 256;
+  merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, p.n_seg, qs.n, qs.n_pad,
+                                                                  qs.norm, p.out_scale, out);
   return cudaGetLastError();
 }
 
@@ -524,18 +596,19 @@ cudaError_t bias(const float* h, const float* log_w, const float* knorm, int64_t
 
 // f-type update of the query side qs against the key side ks.
 cudaError_t update(const Side& qs, const Side& ks, int32_t d_pad, const float* h, const float* log_w,
-                   float* kb, float* out, float eps, int32_t passes, unsigned int* fault,
-                   cudaStream_t s) {
+                   float* kb, float2* part, float* out, float eps, int32_t passes,
+                   unsigned int* fault, cudaStream_t s) {
   cudaError_t e = bias(h, log_w, ks.norm, ks.n, ks.n_pad, eps, kb, s);
   if (e != cudaSuccess) return e;
-  if (passes == 3) return launch_lse<EOT_BN3, 3>(qs, ks, d_pad, kb, out, eps, fault, s);
-  return launch_lse<EOT_BN1, 1>(qs, ks, d_pad, kb, out, eps, fault, s);
+  if (passes == 3) return launch_lse<EOT_BN3, 3>(qs, ks, d_pad, kb, part, out, eps, fault, s);
+  return launch_lse<EOT_BN1, 1>(qs, ks, d_pad, kb, part, out, eps, fault, s);
 }
 
 struct Packed {
   Side x, y;
   int32_t d_pad;
   float* kb;
+  float2* part;
 };
 
 bool workspace_ok(const void* ws, size_t bytes, const Layout& L) {
@@ -555,6 +628,7 @@ cudaError_t pack_both(const float* X, const float* Y, int64_t n, int64_t m, int3
   P->y = Side{yhi, ylo, yn, m, L.m_pad};
   P->d_pad = L.d_pad;
   P->kb = reinterpret_cast<float*>(w + L.bias);
+  P->part = reinterpret_cast<float2*>(w + L.part);
   cudaError_t e = pack(X, n, d, L.n_pad, L.d_pad, xhi, xlo, xn, s);
   if (e != cudaSuccess) return e;
   return pack(Y, m, d, L.m_pad, L.d_pad, yhi, ylo, yn, s);
@@ -584,7 +658,7 @@ extern "C" int eot_update(const float* Xq, const float* Xk, const float* h, cons
   if (e != cudaSuccess) return b4::record_cuda_error(e);
   eot::Packed P;
   e = eot::pack_both(Xq, Xk, nq, nk, d, passes, workspace, L, &P, s);
-  if (e == cudaSuccess) e = eot::update(P.x, P.y, P.d_pad, h, log_w, P.kb, out, eps, passes, fault, s);
+  if (e == cudaSuccess) e = eot::update(P.x, P.y, P.d_pad, h, log_w, P.kb, P.part, out, eps, passes, fault, s);
   return b4::record_cuda_error(e);
 }
 
@@ -609,8 +683,9 @@ extern "C" int eot_sinkhorn(const float* X, const float* Y, const float* log_a, 
   eot::Packed P;
   e = eot::pack_both(X, Y, n, m, d, passes, workspace, L, &P, s);
   for (int32_t it = 0; it < iters && e == cudaSuccess; ++it) {
-    e = eot::update(P.x, P.y, P.d_pad, g, log_b, P.kb, f, eps, passes, fault, s);
-    if (e == cudaSuccess) e = eot::update(P.y, P.x, P.d_pad, f, log_a, P.kb, g, eps, passes, fault, s);
+    e = eot::update(P.x, P.y, P.d_pad, g, log_b, P.kb, P.part, f, eps, passes, fault, s);
+    if (e == cudaSuccess)
+      e = eot::update(P.y, P.x, P.d_pad, f, log_a, P.kb, P.part, g, eps, passes, fault, s);
   }
   return b4::record_cuda_error(e);
 }

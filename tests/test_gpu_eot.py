@@ -57,6 +57,7 @@ CASES = [
     (129, 257, 32),
     (20000, 300, 8),  # more row blocks than SMs
     (64, 3000, 520),  # d past one 512-wide span, ragged
+    (1000, 5000, 64),  # few row blocks: the keys split into segments, partials merged
 ]
 
 
