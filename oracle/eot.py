@@ -13,6 +13,10 @@ the order).  The cost is formed here directly from the differences x_i - y_j,
 not in the expanded dot-product ("attention") form of the pages' Proposition
 1, so this module shares no arithmetic with a kernel that uses that form.
 
+The transport application of s3 (the plan applied to the key points, and
+from it the gradient of the cost and the barycentric map) is the plan
+pi_ij = a_i b_j exp((f_i + g_j - C_ij)/eps) formed densely and multiplied.
+
 Everything is dense numpy float64 over the full n x m cost matrix, processed
 in row blocks to bound memory; it is meant for n, m up to a few thousand.
 """
@@ -104,3 +108,26 @@ def primal_cost64(X, Y, P, log_a, log_b, eps) -> float:
     kl = np.sum(np.where(P > 0, P * (logP - la[:, None] - lb[None, :]) - P, 0.0)) \
         + np.exp(la).sum() * np.exp(lb).sum()
     return float(np.sum(C * P) + eps * kl)
+
+
+def transport64(X, Y, f, g, log_a, log_b, eps):
+    """Transport application ("FlashSinkhorn", Methodik s3): with
+    pi_ij = a_i b_j exp((f_i + g_j - C_ij)/eps), returns (pi Y [n, d],
+    pi 1 [n]), the weighted sums of the key points and the row masses."""
+    P = plan64(X, Y, f, g, log_a, log_b, eps)
+    return P @ np.asarray(Y, dtype=np.float64), P.sum(1)
+
+
+def grad_x64(X, Y, f, g, log_a, log_b, eps):
+    """Gradient of the entropic OT cost with respect to the points X at
+    optimal potentials (envelope theorem on the dual):
+    d/dx_i = sum_j pi_ij d C_ij / d x_i = 2 (r_i x_i - (pi Y)_i)."""
+    PY, r = transport64(X, Y, f, g, log_a, log_b, eps)
+    return 2.0 * (r[:, None] * np.asarray(X, dtype=np.float64) - PY)
+
+
+def eot_cost64(X, Y, log_a, log_b, eps, iters):
+    """The entropic OT cost <f, a> + <g, b> after `iters` alternating
+    iterations from zero potentials (the dual value at convergence)."""
+    f, g = sinkhorn64(X, Y, log_a, log_b, eps, iters)
+    return float(f @ np.exp(_as64(log_a, "log_a", 1)) + g @ np.exp(_as64(log_b, "log_b", 1)))

@@ -179,3 +179,60 @@ def test_planted_mistakes_fail():
 
     for bad in (sign_of_g, weights_dropped, unsquared, eps_misplaced):
         assert not _pins_hold(bad), bad.__name__
+
+
+def test_gradient_matches_finite_differences_of_the_cost():
+    """grad_x64 (a formula in pi) against central differences of the
+    converged dual value, which is computed without it."""
+    X, Y = clouds(5, 7, 2, seed=21)
+    r = R(22)
+    la = np.log(r.uniform(0.3, 1.0, 5))
+    la -= np.log(np.exp(la).sum())
+    lb = uniform(7)
+    eps, iters, h = 0.5, 4000, 1e-5
+    f, g = eot.sinkhorn64(X, Y, la, lb, eps, iters)
+    G = eot.grad_x64(X, Y, f, g, la, lb, eps)
+    fd = np.zeros_like(X)
+    for i in range(X.shape[0]):
+        for k in range(X.shape[1]):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[i, k] += h
+            Xm[i, k] -= h
+            fd[i, k] = (eot.eot_cost64(Xp, Y, la, lb, eps, iters)
+                        - eot.eot_cost64(Xm, Y, la, lb, eps, iters)) / (2 * h)
+    assert np.abs(G - fd).max() <= 1e-8
+
+
+def test_transport_masses_and_single_target():
+    X, Y = clouds(30, 40, 3, seed=23)
+    la, lb = uniform(30), uniform(40)
+    f, g = eot.sinkhorn64(X, Y, la, lb, 0.3, iters=5000)
+    PY, r = eot.transport64(X, Y, f, g, la, lb, 0.3)
+    assert np.abs(r - np.exp(la)).max() <= 1e-13
+    # the barycentric map of a single target point is that point
+    Y1 = Y[:1]
+    f1, g1 = eot.sinkhorn64(X, Y1, la, np.zeros(1), 0.3, iters=3)
+    PY1, r1 = eot.transport64(X, Y1, f1, g1, la, np.zeros(1), 0.3)
+    assert np.abs(PY1 / r1[:, None] - Y1).max() <= 1e-14
+    # translating both clouds translates the barycentric map
+    t = np.array([0.3, -1.2, 2.0])
+    f2, g2 = eot.sinkhorn64(X + t, Y + t, la, lb, 0.3, iters=5000)
+    PY2, r2 = eot.transport64(X + t, Y + t, f2, g2, la, lb, 0.3)
+    assert np.abs(PY2 / r2[:, None] - (PY / r[:, None] + t)).max() <= 1e-10
+
+
+def test_planted_transport_mistake_fails():
+    """A gradient with the sign of (pi Y) flipped fails the FD pin."""
+    X, Y = clouds(4, 5, 2, seed=24)
+    la, lb = uniform(4), uniform(5)
+    f, g = eot.sinkhorn64(X, Y, la, lb, 0.5, 4000)
+    PY, r = eot.transport64(X, Y, f, g, la, lb, 0.5)
+    bad = 2.0 * (r[:, None] * X + PY)
+    h = 1e-5
+    Xp = X.copy()
+    Xp[0, 0] += h
+    Xm = X.copy()
+    Xm[0, 0] -= h
+    fd = (eot.eot_cost64(Xp, Y, la, lb, 0.5, 4000) - eot.eot_cost64(Xm, Y, la, lb, 0.5, 4000)) / (2 * h)
+    assert abs(bad[0, 0] - fd) > 1e-3
+    assert abs(eot.grad_x64(X, Y, f, g, la, lb, 0.5)[0, 0] - fd) <= 1e-8
