@@ -13,6 +13,7 @@
 
 #include "b4_device.cuh"
 #include "b4_launch.cuh"
+#include "eot_common.cuh"
 #include "eot_device.cuh"
 #include "eot_stream.h"
 
@@ -23,10 +24,6 @@ unsigned int* device_fault_latch(cudaError_t* e);  // birkhoff4_api.cu
 
 namespace eot {
 
-constexpr int BM = 128;        // query rows per CTA tile = MMA M = TMEM lanes
-constexpr int KC = 32;         // fp32 coordinates per K chunk (one 128-byte swizzle row)
-constexpr int ROW_PAD = 256;   // point counts are padded to this multiple
-constexpr int KSTEP = 8;       // K of one kind::tf32 MMA
 #ifndef EOT_NEPI
 #define EOT_NEPI 16
 #endif
@@ -35,8 +32,6 @@ constexpr int GROUPS = NEPI / 4;
 static_assert(NEPI % 4 == 0 && NEPI >= 4, "whole lane quarters");
 constexpr int NTHREADS = 64 + 32 * NEPI;
 constexpr int NBIAS = 4;       // key-tile bias buffers in shared memory
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr unsigned int kFaultEot = 4u;
 
 #ifndef EOT_BN1
 #define EOT_BN1 256
@@ -78,23 +73,6 @@ struct LseParams {
 // First key tile of segment `seg` of `n_seg`.
 __device__ __forceinline__ int seg_begin(int seg, int n_seg, int n_kt) {
   return static_cast<int>(static_cast<int64_t>(seg) * n_kt / n_seg);
-}
-
-// mbarrier wait bounded in time and abandoned when another role of the CTA
-// has given up (shared abort flag).
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned int* fault) {
-  if (b4::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = b4::global_ns();
-  for (;;) {
-    if (b4::mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (b4::global_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      if (fault != nullptr) atomicOr(fault, kFaultEot);
-      return false;
-    }
-  }
 }
 
 // One 32-column chunk of a row: scores s_j = acc_j c1 + bias_j (log2
@@ -435,9 +413,24 @@ __global__ void merge_kernel(const float2* __restrict__ part, int n_seg, int64_t
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
+cudaError_t pack(const float* src, int64_t rows, int32_t d, int64_t rows_pad, int32_t d_pad,
+                 float* hi, float* lo, float* norm, cudaStream_t s) {
+  const int64_t blocks = (rows_pad + 7) / 8;
+  pack_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(src, rows, d, rows_pad, d_pad, hi, lo,
+                                                            norm);
+  return cudaGetLastError();
+}
+
+cudaError_t bias(const float* h, const float* log_w, const float* knorm, int64_t nk, int64_t nk_pad,
+                 float eps, float* kb, cudaStream_t s) {
+  const int64_t blocks = (nk_pad + 255) / 256;
+  bias_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      h, log_w, knorm, nk, nk_pad, static_cast<float>(1.4426950408889634 / eps), kb);
+  return cudaGetLastError();
+}
+
 namespace {
 
-constexpr int64_t kMaxPoints = (int64_t(1) << 31) - 512;
 constexpr int kMaxSegments = 32;
 
 // Key segments per row block: the count (1..32, at least 4 key tiles each)
@@ -461,8 +454,6 @@ int choose_segments(int64_t n_rb, int n_kt, int slots) {
   return best;
 }
 
-int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
-size_t align_bytes(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
 
 struct Layout {
   int64_t n_pad, m_pad;
@@ -506,18 +497,6 @@ bool sizes_ok(int64_t n, int64_t m, int32_t d, int32_t passes) {
          (passes == 1 || passes == 3);
 }
 
-bool encode_points(CUtensorMap* map, const float* base, int64_t rows, int32_t d_pad, int box_rows) {
-  b4::EncodeTiledFn fn = b4::encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d_pad), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d_pad) * 4};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(KC), static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // One side of the problem as packed in the workspace.
 struct Side {
   const float* hi;
@@ -544,12 +523,12 @@ cudaError_t launch_lse(const Side& qs, const Side& ks, int32_t d_pad, const floa
     attr_done[dev].store(1, std::memory_order_release);
   }
   LseParams p;
-  if (!encode_points(&p.qmap[0], qs.hi, qs.n_pad, d_pad, BM) ||
-      !encode_points(&p.kmap[0], ks.hi, ks.n_pad, d_pad, BN))
+  if (!encode_rows128(&p.qmap[0], qs.hi, qs.n_pad, d_pad, BM) ||
+      !encode_rows128(&p.kmap[0], ks.hi, ks.n_pad, d_pad, BN))
     return cudaErrorInvalidValue;
   if (PASSES == 3) {
-    if (!encode_points(&p.qmap[1], qs.lo, qs.n_pad, d_pad, BM) ||
-        !encode_points(&p.kmap[1], ks.lo, ks.n_pad, d_pad, BN))
+    if (!encode_rows128(&p.qmap[1], qs.lo, qs.n_pad, d_pad, BM) ||
+        !encode_rows128(&p.kmap[1], ks.lo, ks.n_pad, d_pad, BN))
       return cudaErrorInvalidValue;
   } else {
     p.qmap[1] = p.qmap[0];
@@ -575,22 +554,6 @@ cudaError_t launch_lse(const Side& qs, const Side& ks, int32_t d_pad, const floa
   const int64_t blocks = (qs.n + 255) / 256;
   merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, p.n_seg, qs.n, qs.n_pad,
                                                                   qs.norm, p.out_scale, out);
-  return cudaGetLastError();
-}
-
-cudaError_t pack(const float* src, int64_t rows, int32_t d, int64_t rows_pad, int32_t d_pad,
-                 float* hi, float* lo, float* norm, cudaStream_t s) {
-  const int64_t blocks = (rows_pad + 7) / 8;
-  pack_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(src, rows, d, rows_pad, d_pad, hi, lo,
-                                                            norm);
-  return cudaGetLastError();
-}
-
-cudaError_t bias(const float* h, const float* log_w, const float* knorm, int64_t nk, int64_t nk_pad,
-                 float eps, float* kb, cudaStream_t s) {
-  const int64_t blocks = (nk_pad + 255) / 256;
-  bias_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      h, log_w, knorm, nk, nk_pad, static_cast<float>(1.4426950408889634 / eps), kb);
   return cudaGetLastError();
 }
 

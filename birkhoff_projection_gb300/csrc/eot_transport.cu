@@ -1,0 +1,556 @@
+// eot_transport.cu -- the transport application of streaming entropic OT
+// ("FlashSinkhorn: IO-Aware Entropic OT on GPU", Methodik s3): with the plan
+// of given potentials, pi_ij = a_i b_j exp((f_i + g_j - ||x_i - y_j||^2)/eps),
+// the kernel computes (pi Y)_i = sum_j pi_ij y_j and the row masses
+// r_i = sum_j pi_ij without storing pi, as two chained tensor-core products
+// per key tile (attention form): S = Q K^T into TMEM, P = 2^(S c1 + bias_j +
+// rowterm_i) written by the epilogue warps into shared memory, then
+// O += P V^T into TMEM with V^T the transposed key points.  Because the
+// potential f fixes each row's normaliser, no running maximum is needed and
+// O is never rescaled.  From O and r follow the gradient of the entropic OT
+// cost with respect to X, 2 (r_i x_i - O_i), and the barycentric map O_i / r_i.
+// The extern "C" entries are declared and documented in eot_stream.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "b4_device.cuh"
+#include "b4_launch.cuh"
+#include "eot_common.cuh"
+#include "eot_device.cuh"
+#include "eot_stream.h"
+
+namespace b4 {
+int record_cuda_error(cudaError_t e);              // birkhoff4_api.cu
+unsigned int* device_fault_latch(cudaError_t* e);  // birkhoff4_api.cu
+}  // namespace b4
+
+namespace eot {
+namespace tr {
+
+constexpr int BN = 128;                    // keys per tile (S = 128 x 128)
+constexpr int DV = 128;                    // value coordinates per launch (O columns)
+constexpr int NEPI = 16;                   // epilogue warps: 4 per TMEM lane quarter
+constexpr int NTHREADS = 64 + 32 * NEPI;   // + producer warp + MMA warp
+constexpr int NQK = 3;                     // Q/K chunk stages
+constexpr int NV = 3;                      // value chunk stages
+constexpr int NBIAS = 4;                   // key-tile bias slots
+constexpr int A_BYTES = BM * KC * 4;       // 16 KB: 128 query rows x 32 coordinates
+constexpr int B_BYTES = BN * KC * 4;       // 16 KB: 128 key rows x 32 coordinates
+constexpr int QK_BYTES = A_BYTES + B_BYTES;
+constexpr int V_BYTES = DV * KC * 4;       // up to 16 KB: DV coordinates x 32 keys
+constexpr int PC_BYTES = BM * KC * 4;      // one 32-key chunk of P: 16 KB
+constexpr int P_BYTES = (BN / KC) * PC_BYTES;
+constexpr int SMEM = NQK * QK_BYTES + NV * V_BYTES + P_BYTES + 1024;
+constexpr int TMEM_COLS = 512;             // S: 2 x 128 columns, O: 128 columns
+constexpr int O_COL = 2 * BN;
+static_assert(NEPI == 4 * (BN / KC), "one epilogue warp per lane quarter and 32-key group");
+static_assert(SMEM <= 227 * 1024 - 4096, "shared memory");
+
+struct Params {
+  CUtensorMap qmap;      // query points [nq_pad, d_pad], box {32, 128}
+  CUtensorMap kmap;      // key points [nk_pad, d_pad], box {32, 128}
+  CUtensorMap vmap;      // key points transposed [d_pad, nk_pad], box {32 keys, dv}
+  const float* kbias;    // [nk_pad] (g_j - ||y_j||^2) log2(e)/eps + log2 b_j; -inf past nk
+  const float* rowterm;  // [nq_pad] (f_i - ||x_i||^2) log2(e)/eps + log2 a_i; -inf past nq
+  float* out;            // [nq, d]: columns v0 .. v0 + dv - 1 (those below d) written
+  float* mass;           // [nq] row masses, or NULL
+  int64_t nq;
+  int32_t d, v0, dv;
+  int32_t n_rb, n_kt, n_kc;
+  float c1;              // 2 log2(e) / eps
+  unsigned int* fault;
+};
+
+// MMA instruction descriptor (kind::tf32, fp32 accumulation, both operands
+// K-major) for M = 128 and a run-time N.
+__device__ __forceinline__ uint32_t idesc_tf32_n(int n) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+// Transposed packing of the key points for the value operand:
+// dst[k][j] = tf32(src[j][k]) for j < rows, k < d, zero elsewhere in
+// [d_pad, rows_pad].  32 x 32 tiles through shared memory, both sides
+// coalesced.
+__global__ void pack_transposed_kernel(const float* __restrict__ src, int64_t rows, int32_t d,
+                                       int64_t rows_pad, int32_t d_pad, float* __restrict__ dst) {
+  __shared__ float t[32][33];
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int k0 = blockIdx.y * 32;
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int64_t j = j0 + r;
+    const int k = k0 + threadIdx.x;
+    t[r][threadIdx.x] = (j < rows && k < d) ? tf32_rna(src[j * d + k]) : 0.0f;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int k = k0 + r;
+    const int64_t j = j0 + threadIdx.x;
+    if (k < d_pad && j < rows_pad) dst[static_cast<int64_t>(k) * rows_pad + j] = t[threadIdx.x][r];
+  }
+}
+
+// rowterm_i = (f_i - ||x_i||^2) log2(e)/eps + log2(a_i) for i < nq, -inf
+// for the padding rows.
+__global__ void rowterm_kernel(const float* __restrict__ f, const float* __restrict__ log_a,
+                               const float* __restrict__ qnorm, int64_t nq, int64_t nq_pad,
+                               float scale, float* __restrict__ rt) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= nq_pad) return;
+  rt[i] = i < nq ? fmaf(f[i] - qnorm[i], scale, log_a[i] * b4::LOG2E) : -INFINITY;
+}
+
+// grad_ik = 2 (r_i x_ik - (pi Y)_ik).
+__global__ void grad_kernel(const float* __restrict__ X, const float* __restrict__ PY,
+                            const float* __restrict__ mass, int64_t n, int32_t d,
+                            float* __restrict__ grad) {
+  const int64_t total = n * d;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    grad[e] = 2.0f * fmaf(mass[e / d], X[e], -PY[e]);
+}
+
+// One CTA per SM, persistent over this CTA's row blocks; its tiles are
+// numbered T = 0, 1, ... (row block major, key tile minor).  Warp roles:
+//   0      producer: per tile T the key biases (bulk copy), the Q/K chunks of
+//          S(T), then the value chunks of tile T - 1;
+//   1      TMEM owner and MMA issuer: S(T) into TMEM buffer T % 2, then
+//          O += P(T - 1) V(T - 1)^T into the O columns (the order in which
+//          the producer loads, so neither ring can stall the other);
+//   2..17  epilogue: thread t of warp w owns query row 32 (w % 4) + t and key
+//          group (w - 2) / 4 (32 keys of each tile): p = 2^(S c1 + bias +
+//          rowterm) into the P buffer in shared memory, the row mass, and at
+//          the end of a row block its 32 columns of O.
+__global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_constant__ Params p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* qk_sm = smem;
+  unsigned char* v_sm = smem + NQK * QK_BYTES;
+  unsigned char* p_sm = v_sm + NV * V_BYTES;
+  __shared__ uint64_t qk_full[NQK], qk_empty[NQK], v_full[NV], v_empty[NV];
+  __shared__ uint64_t acc_full[2], acc_empty[2], p_full, p_empty, o_full, o_empty, mma_done;
+  __shared__ uint64_t bias_full[NBIAS], bias_empty[NBIAS];
+  __shared__ __align__(16) float bias_sm[NBIAS][BN];
+  __shared__ float mass_sh[3][BM];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  volatile int* abort_flag = &abort_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int my_rb = (p.n_rb - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                    static_cast<int>(gridDim.x);
+  const int ntiles = my_rb * p.n_kt;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NQK; ++s) {
+      b4::mbar_init(&qk_full[s], 1);
+      b4::mbar_init(&qk_empty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      b4::mbar_init(&v_full[s], 1);
+      b4::mbar_init(&v_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      b4::mbar_init(&acc_full[b], 1);
+      b4::mbar_init(&acc_empty[b], NEPI);
+    }
+    for (int b = 0; b < NBIAS; ++b) {
+      b4::mbar_init(&bias_full[b], 1);
+      b4::mbar_init(&bias_empty[b], NEPI);
+    }
+    b4::mbar_init(&p_full, NEPI);
+    b4::mbar_init(&p_empty, 1);
+    b4::mbar_init(&o_full, 1);
+    b4::mbar_init(&o_empty, NEPI);
+    b4::mbar_init(&mma_done, 1);
+    abort_sh = 0;
+    b4::mbar_init_fence();
+  }
+  if (warp == 0 && lane == 0) {
+    b4::prefetch_tmap(&p.qmap);
+    b4::prefetch_tmap(&p.kmap);
+    b4::prefetch_tmap(&p.vmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      uint32_t iq = 0, iv = 0, nb = 0;
+      bool ok = true;
+      for (int T = 0; T <= ntiles && ok; ++T) {
+        if (T < ntiles) {
+          const int rb = static_cast<int>(blockIdx.x) + (T / p.n_kt) * static_cast<int>(gridDim.x);
+          const int kt = T % p.n_kt;
+          const int slot = T % NBIAS;
+          if (!(ok = wait_bar(&bias_empty[slot], ((T / NBIAS) & 1) ^ 1u, abort_flag, p.fault))) break;
+          b4::mbar_arrive_expect_tx(&bias_full[slot], BN * 4);
+          bulk_load_1d(bias_sm[slot], p.kbias + static_cast<int64_t>(kt) * BN, BN * 4, &bias_full[slot]);
+          ++nb;
+          for (int kc = 0; kc < p.n_kc; ++kc, ++iq) {
+            const int s = static_cast<int>(iq % NQK);
+            if (!(ok = wait_bar(&qk_empty[s], ((iq / NQK) & 1u) ^ 1u, abort_flag, p.fault))) break;
+            unsigned char* st = qk_sm + s * QK_BYTES;
+            b4::mbar_arrive_expect_tx(&qk_full[s], QK_BYTES);
+            b4::tma_load_2d(st, &p.qmap, &qk_full[s], kc * KC, rb * BM);
+            b4::tma_load_2d(st + A_BYTES, &p.kmap, &qk_full[s], kc * KC, kt * BN);
+          }
+          if (!ok) break;
+        }
+        if (T > 0) {
+          const int kt = (T - 1) % p.n_kt;
+          for (int c = 0; c < BN / KC; ++c, ++iv) {
+            const int s = static_cast<int>(iv % NV);
+            if (!(ok = wait_bar(&v_empty[s], ((iv / NV) & 1u) ^ 1u, abort_flag, p.fault))) break;
+            b4::mbar_arrive_expect_tx(&v_full[s], static_cast<uint32_t>(p.dv) * KC * 4);
+            b4::tma_load_2d(v_sm + s * V_BYTES, &p.vmap, &v_full[s], kt * BN + c * KC, p.v0);
+          }
+        }
+      }
+      // every issued copy lands before the CTA may exit
+      for (uint32_t j = iq > NQK ? iq - NQK : 0u; j < iq; ++j)
+        b4::mbar_wait(&qk_full[j % NQK], (j / NQK) & 1u, kWaitLimitNs);
+      for (uint32_t j = iv > NV ? iv - NV : 0u; j < iv; ++j)
+        b4::mbar_wait(&v_full[j % NV], (j / NV) & 1u, kWaitLimitNs);
+      for (uint32_t j = nb > NBIAS ? nb - NBIAS : 0u; j < nb; ++j)
+        b4::mbar_wait(&bias_full[j % NBIAS], (j / NBIAS) & 1u, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t id_s = idesc_tf32_n(BN), id_o = idesc_tf32_n(p.dv);
+      uint32_t iq = 0, iv = 0;
+      bool ok = true;
+      for (int T = 0; T <= ntiles && ok; ++T) {
+        if (T < ntiles) {
+          const int buf = T & 1;
+          const uint32_t use = static_cast<uint32_t>(T) >> 1;
+          if (!(ok = wait_bar(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.fault))) break;
+          tc_fence_after();
+          const uint32_t d_s = tmem + static_cast<uint32_t>(buf * BN);
+          for (int kc = 0; kc < p.n_kc; ++kc, ++iq) {
+            const int s = static_cast<int>(iq % NQK);
+            if (!(ok = wait_bar(&qk_full[s], (iq / NQK) & 1u, abort_flag, p.fault))) break;
+            tc_fence_after();
+            const uint32_t a = b4::smem_addr(qk_sm + s * QK_BYTES);
+            const uint64_t da = desc_sw128_kmajor(a), db = desc_sw128_kmajor(a + A_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < KC / KSTEP; ++kk) {
+              const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
+              mma_tf32(d_s, da + adv, db + adv, id_s, (kc | kk) != 0);
+            }
+            mma_commit(&qk_empty[s]);
+          }
+          if (!ok) break;
+          mma_commit(&acc_full[buf]);
+        }
+        if (T > 0) {
+          const int U = T - 1;
+          const int kt = U % p.n_kt;
+          const bool first = kt == 0, last = kt == p.n_kt - 1;
+          if (first) {
+            const uint32_t rbl = static_cast<uint32_t>(U / p.n_kt);
+            if (!(ok = wait_bar(&o_empty, (rbl & 1u) ^ 1u, abort_flag, p.fault))) break;
+          }
+          if (!(ok = wait_bar(&p_full, static_cast<uint32_t>(U) & 1u, abort_flag, p.fault))) break;
+          tc_fence_after();
+          for (int c = 0; c < BN / KC; ++c, ++iv) {
+            const int s = static_cast<int>(iv % NV);
+            if (!(ok = wait_bar(&v_full[s], (iv / NV) & 1u, abort_flag, p.fault))) break;
+            tc_fence_after();
+            const uint64_t dp = desc_sw128_kmajor(b4::smem_addr(p_sm + c * PC_BYTES));
+            const uint64_t dv = desc_sw128_kmajor(b4::smem_addr(v_sm + s * V_BYTES));
+#pragma unroll
+            for (int kk = 0; kk < KC / KSTEP; ++kk) {
+              const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
+              mma_tf32(tmem + O_COL, dp + adv, dv + adv, id_o, !(first && c == 0 && kk == 0));
+            }
+            mma_commit(&v_empty[s]);
+          }
+          if (!ok) break;
+          mma_commit(&p_empty);  // the P buffer may be rewritten once these MMAs are done
+          if (last) mma_commit(&o_full);
+        }
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      mma_commit(&mma_done);
+      b4::mbar_wait(&mma_done, 0, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;
+    const int grp = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    unsigned char* p_row = p_sm + grp * PC_BYTES + row * 128;
+    uint32_t T = 0;
+    for (int rbl = 0; rbl < my_rb; ++rbl) {
+      const int rb = static_cast<int>(blockIdx.x) + rbl * static_cast<int>(gridDim.x);
+      const int64_t r = static_cast<int64_t>(rb) * BM + row;
+      const float rt = p.rowterm[r];
+      float mass = 0.0f;
+      bool ok = true;
+      for (int kt = 0; kt < p.n_kt; ++kt, ++T) {
+        const int buf = static_cast<int>(T & 1u);
+        const int slot = static_cast<int>(T % NBIAS);
+        ok = wait_bar(&acc_full[buf], (T >> 1) & 1u, abort_flag, p.fault) &&
+             wait_bar(&bias_full[slot], (T / NBIAS) & 1u, abort_flag, p.fault);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(buf * BN + grp * KC), v);
+        tmem_wait32(v);
+        const float4* kb = reinterpret_cast<const float4*>(&bias_sm[slot][grp * KC]);
+        const float2 cc = make_float2(p.c1, p.c1);
+        const float2 rr = make_float2(rt, rt);
+        float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                         make_float2(0.0f, 0.0f)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 b = kb[i];
+          float2 s0 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])),
+                                 cc, __fadd2_rn(make_float2(b.x, b.y), rr));
+          float2 s1 =
+              __ffma2_rn(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), cc,
+                         __fadd2_rn(make_float2(b.z, b.w), rr));
+          s0.x = b4::ex2(s0.x);
+          s0.y = b4::ex2(s0.y);
+          s1.x = b4::ex2(s1.x);
+          s1.y = b4::ex2(s1.y);
+          acc[(2 * i) & 3] = __fadd2_rn(acc[(2 * i) & 3], s0);
+          acc[(2 * i + 1) & 3] = __fadd2_rn(acc[(2 * i + 1) & 3], s1);
+          v[4 * i] = __float_as_uint(s0.x);
+          v[4 * i + 1] = __float_as_uint(s0.y);
+          v[4 * i + 2] = __float_as_uint(s1.x);
+          v[4 * i + 3] = __float_as_uint(s1.y);
+        }
+        const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        mass += t.x + t.y;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[buf]);
+          mbar_arrive(&bias_empty[slot]);
+        }
+        // the P buffer is free once the MMAs of the previous tile have read it
+        ok = wait_bar(&p_empty, (T & 1u) ^ 1u, abort_flag, p.fault);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        // this row's 32 keys as one 128-byte row of the swizzled K-major tile
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16)
+          *reinterpret_cast<uint4*>(p_row + ((c16 ^ (row & 7)) << 4)) =
+              make_uint4(v[4 * c16], v[4 * c16 + 1], v[4 * c16 + 2], v[4 * c16 + 3]);
+        b4::fence_async_smem();  // visible to the tensor cores' reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full);
+      }
+      if (ok) {
+        ok = wait_bar(&o_full, static_cast<uint32_t>(rbl) & 1u, abort_flag, p.fault);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        tc_fence_after();
+        if (grp * KC < p.dv) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(O_COL + grp * KC), o);
+          tmem_wait32(o);
+          if (r < p.nq) {
+            float* orow = p.out + r * p.d;
+            const int c0 = p.v0 + grp * KC;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c0 + i < p.d) orow[c0 + i] = __uint_as_float(o[i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_empty);
+      }
+      // row masses: the four key groups of a row (every epilogue warp reaches
+      // both barriers; an abort is seen by all of them after the first)
+      if (grp > 0) mass_sh[grp - 1][row] = mass;
+      named_bar_sync(1, 32 * NEPI);
+      if (grp == 0 && ok && !*abort_flag && p.mass != nullptr && r < p.nq)
+        p.mass[r] = mass + mass_sh[0][row] + mass_sh[1][row] + mass_sh[2][row];
+      named_bar_sync(1, 32 * NEPI);
+      if (*abort_flag) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace tr
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+namespace {
+
+struct TrLayout {
+  int64_t n_pad, m_pad;
+  int32_t d_pad;
+  size_t x, y, yt, xn, yn, kb, rt, total;  // byte offsets
+};
+
+TrLayout tr_layout(int64_t n, int64_t m, int32_t d) {
+  TrLayout L;
+  L.n_pad = round_up(std::max<int64_t>(n, 1), ROW_PAD);
+  L.m_pad = round_up(std::max<int64_t>(m, 1), ROW_PAD);
+  L.d_pad = static_cast<int32_t>(round_up(d, KC));
+  size_t o = 0;
+  L.x = o;
+  o += align_bytes(static_cast<size_t>(L.n_pad) * L.d_pad * 4);
+  L.y = o;
+  o += align_bytes(static_cast<size_t>(L.m_pad) * L.d_pad * 4);
+  L.yt = o;
+  o += align_bytes(static_cast<size_t>(L.m_pad) * L.d_pad * 4);
+  L.xn = o;
+  o += align_bytes(static_cast<size_t>(L.n_pad) * 4);
+  L.yn = o;
+  o += align_bytes(static_cast<size_t>(L.m_pad) * 4);
+  L.kb = o;
+  o += align_bytes(static_cast<size_t>(L.m_pad) * 4);
+  L.rt = o;
+  o += align_bytes(static_cast<size_t>(L.n_pad) * 4);
+  L.total = o;
+  return L;
+}
+
+bool tr_sizes_ok(int64_t n, int64_t m, int32_t d) {
+  return n >= 0 && m >= 0 && n <= kMaxPoints && m <= kMaxPoints && d >= 1 && d <= 16384;
+}
+
+cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const float* yt, int32_t v0,
+                             int32_t dv, float* mass, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const int nsm = b4::sm_count(dev);
+  if (nsm <= 0) return cudaErrorInvalidDevice;
+  static std::atomic<int> attr_done[64];
+  if (dev < 64 && attr_done[dev].load(std::memory_order_acquire) == 0) {
+    err = cudaFuncSetAttribute(tr::transport_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               tr::SMEM);
+    if (err != cudaSuccess) return err;
+    attr_done[dev].store(1, std::memory_order_release);
+  }
+  tr::Params p = base;
+  // value operand: rows v0 .. v0 + dv - 1 of the transposed key points
+  {
+    b4::EncodeTiledFn fn = b4::encode_fn();
+    if (fn == nullptr) return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.m_pad), static_cast<cuuint64_t>(L.d_pad)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.m_pad) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(KC), static_cast<cuuint32_t>(dv)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (fn(&p.vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(yt), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  p.v0 = v0;
+  p.dv = dv;
+  p.mass = mass;
+  const int grid = std::min(p.n_rb, nsm);
+  tr::transport_kernel<<<grid, tr::NTHREADS, tr::SMEM, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace eot
+
+extern "C" size_t eot_transport_workspace_bytes(int64_t n, int64_t m, int32_t d) {
+  if (!eot::tr_sizes_ok(n, m, d)) return 0;
+  return eot::tr_layout(n, m, d).total;
+}
+
+extern "C" int eot_transport(const float* X, const float* Y, const float* f, const float* g,
+                             const float* log_a, const float* log_b, float* PY, float* mass,
+                             float* grad, int64_t n, int64_t m, int32_t d, float eps,
+                             void* workspace, size_t workspace_bytes, birkhoff4_stream_t stream) {
+  if (!eot::tr_sizes_ok(n, m, d) || !(eps > 0.0f) || !std::isfinite(eps)) return B4_EINVAL;
+  if (n == 0) return B4_OK;
+  if (m == 0) return B4_EINVAL;
+  if (X == nullptr || Y == nullptr || f == nullptr || g == nullptr || log_a == nullptr ||
+      log_b == nullptr || PY == nullptr || mass == nullptr)
+    return B4_EINVAL;
+  const eot::TrLayout L = eot::tr_layout(n, m, d);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < L.total)
+    return B4_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  unsigned int* fault = b4::device_fault_latch(&e);
+  if (e != cudaSuccess) return b4::record_cuda_error(e);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  float* xp = reinterpret_cast<float*>(w + L.x);
+  float* yp = reinterpret_cast<float*>(w + L.y);
+  float* ytp = reinterpret_cast<float*>(w + L.yt);
+  float* xn = reinterpret_cast<float*>(w + L.xn);
+  float* yn = reinterpret_cast<float*>(w + L.yn);
+  float* kb = reinterpret_cast<float*>(w + L.kb);
+  float* rt = reinterpret_cast<float*>(w + L.rt);
+  e = eot::pack(X, n, d, L.n_pad, L.d_pad, xp, nullptr, xn, s);
+  if (e == cudaSuccess) e = eot::pack(Y, m, d, L.m_pad, L.d_pad, yp, nullptr, yn, s);
+  if (e == cudaSuccess) {
+    const dim3 grid(static_cast<unsigned>(L.m_pad / 32), static_cast<unsigned>(L.d_pad / 32));
+    eot::tr::pack_transposed_kernel<<<grid, dim3(32, 8), 0, s>>>(Y, m, d, L.m_pad, L.d_pad, ytp);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = eot::bias(g, log_b, yn, m, L.m_pad, eps, kb, s);
+  if (e == cudaSuccess) {
+    eot::tr::rowterm_kernel<<<static_cast<unsigned>((L.n_pad + 255) / 256), 256, 0, s>>>(
+        f, log_a, xn, n, L.n_pad, static_cast<float>(1.4426950408889634 / eps), rt);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return b4::record_cuda_error(e);
+  eot::tr::Params p;
+  if (!eot::encode_rows128(&p.qmap, xp, L.n_pad, L.d_pad, eot::BM) ||
+      !eot::encode_rows128(&p.kmap, yp, L.m_pad, L.d_pad, eot::tr::BN))
+    return b4::record_cuda_error(cudaErrorInvalidValue);
+  p.kbias = kb;
+  p.rowterm = rt;
+  p.out = PY;
+  p.mass = nullptr;
+  p.nq = n;
+  p.d = d;
+  p.n_rb = static_cast<int32_t>(L.n_pad / eot::BM);
+  p.n_kt = static_cast<int32_t>(L.m_pad / eot::tr::BN);
+  p.n_kc = L.d_pad / eot::KC;
+  p.c1 = static_cast<float>(2.0 * 1.4426950408889634 / eps);
+  p.fault = fault;
+  // one launch per slice of up to 128 value coordinates; the first also
+  // writes the row masses
+  for (int32_t v0 = 0; v0 < L.d_pad && e == cudaSuccess; v0 += eot::tr::DV) {
+    const int32_t dv = std::min<int32_t>(eot::tr::DV, L.d_pad - v0);
+    e = eot::launch_transport(p, L, ytp, v0, dv, v0 == 0 ? mass : nullptr, s);
+  }
+  if (e == cudaSuccess && grad != nullptr) {
+    const int64_t total = n * static_cast<int64_t>(d);
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, 1 << 20);
+    eot::tr::grad_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(X, PY, mass, n, d, grad);
+    e = cudaGetLastError();
+  }
+  return b4::record_cuda_error(e);
+}

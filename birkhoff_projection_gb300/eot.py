@@ -96,3 +96,36 @@ def sinkhorn(X: torch.Tensor, Y: torch.Tensor, log_a: torch.Tensor, log_b: torch
                                  _stream(X)),
               "eot_sinkhorn")
     return f, g
+
+
+def transport(X: torch.Tensor, Y: torch.Tensor, f: torch.Tensor, g: torch.Tensor,
+              log_a: torch.Tensor, log_b: torch.Tensor, eps: float, want_grad: bool = False,
+              workspace: torch.Tensor = None):
+    """Transport application of the plan pi_ij = a_i b_j exp((f_i + g_j -
+    ||x_i - y_j||^2)/eps): returns (pi Y [n, d], pi 1 [n]) and, with
+    want_grad, also 2 (r_i x_i - (pi Y)_i), the gradient of the entropic OT
+    cost with respect to X at converged potentials.  The barycentric map is
+    (pi Y) / (pi 1)[:, None]."""
+    n = _points(X, "X")
+    m = _points(Y, "Y")
+    if Y.device != X.device or Y.shape[1] != X.shape[1]:
+        raise ValueError("X and Y must share the device and the dimension")
+    for t, name, k in ((f, "f", n), (g, "g", m), (log_a, "log_a", n), (log_b, "log_b", m)):
+        _vector(t, name, k, X.device)
+    d = X.shape[1]
+    need = lib().eot_transport_workspace_bytes(n, m, d)
+    if need == 0:
+        raise ValueError("invalid sizes")
+    ws = workspace if workspace is not None else torch.empty(need, dtype=torch.uint8,
+                                                             device=X.device)
+    if ws.numel() < need or ws.device != X.device:
+        raise ValueError("workspace needs %d bytes on %s" % (need, X.device))
+    PY = torch.empty(n, d, dtype=torch.float32, device=X.device)
+    mass = torch.empty(n, dtype=torch.float32, device=X.device)
+    grad = torch.empty(n, d, dtype=torch.float32, device=X.device) if want_grad else None
+    with _on_device(X):
+        check(lib().eot_transport(_ptr(X), _ptr(Y), _ptr(f), _ptr(g), _ptr(log_a), _ptr(log_b),
+                                  _ptr(PY), _ptr(mass), _ptr(grad), n, m, d, float(eps), _ptr(ws),
+                                  ws.numel(), _stream(X)),
+              "eot_transport")
+    return (PY, mass, grad) if want_grad else (PY, mass)

@@ -77,6 +77,29 @@ int eot_sinkhorn(const float *X, const float *Y, const float *log_a, const float
                  int32_t passes, void *workspace, size_t workspace_bytes,
                  birkhoff4_stream_t stream);
 
+/* Transport application [FlashSinkhorn, Methodik s3]: with the plan of
+ * the potentials f [n] and g [m],
+ *     pi_ij = a_i b_j exp((f_i + g_j - ||x_i - y_j||^2) / eps),
+ * computes PY [n, d] = pi Y (PY_i = sum_j pi_ij y_j) and mass [n] = pi 1
+ * without storing pi.  If grad is not NULL it also writes grad [n, d] =
+ * 2 (mass_i x_i - PY_i): at Sinkhorn-converged potentials this is the
+ * gradient of the entropic OT cost <f, a> + <g, b> with respect to X
+ * (envelope theorem); PY_i / mass_i is the barycentric map.  For f the exact
+ * update of g (eot_update), pi's rows are normalised softmax weights, so no
+ * running maximum is needed.  Otherwise pi is evaluated as given, and
+ * potentials far from consistent can overflow.
+ * Arithmetic: TF32 products with fp32 accumulation for both chained
+ * products (S = X Y^T, then pi Y); exponentials and masses in fp32.  The
+ * value coordinates are processed 128 at a time, one launch each.
+ * Workspace: eot_transport_workspace_bytes(n, m, d), 256-byte aligned.
+ * Errors as for eot_update; PY, mass must not alias the inputs or each
+ * other, grad may be NULL. */
+size_t eot_transport_workspace_bytes(int64_t n, int64_t m, int32_t d);
+int eot_transport(const float *X, const float *Y, const float *f, const float *g,
+                  const float *log_a, const float *log_b, float *PY, float *mass, float *grad,
+                  int64_t n, int64_t m, int32_t d, float eps, void *workspace,
+                  size_t workspace_bytes, birkhoff4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

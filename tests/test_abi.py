@@ -121,6 +121,27 @@ def test_eot_arguments_are_checked(L):
     assert sk(n=0, m=0) == _lib.B4_OK
 
 
+def test_eot_transport_arguments_are_checked(L):
+    f32 = ctypes.c_float
+    need = L.eot_transport_workspace_bytes(100, 200, 64)
+    assert need > 0 and L.eot_transport_workspace_bytes(100, 200, 0) == 0
+    ws = ctypes.c_void_p(0x100000)
+
+    def tr(n=100, m=200, d=64, eps=0.1, w=ws, wb=need, py=FAKE, mass=FAKE):
+        return L.eot_transport(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, py, mass, None, n, m, d,
+                               f32(eps), w, wb, None)
+
+    assert tr(eps=0.0) == _lib.B4_EINVAL
+    assert tr(eps=float("nan")) == _lib.B4_EINVAL
+    assert tr(d=0) == _lib.B4_EINVAL
+    assert tr(m=0) == _lib.B4_EINVAL
+    assert tr(py=None) == _lib.B4_EINVAL
+    assert tr(mass=None) == _lib.B4_EINVAL
+    assert tr(w=ctypes.c_void_p(0x100080)) == _lib.B4_EINVAL
+    assert tr(wb=need - 1) == _lib.B4_EINVAL
+    assert tr(n=0, w=None, py=None, mass=None) == _lib.B4_OK
+
+
 def test_bad_options_are_einval(L):
     def opts(**kw):
         o = _lib.Opts(in_dtype=0, out_dtype=0, max_evals=0, tol=0.0)

@@ -140,3 +140,88 @@ def test_full_size_sampled_rows():
         tol = row_bound(Xs, Yn, np.zeros(m), np64(log_b), ref, workloads.EOT_EPS, passes)
         assert np.all(np.abs(np64(f)[rows] - ref) <= tol)
         assert np.all(np.isfinite(np64(f)))
+
+
+def transport_bounds(X, Y, f, g, log_a, log_b, eps):
+    """Element bounds for (pi Y, pi 1) from one TF32 pass: each pi_ij is off
+    by at most exp(e_i) - 1 relative, e_i the exponent error of row i (the
+    update's per-row bound over eps, plus the ex2 approximation); the second
+    product adds TF32 truncation of pi (2^-10) and rounding of y (2^-11) and
+    fp32 accumulation over m_pad keys.  The tests assert twice the bound."""
+    X = np.asarray(X, np.float64)
+    Y = np.asarray(Y, np.float64)
+    m_pad = -(-Y.shape[0] // 256) * 256
+    fr = np.abs(f) + eps * np.abs(log_a)
+    t = row_bound(X, Y, g, log_b, fr, eps, eot.TF32) / 2.0
+    rel = np.expm1(t / eps + 2.0 ** -20)
+    P = oeot.plan64(X, Y, f, g, log_a, log_b, eps)
+    acc = m_pad * 2.0 ** -23
+    b_py = (rel + 2.0 ** -10 + 2.0 ** -11 + acc)[:, None] * (P @ np.abs(Y))
+    b_mass = (rel + acc) * P.sum(1)
+    return 2.0 * b_py, 2.0 * b_mass
+
+
+TRANSPORT_CASES = [
+    (1000, 1500, 64),
+    (300, 700, 3),
+    (129, 257, 160),   # two value slices, ragged everything
+    (1, 1, 1),
+    (20000, 300, 8),   # more row blocks than SMs
+    (300, 400, 520),   # five value slices
+]
+
+
+@pytest.mark.parametrize("n,m,d", TRANSPORT_CASES)
+def test_transport_parity(n, m, d):
+    eps = workloads.EOT_EPS
+    X, Y, log_a, log_b = workloads.eot_clouds(n, m, d, seed=n + 3 * m + d, device=DEV,
+                                              random_weights=True)
+    f64, g64 = oeot.sinkhorn64(np64(X), np64(Y), np64(log_a), np64(log_b), eps, 30)
+    f = torch.tensor(f64, dtype=torch.float32, device=DEV)
+    g = torch.tensor(g64, dtype=torch.float32, device=DEV)
+    PY, mass, grad = eot.transport(X, Y, f, g, log_a, log_b, eps, want_grad=True)
+    args = (np64(X), np64(Y), np64(f), np64(g), np64(log_a), np64(log_b), eps)
+    PYr, mr = oeot.transport64(*args)
+    b_py, b_mass = transport_bounds(*args)
+    assert np.all(np.isfinite(np64(PY))) and np.all(np.isfinite(np64(mass)))
+    assert np.all(np.abs(np64(PY) - PYr) <= b_py)
+    assert np.all(np.abs(np64(mass) - mr) <= b_mass)
+    Gr = oeot.grad_x64(*args)
+    b_g = 2.0 * (b_mass[:, None] * np.abs(np64(X)) + b_py) + 2.0 ** -20 * np.abs(Gr) + 1e-30
+    assert np.all(np.abs(np64(grad) - Gr) <= 2.0 * b_g)
+
+
+def test_transport_row_masses_at_consistent_potentials():
+    """With f the (split-form) update of g, every row of pi sums to a_i: the
+    GPU masses match the oracle's masses of the same potentials within the
+    derived bound, and those are a to the split form's accuracy."""
+    n, m, d, eps = 600, 800, 16, 0.1
+    X, Y, log_a, log_b = workloads.eot_clouds(n, m, d, seed=11, device=DEV, random_weights=True)
+    f, g = eot.sinkhorn(X, Y, log_a, log_b, eps, 50, passes=eot.TF32X3)
+    f = eot.update(X, Y, g, log_b, eps, passes=eot.TF32X3)
+    PY, mass = eot.transport(X, Y, f, g, log_a, log_b, eps)
+    args = (np64(X), np64(Y), np64(f), np64(g), np64(log_a), np64(log_b), eps)
+    _, mr = oeot.transport64(*args)
+    _, b_mass = transport_bounds(*args)
+    assert np.all(np.abs(np64(mass) - mr) <= b_mass)
+    a = np.exp(np64(log_a))
+    assert np.abs(mr / a - 1).max() <= 1e-3
+
+
+def test_transport_full_size_sampled_rows():
+    """65536 x 65536 points, d = 512 (four value slices): sampled rows
+    against the oracle's plan rows."""
+    n = m = 65536
+    d = 512
+    eps = workloads.EOT_EPS
+    X, Y, log_a, log_b = workloads.eot_clouds(n, m, d, seed=0, device=DEV)
+    g = torch.zeros(m, device=DEV)
+    f = eot.update(X, Y, g, log_b, eps)
+    PY, mass = eot.transport(X, Y, f, g, log_a, log_b, eps)
+    rows = np.r_[0, 127, 128, 30000, n - 1, np.random.default_rng(1).integers(0, n, 5)]
+    idx = torch.as_tensor(rows, device=DEV)
+    args = (np64(X[idx]), np64(Y), np64(f[idx]), np64(g), np64(log_a[idx]), np64(log_b), eps)
+    PYr, mr = oeot.transport64(*args)
+    b_py, b_mass = transport_bounds(*args)
+    assert np.all(np.abs(np64(PY)[rows] - PYr) <= b_py)
+    assert np.all(np.abs(np64(mass)[rows] - mr) <= b_mass)
