@@ -483,6 +483,12 @@ def tf32_peak():
         return 1900.0 * 1.1 / 2.25, "fallback bf16 x 1.1/2.25"
 
 
+def lib_tr_bytes(n, m, d):
+    from birkhoff_projection_gb300 import lib
+
+    return lib().eot_transport_workspace_bytes(n, m, d)
+
+
 def run_eot(dev):
     """Streaming EOT lines: time per Sinkhorn iteration (two potential
     updates) at n = m = 65536, from the difference of 1 + K and 1 iterations
@@ -515,6 +521,21 @@ def run_eot(dev):
                               "ex2_per_update": n * m,
                               "f_finite": bool(torch.isfinite(f).all())}), flush=True)
             del ws
+        # transport application (pi Y, row masses, gradient) at the potentials
+        # of one f update
+        f = eot.update(X, Y, torch.zeros(m, device=dev), lb, eps)
+        g = torch.zeros(m, device=dev)
+        ws = torch.empty(lib_tr_bytes(n, m, d), dtype=torch.uint8, device=dev)
+        tt = time_device(lambda i: eot.transport(X, Y, f, g, la, lb, eps, want_grad=True,
+                                                 workspace=ws), 5, dev)
+        slices = -(-(-(-d // 32) * 32) // 256)  # value coordinates per launch: 256
+        alg = 4.0 * n * m * d / (tt * 1e-3) / 1e12
+        tensor = (2.0 * n * m * (-(-d // 32) * 32) * (slices + 1)) / (tt * 1e-3) / 1e12
+        print(json.dumps({"eot_transport": True, "n": n, "m": m, "d": d, "eps": eps,
+                          "ms": tt, "algorithmic_tflops": alg, "tensor_tflops": tensor,
+                          "value_slices": slices, "tf32_peak_tflops": peak,
+                          "frac_of_tensor_peak": tensor / peak}), flush=True)
+        del ws
         del X, Y
         torch.cuda.empty_cache()
 

@@ -51,6 +51,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose else []
+    # tile-shape and pipeline macros for measurement sweeps, e.g.
+    # B4_NVCC_DEFINES="EOT_TR_NEPI=16 B4_FWD_TILE=256"
+    extra += ["-D" + d for d in os.environ.get("B4_NVCC_DEFINES", "").split()]
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))

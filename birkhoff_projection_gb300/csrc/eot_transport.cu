@@ -4,8 +4,9 @@
 // the kernel computes (pi Y)_i = sum_j pi_ij y_j and the row masses
 // r_i = sum_j pi_ij without storing pi, as two chained tensor-core products
 // per key tile (attention form): S = Q K^T into TMEM, P = 2^(S c1 + bias_j +
-// rowterm_i) written by the epilogue warps into shared memory, then
-// O += P V^T into TMEM with V^T the transposed key points.  Because the
+// rowterm_i) written by the epilogue warps back over S in TMEM, then
+// O += P V^T into TMEM with P read from TMEM and V^T (the transposed key
+// points) from shared memory.  Because the
 // potential f fixes each row's normaliser, no running maximum is needed and
 // O is never rescaled.  From O and r follow the gradient of the entropic OT
 // cost with respect to X, 2 (r_i x_i - O_i), and the barycentric map O_i / r_i.
@@ -32,23 +33,33 @@ unsigned int* device_fault_latch(cudaError_t* e);  // birkhoff4_api.cu
 namespace eot {
 namespace tr {
 
+#ifndef EOT_TR_DV
+#define EOT_TR_DV 256
+#endif
 constexpr int BN = 128;                    // keys per tile (S = 128 x 128)
-constexpr int DV = 128;                    // value coordinates per launch (O columns)
-constexpr int NEPI = 16;                   // epilogue warps: 4 per TMEM lane quarter
+constexpr int DV = EOT_TR_DV;              // value coordinates per launch (O columns)
+#ifndef EOT_TR_NBUF3
+#define EOT_TR_NBUF3 1
+#endif
+#ifndef EOT_TR_NEPI
+#define EOT_TR_NEPI 8
+#endif
+constexpr int NEPI = EOT_TR_NEPI;          // epilogue warps: NEPI / 4 per TMEM lane quarter
 constexpr int NTHREADS = 64 + 32 * NEPI;   // + producer warp + MMA warp
 constexpr int NQK = 3;                     // Q/K chunk stages
-constexpr int NV = 3;                      // value chunk stages
+constexpr int NV_MAX = 24;                 // value chunk stages (run time: the region / chunk size)
 constexpr int NBIAS = 4;                   // key-tile bias slots
 constexpr int A_BYTES = BM * KC * 4;       // 16 KB: 128 query rows x 32 coordinates
 constexpr int B_BYTES = BN * KC * 4;       // 16 KB: 128 key rows x 32 coordinates
 constexpr int QK_BYTES = A_BYTES + B_BYTES;
-constexpr int V_BYTES = DV * KC * 4;       // up to 16 KB: DV coordinates x 32 keys
-constexpr int PC_BYTES = BM * KC * 4;      // one 32-key chunk of P: 16 KB
-constexpr int P_BYTES = (BN / KC) * PC_BYTES;
-constexpr int SMEM = NQK * QK_BYTES + NV * V_BYTES + P_BYTES + 1024;
-constexpr int TMEM_COLS = 512;             // S: 2 x 128 columns, O: 128 columns
-constexpr int O_COL = 2 * BN;
-static_assert(NEPI == 4 * (BN / KC), "one epilogue warp per lane quarter and 32-key group");
+constexpr int V_REGION = 96 * 1024;       // value chunks of dv coordinates x 32 keys
+constexpr int SMEM = NQK * QK_BYTES + V_REGION + 1024;
+static_assert(DV % KC == 0 && DV <= 256 && V_REGION >= 3 * DV * KC * 4, "value slices");
+constexpr int TMEM_COLS = 512;             // S / P buffers of 128 columns, then O
+constexpr int NBUF_MAX = 3;                // 3 S / P buffers when O needs <= 128 columns
+constexpr int GROUPS = NEPI / 4;           // key groups per tile (one per epilogue warp of a quarter)
+constexpr int CPG = BN / KC / GROUPS;      // 32-key chunks per group
+static_assert(NEPI % 4 == 0 && (BN / KC) % GROUPS == 0, "whole chunks per epilogue warp");
 static_assert(SMEM <= 227 * 1024 - 4096, "shared memory");
 
 struct Params {
@@ -61,6 +72,8 @@ struct Params {
   float* mass;           // [nq] row masses, or NULL
   int64_t nq;
   int32_t d, v0, dv;
+  int32_t nv;            // value stages: V_REGION / (dv * 128), at most NV_MAX
+  int32_t nbuf;          // S / P buffers in TMEM: 3 if dv <= 128, else 2; O follows them
   int32_t n_rb, n_kt, n_kc;
   float c1;              // 2 log2(e) / eps
   unsigned int* fault;
@@ -115,29 +128,60 @@ __global__ void grad_kernel(const float* __restrict__ X, const float* __restrict
     grad[e] = 2.0f * fmaf(mass[e / d], X[e], -PY[e]);
 }
 
+// p = 2^(acc c1 + bias_j + rt) for one 32-key chunk of a row, in place over
+// the accumulator bits; returns the chunk's sum.
+__device__ __forceinline__ float p_chunk(uint32_t (&v)[32], const float4* kb, float c1, float rt) {
+  const float2 cc = make_float2(c1, c1);
+  const float2 rr = make_float2(rt, rt);
+  float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                   make_float2(0.0f, 0.0f)};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 b = kb[i];
+    float2 s0 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])),
+                           cc, __fadd2_rn(make_float2(b.x, b.y), rr));
+    float2 s1 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
+                           cc, __fadd2_rn(make_float2(b.z, b.w), rr));
+    s0.x = b4::ex2(s0.x);
+    s0.y = b4::ex2(s0.y);
+    s1.x = b4::ex2(s1.x);
+    s1.y = b4::ex2(s1.y);
+    acc[(2 * i) & 3] = __fadd2_rn(acc[(2 * i) & 3], s0);
+    acc[(2 * i + 1) & 3] = __fadd2_rn(acc[(2 * i + 1) & 3], s1);
+    v[4 * i] = __float_as_uint(s0.x);
+    v[4 * i + 1] = __float_as_uint(s0.y);
+    v[4 * i + 2] = __float_as_uint(s1.x);
+    v[4 * i + 3] = __float_as_uint(s1.y);
+  }
+  const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  return t.x + t.y;
+}
+
 // One CTA per SM, persistent over this CTA's row blocks; its tiles are
 // numbered T = 0, 1, ... (row block major, key tile minor).  Warp roles:
-//   0      producer: per tile T the key biases (bulk copy), the Q/K chunks of
-//          S(T), then the value chunks of tile T - 1;
+//   0      producers: lane 0 per tile T the key biases (bulk copy) and the
+//          Q/K chunks of S(T); lane 1 the value chunks of every tile, on a
+//          ring of its own (neither producer can hold the other up);
 //   1      TMEM owner and MMA issuer: S(T) into TMEM buffer T % 2, then
-//          O += P(T - 1) V(T - 1)^T into the O columns (the order in which
-//          the producer loads, so neither ring can stall the other);
+//          O += P(T - 1) V(T - 1)^T into the O columns with P(T - 1) read
+//          from its TMEM buffer (the order in which the producer loads, so
+//          neither ring can stall the other); the buffer is released when
+//          those MMAs complete;
 //   2..17  epilogue: thread t of warp w owns query row 32 (w % 4) + t and key
 //          group (w - 2) / 4 (32 keys of each tile): p = 2^(S c1 + bias +
-//          rowterm) into the P buffer in shared memory, the row mass, and at
-//          the end of a row block its 32 columns of O.
+//          rowterm) stored over its S columns in TMEM, the row mass, and at
+//          the end of a row block its chunks of O.
 __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_constant__ Params p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* qk_sm = smem;
   unsigned char* v_sm = smem + NQK * QK_BYTES;
-  unsigned char* p_sm = v_sm + NV * V_BYTES;
-  __shared__ uint64_t qk_full[NQK], qk_empty[NQK], v_full[NV], v_empty[NV];
-  __shared__ uint64_t acc_full[2], acc_empty[2], p_full, p_empty, o_full, o_empty, mma_done;
+  __shared__ uint64_t qk_full[NQK], qk_empty[NQK], v_full[NV_MAX], v_empty[NV_MAX];
+  __shared__ uint64_t acc_full[NBUF_MAX], acc_empty[NBUF_MAX], p_full, o_full, o_empty, mma_done;
   __shared__ uint64_t bias_full[NBIAS], bias_empty[NBIAS];
   __shared__ __align__(16) float bias_sm[NBIAS][BN];
-  __shared__ float mass_sh[3][BM];
+  __shared__ float mass_sh[GROUPS > 1 ? GROUPS - 1 : 1][BM];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   volatile int* abort_flag = &abort_sh;
@@ -151,20 +195,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       b4::mbar_init(&qk_full[s], 1);
       b4::mbar_init(&qk_empty[s], 1);
     }
-    for (int s = 0; s < NV; ++s) {
+    for (int s = 0; s < p.nv; ++s) {
       b4::mbar_init(&v_full[s], 1);
       b4::mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NBUF_MAX; ++b) {
       b4::mbar_init(&acc_full[b], 1);
-      b4::mbar_init(&acc_empty[b], NEPI);
+      b4::mbar_init(&acc_empty[b], 1);
     }
     for (int b = 0; b < NBIAS; ++b) {
       b4::mbar_init(&bias_full[b], 1);
       b4::mbar_init(&bias_empty[b], NEPI);
     }
     b4::mbar_init(&p_full, NEPI);
-    b4::mbar_init(&p_empty, 1);
     b4::mbar_init(&o_full, 1);
     b4::mbar_init(&o_empty, NEPI);
     b4::mbar_init(&mma_done, 1);
@@ -184,60 +227,66 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  const uint32_t nbuf = static_cast<uint32_t>(p.nbuf);
+  const uint32_t o_col = nbuf * BN;
 
   if (warp == 0) {
-    // ---------------- producer ----------------
+    // ---------------- producers ----------------
+    const uint32_t vbytes = static_cast<uint32_t>(p.dv) * KC * 4;
+    const uint32_t nv = static_cast<uint32_t>(p.nv);
     if (lane == 0) {
-      uint32_t iq = 0, iv = 0, nb = 0;
+      uint32_t iq = 0, nb = 0;
       bool ok = true;
-      for (int T = 0; T <= ntiles && ok; ++T) {
-        if (T < ntiles) {
-          const int rb = static_cast<int>(blockIdx.x) + (T / p.n_kt) * static_cast<int>(gridDim.x);
-          const int kt = T % p.n_kt;
-          const int slot = T % NBIAS;
-          if (!(ok = wait_bar(&bias_empty[slot], ((T / NBIAS) & 1) ^ 1u, abort_flag, p.fault))) break;
-          b4::mbar_arrive_expect_tx(&bias_full[slot], BN * 4);
-          bulk_load_1d(bias_sm[slot], p.kbias + static_cast<int64_t>(kt) * BN, BN * 4, &bias_full[slot]);
-          ++nb;
-          for (int kc = 0; kc < p.n_kc; ++kc, ++iq) {
-            const int s = static_cast<int>(iq % NQK);
-            if (!(ok = wait_bar(&qk_empty[s], ((iq / NQK) & 1u) ^ 1u, abort_flag, p.fault))) break;
-            unsigned char* st = qk_sm + s * QK_BYTES;
-            b4::mbar_arrive_expect_tx(&qk_full[s], QK_BYTES);
-            b4::tma_load_2d(st, &p.qmap, &qk_full[s], kc * KC, rb * BM);
-            b4::tma_load_2d(st + A_BYTES, &p.kmap, &qk_full[s], kc * KC, kt * BN);
-          }
-          if (!ok) break;
-        }
-        if (T > 0) {
-          const int kt = (T - 1) % p.n_kt;
-          for (int c = 0; c < BN / KC; ++c, ++iv) {
-            const int s = static_cast<int>(iv % NV);
-            if (!(ok = wait_bar(&v_empty[s], ((iv / NV) & 1u) ^ 1u, abort_flag, p.fault))) break;
-            b4::mbar_arrive_expect_tx(&v_full[s], static_cast<uint32_t>(p.dv) * KC * 4);
-            b4::tma_load_2d(v_sm + s * V_BYTES, &p.vmap, &v_full[s], kt * BN + c * KC, p.v0);
-          }
+      for (int T = 0; T < ntiles && ok; ++T) {
+        const int rb = static_cast<int>(blockIdx.x) + (T / p.n_kt) * static_cast<int>(gridDim.x);
+        const int kt = T % p.n_kt;
+        const int slot = T % NBIAS;
+        if (!(ok = wait_bar(&bias_empty[slot], ((T / NBIAS) & 1) ^ 1u, abort_flag, p.fault))) break;
+        b4::mbar_arrive_expect_tx(&bias_full[slot], BN * 4);
+        bulk_load_1d(bias_sm[slot], p.kbias + static_cast<int64_t>(kt) * BN, BN * 4, &bias_full[slot]);
+        ++nb;
+        for (int kc = 0; kc < p.n_kc; ++kc, ++iq) {
+          const int s = static_cast<int>(iq % NQK);
+          if (!(ok = wait_bar(&qk_empty[s], ((iq / NQK) & 1u) ^ 1u, abort_flag, p.fault))) break;
+          unsigned char* st = qk_sm + s * QK_BYTES;
+          b4::mbar_arrive_expect_tx(&qk_full[s], QK_BYTES);
+          b4::tma_load_2d(st, &p.qmap, &qk_full[s], kc * KC, rb * BM);
+          b4::tma_load_2d(st + A_BYTES, &p.kmap, &qk_full[s], kc * KC, kt * BN);
         }
       }
       // every issued copy lands before the CTA may exit
       for (uint32_t j = iq > NQK ? iq - NQK : 0u; j < iq; ++j)
         b4::mbar_wait(&qk_full[j % NQK], (j / NQK) & 1u, kWaitLimitNs);
-      for (uint32_t j = iv > NV ? iv - NV : 0u; j < iv; ++j)
-        b4::mbar_wait(&v_full[j % NV], (j / NV) & 1u, kWaitLimitNs);
       for (uint32_t j = nb > NBIAS ? nb - NBIAS : 0u; j < nb; ++j)
         b4::mbar_wait(&bias_full[j % NBIAS], (j / NBIAS) & 1u, kWaitLimitNs);
+    } else if (lane == 1) {
+      uint32_t iv = 0;
+      bool ok = true;
+      for (int T = 0; T < ntiles && ok; ++T) {
+        const int kt = T % p.n_kt;
+        for (int c = 0; c < BN / KC; ++c, ++iv) {
+          const uint32_t s = iv % nv;
+          if (!(ok = wait_bar(&v_empty[s], ((iv / nv) & 1u) ^ 1u, abort_flag, p.fault))) break;
+          b4::mbar_arrive_expect_tx(&v_full[s], vbytes);
+          b4::tma_load_2d(v_sm + s * vbytes, &p.vmap, &v_full[s], kt * BN + c * KC, p.v0);
+        }
+      }
+      for (uint32_t j = iv > nv ? iv - nv : 0u; j < iv; ++j)
+        b4::mbar_wait(&v_full[j % nv], (j / nv) & 1u, kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t id_s = idesc_tf32_n(BN), id_o = idesc_tf32_n(p.dv);
+      const uint32_t vbytes = static_cast<uint32_t>(p.dv) * KC * 4;
+      const uint32_t nv = static_cast<uint32_t>(p.nv);
       uint32_t iq = 0, iv = 0;
       bool ok = true;
       for (int T = 0; T <= ntiles && ok; ++T) {
         if (T < ntiles) {
-          const int buf = T & 1;
-          const uint32_t use = static_cast<uint32_t>(T) >> 1;
+          const int buf = static_cast<int>(static_cast<uint32_t>(T) % nbuf);
+          const uint32_t use = static_cast<uint32_t>(T) / nbuf;
           if (!(ok = wait_bar(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.fault))) break;
           tc_fence_after();
           const uint32_t d_s = tmem + static_cast<uint32_t>(buf * BN);
@@ -268,20 +317,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
           if (!(ok = wait_bar(&p_full, static_cast<uint32_t>(U) & 1u, abort_flag, p.fault))) break;
           tc_fence_after();
           for (int c = 0; c < BN / KC; ++c, ++iv) {
-            const int s = static_cast<int>(iv % NV);
-            if (!(ok = wait_bar(&v_full[s], (iv / NV) & 1u, abort_flag, p.fault))) break;
+            const uint32_t s = iv % nv;
+            if (!(ok = wait_bar(&v_full[s], (iv / nv) & 1u, abort_flag, p.fault))) break;
             tc_fence_after();
-            const uint64_t dp = desc_sw128_kmajor(b4::smem_addr(p_sm + c * PC_BYTES));
-            const uint64_t dv = desc_sw128_kmajor(b4::smem_addr(v_sm + s * V_BYTES));
+            const uint32_t pa = tmem + (static_cast<uint32_t>(U) % nbuf) * BN + c * KC;
+            const uint64_t dv = desc_sw128_kmajor(b4::smem_addr(v_sm + s * vbytes));
 #pragma unroll
             for (int kk = 0; kk < KC / KSTEP; ++kk) {
               const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
-              mma_tf32(tmem + O_COL, dp + adv, dv + adv, id_o, !(first && c == 0 && kk == 0));
+              mma_tf32_ts(tmem + o_col, pa + static_cast<uint32_t>(kk * KSTEP), dv + adv, id_o,
+                          !(first && c == 0 && kk == 0));
             }
             mma_commit(&v_empty[s]);
           }
           if (!ok) break;
-          mma_commit(&p_empty);  // the P buffer may be rewritten once these MMAs are done
+          mma_commit(&acc_empty[static_cast<uint32_t>(U) % nbuf]);  // the S / P buffer is free once these MMAs are done
           if (last) mma_commit(&o_full);
         }
       }
@@ -296,7 +346,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     const int grp = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    unsigned char* p_row = p_sm + grp * PC_BYTES + row * 128;
     uint32_t T = 0;
     for (int rbl = 0; rbl < my_rb; ++rbl) {
       const int rb = static_cast<int>(blockIdx.x) + rbl * static_cast<int>(gridDim.x);
@@ -305,60 +354,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       float mass = 0.0f;
       bool ok = true;
       for (int kt = 0; kt < p.n_kt; ++kt, ++T) {
-        const int buf = static_cast<int>(T & 1u);
+        const int buf = static_cast<int>(T % nbuf);
         const int slot = static_cast<int>(T % NBIAS);
-        ok = wait_bar(&acc_full[buf], (T >> 1) & 1u, abort_flag, p.fault) &&
+        ok = wait_bar(&acc_full[buf], (T / nbuf) & 1u, abort_flag, p.fault) &&
              wait_bar(&bias_full[slot], (T / NBIAS) & 1u, abort_flag, p.fault);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(buf * BN + grp * KC), v);
+        // this warp's CPG chunks: the next chunk's TMEM load overlaps the
+        // current one's arithmetic; P is stored over S in place
+        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(buf * BN + grp * CPG * KC);
+        const float4* kb = reinterpret_cast<const float4*>(&bias_sm[slot][grp * CPG * KC]);
+        uint32_t v[32], w[32];
+        tmem_ld32(taddr, v);
         tmem_wait32(v);
-        const float4* kb = reinterpret_cast<const float4*>(&bias_sm[slot][grp * KC]);
-        const float2 cc = make_float2(p.c1, p.c1);
-        const float2 rr = make_float2(rt, rt);
-        float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                         make_float2(0.0f, 0.0f)};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 b = kb[i];
-          float2 s0 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])),
-                                 cc, __fadd2_rn(make_float2(b.x, b.y), rr));
-          float2 s1 =
-              __ffma2_rn(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), cc,
-                         __fadd2_rn(make_float2(b.z, b.w), rr));
-          s0.x = b4::ex2(s0.x);
-          s0.y = b4::ex2(s0.y);
-          s1.x = b4::ex2(s1.x);
-          s1.y = b4::ex2(s1.y);
-          acc[(2 * i) & 3] = __fadd2_rn(acc[(2 * i) & 3], s0);
-          acc[(2 * i + 1) & 3] = __fadd2_rn(acc[(2 * i + 1) & 3], s1);
-          v[4 * i] = __float_as_uint(s0.x);
-          v[4 * i + 1] = __float_as_uint(s0.y);
-          v[4 * i + 2] = __float_as_uint(s1.x);
-          v[4 * i + 3] = __float_as_uint(s1.y);
+        for (int ch = 0; ch < CPG; ++ch) {
+          if (ch + 1 < CPG) tmem_ld32(taddr + static_cast<uint32_t>((ch + 1) * KC), w);
+          mass += p_chunk(v, kb + ch * 8, p.c1, rt);
+          tmem_st32(taddr + static_cast<uint32_t>(ch * KC), v);
+          if (ch + 1 < CPG) {
+            tmem_wait32(w);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = w[i];
+          }
         }
-        const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        mass += t.x + t.y;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&acc_empty[buf]);
+          mbar_arrive(&p_full);
           mbar_arrive(&bias_empty[slot]);
         }
-        // the P buffer is free once the MMAs of the previous tile have read it
-        ok = wait_bar(&p_empty, (T & 1u) ^ 1u, abort_flag, p.fault);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        // this row's 32 keys as one 128-byte row of the swizzled K-major tile
-#pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16)
-          *reinterpret_cast<uint4*>(p_row + ((c16 ^ (row & 7)) << 4)) =
-              make_uint4(v[4 * c16], v[4 * c16 + 1], v[4 * c16 + 2], v[4 * c16 + 3]);
-        b4::fence_async_smem();  // visible to the tensor cores' reads
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full);
       }
       if (ok) {
         ok = wait_bar(&o_full, static_cast<uint32_t>(rbl) & 1u, abort_flag, p.fault);
@@ -366,13 +392,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       }
       if (ok) {
         tc_fence_after();
-        if (grp * KC < p.dv) {
+        for (int c = grp; c * KC < p.dv; c += GROUPS) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(O_COL + grp * KC), o);
+          tmem_ld32(tmem + lane_base + o_col + static_cast<uint32_t>(c * KC), o);
           tmem_wait32(o);
           if (r < p.nq) {
             float* orow = p.out + r * p.d;
-            const int c0 = p.v0 + grp * KC;
+            const int c0 = p.v0 + c * KC;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (c0 + i < p.d) orow[c0 + i] = __uint_as_float(o[i]);
@@ -387,7 +413,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       if (grp > 0) mass_sh[grp - 1][row] = mass;
       named_bar_sync(1, 32 * NEPI);
       if (grp == 0 && ok && !*abort_flag && p.mass != nullptr && r < p.nq)
-        p.mass[r] = mass + mass_sh[0][row] + mass_sh[1][row] + mass_sh[2][row];
+        p.mass[r] = [&] {
+          float m = mass;
+#pragma unroll
+          for (int g = 0; g < GROUPS - 1; ++g) m += mass_sh[g][row];
+          return m;
+        }();
       named_bar_sync(1, 32 * NEPI);
       if (*abort_flag) break;
     }
@@ -471,6 +502,8 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const fl
   }
   p.v0 = v0;
   p.dv = dv;
+  p.nv = std::min(tr::NV_MAX, tr::V_REGION / (dv * eot::KC * 4));
+  p.nbuf = (EOT_TR_NBUF3 != 0 && dv <= 128) ? 3 : 2;
   p.mass = mass;
   const int grid = std::min(p.n_rb, nsm);
   tr::transport_kernel<<<grid, tr::NTHREADS, tr::SMEM, stream>>>(p);
@@ -540,7 +573,7 @@ extern "C" int eot_transport(const float* X, const float* Y, const float* f, con
   p.n_kc = L.d_pad / eot::KC;
   p.c1 = static_cast<float>(2.0 * 1.4426950408889634 / eps);
   p.fault = fault;
-  // one launch per slice of up to 128 value coordinates; the first also
+  // one launch per slice of up to 256 value coordinates; the first also
   // writes the row masses
   for (int32_t v0 = 0; v0 < L.d_pad && e == cudaSuccess; v0 += eot::tr::DV) {
     const int32_t dv = std::min<int32_t>(eot::tr::DV, L.d_pad - v0);

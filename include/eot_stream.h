@@ -89,8 +89,9 @@ int eot_sinkhorn(const float *X, const float *Y, const float *log_a, const float
  * running maximum is needed.  Otherwise pi is evaluated as given, and
  * potentials far from consistent can overflow.
  * Arithmetic: TF32 products with fp32 accumulation for both chained
- * products (S = X Y^T, then pi Y); exponentials and masses in fp32.  The
- * value coordinates are processed 128 at a time, one launch each.
+ * products (S = X Y^T, then pi Y, with pi held in tensor memory);
+ * exponentials and masses in fp32.  The value coordinates are processed 256
+ * at a time, one launch each.
  * Workspace: eot_transport_workspace_bytes(n, m, d), 256-byte aligned.
  * Errors as for eot_update; PY, mass must not alias the inputs or each
  * other, grad may be NULL. */
