@@ -347,7 +347,14 @@ def main():
         "wall_s": wall,
     }
     if not args.no_e2e:
-        line["e2e"] = e2e_host(b4, X, G, dev, steps=3)
+        # two public host-memory paths: the kernel reading and writing pinned
+        # host memory itself (zero copy) and chunked copies on the copy
+        # engines; the faster is the e2e figure, the other is reported beside it
+        mapped = e2e_mapped(b4, X, G, dev, steps=3)
+        copies = e2e_host(b4, X, G, dev, steps=3)
+        best, other = (mapped, copies) if mapped["value"] >= copies["value"] else (copies, mapped)
+        best["other_path"] = {k: other[k] for k in ("api", "value", "ms_per_step", "host_link_gbs")}
+        line["e2e"] = best
     if not args.no_cpu_baseline:
         idx = slice(0, 1 << 22)
         line["cpu_baseline"] = cpu_baseline(X[idx].double().cpu().numpy(),
@@ -576,6 +583,38 @@ def bind_to_gpu_numa_node(dev) -> str:
         return "node %d (%d cores)" % (node, len(sel))
     except (OSError, ValueError, AttributeError) as e:
         return "unbound (%s)" % type(e).__name__
+
+
+def e2e_mapped(b4, X, G, dev, steps=3):
+    """The step on host-resident tokens without copies
+    (birkhoff4_forward_backward_mapped): the kernel reads pinned host X and dP
+    and writes P and dX back to pinned host memory over the host link; every
+    byte crosses the link inside the timed region."""
+    import torch
+
+    numa = bind_to_gpu_numa_node(dev)
+    T = X.shape[0]
+    Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    Gh = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
+    Ph = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    dXh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    Xh.copy_(X)
+    Gh.copy_(G)
+    b4.forward_backward_mapped(Xh, Gh, Ph, dXh, device=dev)
+    torch.cuda.synchronize(dev)
+    s = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        b4.forward_backward_mapped(Xh, Gh, Ph, dXh, device=dev)
+    e1.record(s)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = X.numel() * X.element_size()
+    return {"value": T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": 2 * nbytes,
+            "d2h_bytes_per_step": 2 * nbytes, "ms_per_step": ms, "steps": steps,
+            "host_link_gbs": 4 * nbytes / (ms * 1e-3) / 1e9,
+            "api": "birkhoff4_forward_backward_mapped (zero copy, fused pass)", "numa": numa}
 
 
 def e2e_host(b4, X, G, dev, steps=3, nstreams=4, chunk=1 << 21):

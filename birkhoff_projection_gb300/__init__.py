@@ -24,7 +24,7 @@ from . import _lib
 from ._lib import B4_BF16, B4_F32, Birkhoff4Error, Opts, check, lib
 
 __all__ = ["project", "forward", "backward", "forward_backward", "forward_backward_host",
-           "forward_nxn", "backward_nxn", "sinkhorn", "Birkhoff4Error", "lib", "Projection"]
+           "forward_nxn", "backward_nxn", "forward_backward_mapped", "sinkhorn", "Birkhoff4Error", "lib", "Projection"]
 
 _DT = {torch.float32: B4_F32, torch.bfloat16: B4_BF16}
 
@@ -198,6 +198,29 @@ def forward_backward_host(X: torch.Tensor, dP: torch.Tensor, P_out, dX_out: torc
         done.record(s)
         cur.wait_event(done)
         workspace.record_stream(s)
+
+
+def forward_backward_mapped(X: torch.Tensor, dP: torch.Tensor, P_out, dX_out: torch.Tensor, *,
+                            device=None):
+    """Forward + backward of host-resident tokens without copies
+    (birkhoff4_forward_backward_mapped): the kernel on `device` reads X and
+    dP and writes P_out (or None) and dX_out in place in pinned host memory.
+    Enqueued on the device's current stream; synchronize before reading the
+    outputs."""
+    T = X.numel() // 16
+    for name, t in (("X", X), ("dP", dP), ("dX_out", dX_out)) + ((("P_out", P_out),) if P_out is not None else ()):
+        if t.is_cuda or t.dtype != X.dtype or t.numel() != X.numel() or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CPU tensor like X" % name)
+        if not t.is_pinned():
+            raise ValueError("%s must be in pinned host memory" % name)
+    if X.dtype not in _DT:
+        raise TypeError("X must be float32 or bfloat16")
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        check(lib().birkhoff4_forward_backward_mapped(
+            _ptr(X), _ptr(dP), _ptr(P_out), _ptr(dX_out), T, _DT[X.dtype],
+            ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)),
+            "birkhoff4_forward_backward_mapped")
 
 
 def host_workspace(device, dtype, chunk_tokens: int = 1 << 22, nstreams: int = 3) -> torch.Tensor:

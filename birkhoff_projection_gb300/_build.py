@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(PKG, "libbirkhoff4.so")
 
 SOURCES = ["birkhoff4_api.cu", "k_forward.cu", "k_backward.cu", "k_fused.cu", "k_sinkhorn.cu",
            "birkhoff4_noalloc.cu", "k_nxn.cu", "eot_stream.cu",
-           "eot_transport.cu"]
+           "eot_transport.cu", "k_mapped.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I", CSRC, "-I", INCLUDE]

@@ -34,6 +34,7 @@ SIGNATURES = {
     "birkhoff4_forward_backward_host_static": (_int, [_vp, _vp, _vp, _vp, _i64, ctypes.c_int32,
                                                       _i64, _vp, ctypes.c_int32]),
     "birkhoff4_forward_nxn": (_int, [_vp, _vp, _vp, ctypes.c_int32, _i64, _vp]),
+    "birkhoff4_forward_backward_mapped": (_int, [_vp, _vp, _vp, _vp, _i64, ctypes.c_int32, _vp]),
     "eot_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, ctypes.c_int32, ctypes.c_int32]),
     "eot_update": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int32, ctypes.c_float,
                           ctypes.c_int32, _vp, ctypes.c_size_t, _vp]),

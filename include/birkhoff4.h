@@ -219,6 +219,27 @@ int birkhoff4_forward_backward_host_static(const void *X_h, const void *dP_h, vo
                                            const birkhoff4_stream_t *streams, int32_t nstreams);
 
 /* ---------------------------------------------------------------------- */
+/* Host-resident tokens, zero copy [mHC s2.1, s2.2; batched as in s2.3]:   */
+/* the fused forward + backward on tokens that stay in page-locked host    */
+/* memory.  The kernel reads X and dP and writes P and dX over the host    */
+/* link itself: no device buffer and no cudaMemcpy.  On a GPU whose host   */
+/* memory is coherently attached (GB300: NVLink-C2C) the SMs' own loads    */
+/* and stores can outrun the copy engines.  Same layouts and dtypes as     */
+/* birkhoff4_forward_backward_host.  Every buffer must be host memory the */
+/* device can address: page-locked and mapped (cudaHostAlloc /             */
+/* cudaMallocHost, or cudaHostRegister with cudaHostRegisterMapped), or,   */
+/* on systems where the GPU addresses all host memory (Grace-based GB300), */
+/* any host memory.  If cudaHostGetDevicePointer refuses a buffer,         */
+/* B4_EINVAL is returned (birkhoff4_last_cuda_error has the code) and      */
+/* nothing runs.  P_h may be                                               */
+/* NULL (P not written); in-place use (P_h == X_h, dX_h == dP_h) is        */
+/* allowed.  Asynchronous on `stream`: the host must not touch the buffers */
+/* until the stream has been synchronised.                                 */
+/* ---------------------------------------------------------------------- */
+int birkhoff4_forward_backward_mapped(const void *X_h, const void *dP_h, void *P_h, void *dX_h,
+                                      int64_t T, int32_t dtype, birkhoff4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* Reference: fixed-iteration Sinkhorn-Knopp [mHC s1], the scheme current  */
 /* mHC uses (e.g. iters = 20), kept for the accuracy comparison.           */
 /* Log domain, b = 0 start; one iteration is a row normalisation           */

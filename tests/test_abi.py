@@ -121,6 +121,16 @@ def test_eot_arguments_are_checked(L):
     assert sk(n=0, m=0) == _lib.B4_OK
 
 
+def test_mapped_arguments_are_checked(L):
+    f = L.birkhoff4_forward_backward_mapped
+    assert f(FAKE, FAKE, FAKE, FAKE, -1, 0, None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 2, None) == _lib.B4_EINVAL
+    assert f(None, FAKE, FAKE, FAKE, 4, 0, None) == _lib.B4_EINVAL
+    assert f(FAKE, None, FAKE, FAKE, 4, 0, None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, FAKE, None, 4, 0, None) == _lib.B4_EINVAL
+    assert f(None, None, None, None, 0, 0, None) == _lib.B4_OK
+
+
 def test_eot_transport_arguments_are_checked(L):
     f32 = ctypes.c_float
     need = L.eot_transport_workspace_bytes(100, 200, 64)

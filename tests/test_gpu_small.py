@@ -295,3 +295,44 @@ def test_cuda_graph_capture_and_replay():
         Pe = b4.forward(X)
         assert torch.equal(P, Pe)
         assert torch.equal(dX, b4.backward(G, P=Pe))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T", [1, 129, 5000])
+@pytest.mark.parametrize("with_P", [True, False])
+def test_mapped_host_api(dtype, T, with_P):
+    """birkhoff4_forward_backward_mapped: the kernel reads and writes pinned
+    host tokens in place and gives exactly the device pass's results."""
+    X = normal(T, seed=26).to(dtype)
+    G = normal(T, seed=27).to(dtype)
+    P, dX = b4.forward_backward(X, G)
+    Xh, Gh = X.cpu().pin_memory(), G.cpu().pin_memory()
+    Ph = torch.empty_like(Xh).pin_memory() if with_P else None
+    dXh = torch.empty_like(Xh).pin_memory()
+    b4.forward_backward_mapped(Xh, Gh, Ph, dXh, device=DEV)
+    torch.cuda.synchronize()
+    if with_P:
+        assert torch.equal(Ph, P.cpu())
+    assert torch.equal(dXh, dX.cpu())
+
+
+def test_mapped_host_in_place_and_pageable_memory():
+    T = 3000
+    X, G = normal(T, seed=28), normal(T, seed=29)
+    P, dX = b4.forward_backward(X, G)
+    Xh, Gh = X.cpu().pin_memory(), G.cpu().pin_memory()
+    b4.forward_backward_mapped(Xh, Gh, Xh, Gh, device=DEV)  # P over X, dX over dP
+    torch.cuda.synchronize()
+    assert torch.equal(Xh, P.cpu()) and torch.equal(Gh, dX.cpu())
+    # pageable host memory: refused before anything runs where the device
+    # cannot address it, or processed in place where it can (Grace-based
+    # systems address all host memory)
+    Xp, Gp, Dp = X.cpu(), G.cpu(), torch.empty(T, 4, 4)
+    L = _lib.lib()
+    st = L.birkhoff4_forward_backward_mapped(ctypes.c_void_p(Xp.data_ptr()), ctypes.c_void_p(Gp.data_ptr()),
+                                             None, ctypes.c_void_p(Dp.data_ptr()), T, _lib.B4_F32, None)
+    assert st in (_lib.B4_OK, _lib.B4_EINVAL)
+    if st == _lib.B4_OK:
+        torch.cuda.synchronize()
+        assert torch.equal(Dp, dX.cpu())
+    assert float(b4.forward(X[:4]).sum()) > 0  # the context is still usable
