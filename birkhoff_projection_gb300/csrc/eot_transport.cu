@@ -440,22 +440,23 @@ namespace {
 
 struct TrLayout {
   int64_t n_pad, m_pad;
-  int32_t d_pad;
-  size_t x, y, yt, xn, yn, kb, rt, total;  // byte offsets
+  int32_t d_pad, v_pad;
+  size_t x, y, yt, xn, yn, kb, rt, total;  // byte offsets (yt: the values, transposed)
 };
 
-TrLayout tr_layout(int64_t n, int64_t m, int32_t d) {
+TrLayout tr_layout(int64_t n, int64_t m, int32_t d, int32_t dv) {
   TrLayout L;
   L.n_pad = round_up(std::max<int64_t>(n, 1), ROW_PAD);
   L.m_pad = round_up(std::max<int64_t>(m, 1), ROW_PAD);
   L.d_pad = static_cast<int32_t>(round_up(d, KC));
+  L.v_pad = static_cast<int32_t>(round_up(dv, KC));
   size_t o = 0;
   L.x = o;
   o += align_bytes(static_cast<size_t>(L.n_pad) * L.d_pad * 4);
   L.y = o;
   o += align_bytes(static_cast<size_t>(L.m_pad) * L.d_pad * 4);
   L.yt = o;
-  o += align_bytes(static_cast<size_t>(L.m_pad) * L.d_pad * 4);
+  o += align_bytes(static_cast<size_t>(L.m_pad) * L.v_pad * 4);
   L.xn = o;
   o += align_bytes(static_cast<size_t>(L.n_pad) * 4);
   L.yn = o;
@@ -468,8 +469,9 @@ TrLayout tr_layout(int64_t n, int64_t m, int32_t d) {
   return L;
 }
 
-bool tr_sizes_ok(int64_t n, int64_t m, int32_t d) {
-  return n >= 0 && m >= 0 && n <= kMaxPoints && m <= kMaxPoints && d >= 1 && d <= 16384;
+bool tr_sizes_ok(int64_t n, int64_t m, int32_t d, int32_t dv) {
+  return n >= 0 && m >= 0 && n <= kMaxPoints && m <= kMaxPoints && d >= 1 && d <= 16384 &&
+         dv >= 1 && dv <= 16384;
 }
 
 cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const float* yt, int32_t v0,
@@ -491,7 +493,7 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const fl
   {
     b4::EncodeTiledFn fn = b4::encode_fn();
     if (fn == nullptr) return cudaErrorInvalidValue;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.m_pad), static_cast<cuuint64_t>(L.d_pad)};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.m_pad), static_cast<cuuint64_t>(L.v_pad)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.m_pad) * 4};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(KC), static_cast<cuuint32_t>(dv)};
     const cuuint32_t estr[2] = {1, 1};
@@ -510,80 +512,102 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const fl
   return cudaGetLastError();
 }
 
-}  // namespace
-}  // namespace eot
-
-extern "C" size_t eot_transport_workspace_bytes(int64_t n, int64_t m, int32_t d) {
-  if (!eot::tr_sizes_ok(n, m, d)) return 0;
-  return eot::tr_layout(n, m, d).total;
-}
-
-extern "C" int eot_transport(const float* X, const float* Y, const float* f, const float* g,
-                             const float* log_a, const float* log_b, float* PY, float* mass,
-                             float* grad, int64_t n, int64_t m, int32_t d, float eps,
-                             void* workspace, size_t workspace_bytes, birkhoff4_stream_t stream) {
-  if (!eot::tr_sizes_ok(n, m, d) || !(eps > 0.0f) || !std::isfinite(eps)) return B4_EINVAL;
+// The plan of (f, g) applied to the values V [m, dv]: out = pi V, mass =
+// pi 1.
+int apply_impl(const float* X, const float* Y, const float* f, const float* g, const float* log_a,
+               const float* log_b, const float* V, int32_t dv, float* out, float* mass, int64_t n,
+               int64_t m, int32_t d, float eps, void* workspace, size_t workspace_bytes,
+               cudaStream_t s) {
+  if (!tr_sizes_ok(n, m, d, dv) || !(eps > 0.0f) || !std::isfinite(eps)) return B4_EINVAL;
   if (n == 0) return B4_OK;
   if (m == 0) return B4_EINVAL;
   if (X == nullptr || Y == nullptr || f == nullptr || g == nullptr || log_a == nullptr ||
-      log_b == nullptr || PY == nullptr || mass == nullptr)
+      log_b == nullptr || V == nullptr || out == nullptr || mass == nullptr)
     return B4_EINVAL;
-  const eot::TrLayout L = eot::tr_layout(n, m, d);
+  const TrLayout L = tr_layout(n, m, d, dv);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < L.total)
     return B4_EINVAL;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   unsigned int* fault = b4::device_fault_latch(&e);
   if (e != cudaSuccess) return b4::record_cuda_error(e);
   unsigned char* w = static_cast<unsigned char*>(workspace);
   float* xp = reinterpret_cast<float*>(w + L.x);
   float* yp = reinterpret_cast<float*>(w + L.y);
-  float* ytp = reinterpret_cast<float*>(w + L.yt);
+  float* vt = reinterpret_cast<float*>(w + L.yt);
   float* xn = reinterpret_cast<float*>(w + L.xn);
   float* yn = reinterpret_cast<float*>(w + L.yn);
   float* kb = reinterpret_cast<float*>(w + L.kb);
   float* rt = reinterpret_cast<float*>(w + L.rt);
-  e = eot::pack(X, n, d, L.n_pad, L.d_pad, xp, nullptr, xn, s);
-  if (e == cudaSuccess) e = eot::pack(Y, m, d, L.m_pad, L.d_pad, yp, nullptr, yn, s);
+  e = pack(X, n, d, L.n_pad, L.d_pad, xp, nullptr, xn, s);
+  if (e == cudaSuccess) e = pack(Y, m, d, L.m_pad, L.d_pad, yp, nullptr, yn, s);
   if (e == cudaSuccess) {
-    const dim3 grid(static_cast<unsigned>(L.m_pad / 32), static_cast<unsigned>(L.d_pad / 32));
-    eot::tr::pack_transposed_kernel<<<grid, dim3(32, 8), 0, s>>>(Y, m, d, L.m_pad, L.d_pad, ytp);
+    const dim3 grid(static_cast<unsigned>(L.m_pad / 32), static_cast<unsigned>(L.v_pad / 32));
+    tr::pack_transposed_kernel<<<grid, dim3(32, 8), 0, s>>>(V, m, dv, L.m_pad, L.v_pad, vt);
     e = cudaGetLastError();
   }
-  if (e == cudaSuccess) e = eot::bias(g, log_b, yn, m, L.m_pad, eps, kb, s);
+  if (e == cudaSuccess) e = bias(g, log_b, yn, m, L.m_pad, eps, kb, s);
   if (e == cudaSuccess) {
-    eot::tr::rowterm_kernel<<<static_cast<unsigned>((L.n_pad + 255) / 256), 256, 0, s>>>(
+    tr::rowterm_kernel<<<static_cast<unsigned>((L.n_pad + 255) / 256), 256, 0, s>>>(
         f, log_a, xn, n, L.n_pad, static_cast<float>(1.4426950408889634 / eps), rt);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return b4::record_cuda_error(e);
-  eot::tr::Params p;
-  if (!eot::encode_rows128(&p.qmap, xp, L.n_pad, L.d_pad, eot::BM) ||
-      !eot::encode_rows128(&p.kmap, yp, L.m_pad, L.d_pad, eot::tr::BN))
+  tr::Params p;
+  if (!encode_rows128(&p.qmap, xp, L.n_pad, L.d_pad, BM) ||
+      !encode_rows128(&p.kmap, yp, L.m_pad, L.d_pad, tr::BN))
     return b4::record_cuda_error(cudaErrorInvalidValue);
   p.kbias = kb;
   p.rowterm = rt;
-  p.out = PY;
+  p.out = out;
   p.mass = nullptr;
   p.nq = n;
-  p.d = d;
-  p.n_rb = static_cast<int32_t>(L.n_pad / eot::BM);
-  p.n_kt = static_cast<int32_t>(L.m_pad / eot::tr::BN);
-  p.n_kc = L.d_pad / eot::KC;
+  p.d = dv;
+  p.n_rb = static_cast<int32_t>(L.n_pad / BM);
+  p.n_kt = static_cast<int32_t>(L.m_pad / tr::BN);
+  p.n_kc = L.d_pad / KC;
   p.c1 = static_cast<float>(2.0 * 1.4426950408889634 / eps);
   p.fault = fault;
   // one launch per slice of up to 256 value coordinates; the first also
   // writes the row masses
-  for (int32_t v0 = 0; v0 < L.d_pad && e == cudaSuccess; v0 += eot::tr::DV) {
-    const int32_t dv = std::min<int32_t>(eot::tr::DV, L.d_pad - v0);
-    e = eot::launch_transport(p, L, ytp, v0, dv, v0 == 0 ? mass : nullptr, s);
-  }
-  if (e == cudaSuccess && grad != nullptr) {
-    const int64_t total = n * static_cast<int64_t>(d);
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, 1 << 20);
-    eot::tr::grad_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(X, PY, mass, n, d, grad);
-    e = cudaGetLastError();
+  for (int32_t v0 = 0; v0 < L.v_pad && e == cudaSuccess; v0 += tr::DV) {
+    const int32_t w_slice = std::min<int32_t>(tr::DV, L.v_pad - v0);
+    e = launch_transport(p, L, vt, v0, w_slice, v0 == 0 ? mass : nullptr, s);
   }
   return b4::record_cuda_error(e);
+}
+
+}  // namespace
+}  // namespace eot
+
+extern "C" size_t eot_transport_workspace_bytes(int64_t n, int64_t m, int32_t d) {
+  if (!eot::tr_sizes_ok(n, m, d, d)) return 0;
+  return eot::tr_layout(n, m, d, d).total;
+}
+
+extern "C" size_t eot_apply_plan_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t dv) {
+  if (!eot::tr_sizes_ok(n, m, d, dv)) return 0;
+  return eot::tr_layout(n, m, d, dv).total;
+}
+
+extern "C" int eot_apply_plan(const float* X, const float* Y, const float* f, const float* g,
+                              const float* log_a, const float* log_b, const float* V, int32_t dv,
+                              float* out, float* mass, int64_t n, int64_t m, int32_t d, float eps,
+                              void* workspace, size_t workspace_bytes, birkhoff4_stream_t stream) {
+  return eot::apply_impl(X, Y, f, g, log_a, log_b, V, dv, out, mass, n, m, d, eps, workspace,
+                         workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int eot_transport(const float* X, const float* Y, const float* f, const float* g,
+                             const float* log_a, const float* log_b, float* PY, float* mass,
+                             float* grad, int64_t n, int64_t m, int32_t d, float eps,
+                             void* workspace, size_t workspace_bytes, birkhoff4_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int st = eot::apply_impl(X, Y, f, g, log_a, log_b, Y, d, PY, mass, n, m, d, eps, workspace,
+                                 workspace_bytes, s);
+  if (st != B4_OK || n == 0 || grad == nullptr) return st;
+  const int64_t total = n * static_cast<int64_t>(d);
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, 1 << 20);
+  eot::tr::grad_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(X, PY, mass, n, d, grad);
+  return b4::record_cuda_error(cudaGetLastError());
 }

@@ -129,3 +129,34 @@ def transport(X: torch.Tensor, Y: torch.Tensor, f: torch.Tensor, g: torch.Tensor
                                   ws.numel(), _stream(X)),
               "eot_transport")
     return (PY, mass, grad) if want_grad else (PY, mass)
+
+
+def apply_plan(X: torch.Tensor, Y: torch.Tensor, f: torch.Tensor, g: torch.Tensor,
+               log_a: torch.Tensor, log_b: torch.Tensor, V: torch.Tensor, eps: float,
+               workspace: torch.Tensor = None):
+    """The plan of (f, g) applied to values V [m, dv] at the key points,
+    without forming it: returns (pi V [n, dv], pi 1 [n])."""
+    n = _points(X, "X")
+    m = _points(Y, "Y")
+    if Y.device != X.device or Y.shape[1] != X.shape[1]:
+        raise ValueError("X and Y must share the device and the dimension")
+    if _points(V, "V") != m or V.device != X.device:
+        raise ValueError("V must be [m, dv] on the device of X")
+    for t, name, k in ((f, "f", n), (g, "g", m), (log_a, "log_a", n), (log_b, "log_b", m)):
+        _vector(t, name, k, X.device)
+    d, dv = X.shape[1], V.shape[1]
+    need = lib().eot_apply_plan_workspace_bytes(n, m, d, dv)
+    if need == 0:
+        raise ValueError("invalid sizes")
+    ws = workspace if workspace is not None else torch.empty(need, dtype=torch.uint8,
+                                                             device=X.device)
+    if ws.numel() < need or ws.device != X.device:
+        raise ValueError("workspace needs %d bytes on %s" % (need, X.device))
+    out = torch.empty(n, dv, dtype=torch.float32, device=X.device)
+    mass = torch.empty(n, dtype=torch.float32, device=X.device)
+    with _on_device(X):
+        check(lib().eot_apply_plan(_ptr(X), _ptr(Y), _ptr(f), _ptr(g), _ptr(log_a), _ptr(log_b),
+                                   _ptr(V), dv, _ptr(out), _ptr(mass), n, m, d, float(eps),
+                                   _ptr(ws), ws.numel(), _stream(X)),
+              "eot_apply_plan")
+    return out, mass

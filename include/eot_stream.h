@@ -96,6 +96,18 @@ int eot_sinkhorn(const float *X, const float *Y, const float *log_a, const float
  * Errors as for eot_update; PY, mass must not alias the inputs or each
  * other, grad may be NULL. */
 size_t eot_transport_workspace_bytes(int64_t n, int64_t m, int32_t d);
+
+/* The plan of f and g applied to any values V [m, dv] (row-major fp32) at
+ * the key points [FlashSinkhorn, Methodik s3: the transport matrix applied
+ * without materialising it]: out [n, dv] = pi V, mass [n] = pi 1, with pi
+ * as for eot_transport (which is the case V = Y).  Same arithmetic, errors
+ * and conditions; the workspace is eot_apply_plan_workspace_bytes(n, m, d,
+ * dv) bytes. */
+size_t eot_apply_plan_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t dv);
+int eot_apply_plan(const float *X, const float *Y, const float *f, const float *g,
+                   const float *log_a, const float *log_b, const float *V, int32_t dv, float *out,
+                   float *mass, int64_t n, int64_t m, int32_t d, float eps, void *workspace,
+                   size_t workspace_bytes, birkhoff4_stream_t stream);
 int eot_transport(const float *X, const float *Y, const float *f, const float *g,
                   const float *log_a, const float *log_b, float *PY, float *mass, float *grad,
                   int64_t n, int64_t m, int32_t d, float eps, void *workspace,

@@ -131,3 +131,9 @@ def eot_cost64(X, Y, log_a, log_b, eps, iters):
     iterations from zero potentials (the dual value at convergence)."""
     f, g = sinkhorn64(X, Y, log_a, log_b, eps, iters)
     return float(f @ np.exp(_as64(log_a, "log_a", 1)) + g @ np.exp(_as64(log_b, "log_b", 1)))
+
+
+def apply_plan64(X, Y, f, g, log_a, log_b, eps, V):
+    """The plan of (f, g) applied to values V [m, dv]: (pi V, pi 1)."""
+    P = plan64(X, Y, f, g, log_a, log_b, eps)
+    return P @ np.asarray(V, dtype=np.float64), P.sum(1)

@@ -150,6 +150,13 @@ def test_eot_transport_arguments_are_checked(L):
     assert tr(w=ctypes.c_void_p(0x100080)) == _lib.B4_EINVAL
     assert tr(wb=need - 1) == _lib.B4_EINVAL
     assert tr(n=0, w=None, py=None, mass=None) == _lib.B4_OK
+    assert L.eot_apply_plan_workspace_bytes(100, 200, 64, 0) == 0
+    assert L.eot_apply_plan_workspace_bytes(100, 200, 64, 64) == need
+    ap = L.eot_apply_plan
+    assert ap(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 3, FAKE, FAKE, 100, 200, 64, f32(0.1),
+              ws, need, None) == _lib.B4_EINVAL
+    assert ap(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, 100, 200, 64, f32(0.1),
+              ws, need, None) == _lib.B4_EINVAL
 
 
 def test_bad_options_are_einval(L):

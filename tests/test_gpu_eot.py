@@ -225,3 +225,30 @@ def test_transport_full_size_sampled_rows():
     b_py, b_mass = transport_bounds(*args)
     assert np.all(np.abs(np64(PY)[rows] - PYr) <= b_py)
     assert np.all(np.abs(np64(mass)[rows] - mr) <= b_mass)
+
+
+@pytest.mark.parametrize("n,m,d,dv", [(700, 900, 16, 5), (300, 500, 64, 1), (257, 300, 8, 300)])
+def test_apply_plan_parity(n, m, d, dv):
+    """pi V for arbitrary values (an odd width, a single column, two
+    256-wide slices) against the oracle, within the bound of the transport
+    arithmetic with |V| in place of |Y|."""
+    eps = workloads.EOT_EPS
+    X, Y, log_a, log_b = workloads.eot_clouds(n, m, d, seed=n + m, device=DEV, random_weights=True)
+    gen = torch.Generator(device="cpu").manual_seed(dv)
+    V = torch.randn(m, dv, generator=gen).to(DEV)
+    f64, g64 = oeot.sinkhorn64(np64(X), np64(Y), np64(log_a), np64(log_b), eps, 20)
+    f = torch.tensor(f64, dtype=torch.float32, device=DEV)
+    g = torch.tensor(g64, dtype=torch.float32, device=DEV)
+    out, mass = eot.apply_plan(X, Y, f, g, log_a, log_b, V, eps)
+    args = (np64(X), np64(Y), np64(f), np64(g), np64(log_a), np64(log_b), eps)
+    ref, mr = oeot.apply_plan64(*args, np64(V))
+    fr = np.abs(np64(f)) + eps * np.abs(np64(log_a))
+    t = row_bound(np64(X), np64(Y), np64(g), np64(log_b), fr, eps, eot.TF32) / 2.0
+    rel = np.expm1(t / eps + 2.0 ** -20)
+    P = oeot.plan64(*args)
+    m_pad = -(-m // 256) * 256
+    bound = 2.0 * (rel + 2.0 ** -10 + 2.0 ** -11 + m_pad * 2.0 ** -23)[:, None] * (P @ np.abs(np64(V)))
+    assert np.all(np.abs(np64(out) - ref) <= bound)
+    assert np.all(np.abs(np64(mass) - mr) <= 2.0 * (rel + m_pad * 2.0 ** -23) * mr)
+    if dv == 1:
+        assert out.shape == (n, 1)

@@ -236,3 +236,14 @@ def test_planted_transport_mistake_fails():
     fd = (eot.eot_cost64(Xp, Y, la, lb, 0.5, 4000) - eot.eot_cost64(Xm, Y, la, lb, 0.5, 4000)) / (2 * h)
     assert abs(bad[0, 0] - fd) > 1e-3
     assert abs(eot.grad_x64(X, Y, f, g, la, lb, 0.5)[0, 0] - fd) <= 1e-8
+
+
+def test_apply_plan_is_linear_and_matches_transport():
+    X, Y = clouds(9, 11, 3, seed=25)
+    la, lb = uniform(9), uniform(11)
+    f, g = eot.sinkhorn64(X, Y, la, lb, 0.4, iters=200)
+    PY, r = eot.transport64(X, Y, f, g, la, lb, 0.4)
+    PV, r2 = eot.apply_plan64(X, Y, f, g, la, lb, 0.4, Y)
+    assert np.array_equal(PV, PY) and np.array_equal(r, r2)
+    ones, _ = eot.apply_plan64(X, Y, f, g, la, lb, 0.4, np.ones((11, 1)))
+    assert np.abs(ones[:, 0] - r).max() <= 1e-15
