@@ -6,7 +6,8 @@
 // start, row-max-shifted first evaluation, multiplicative re-evaluation with
 // a log-domain refresh every 8 steps, Laplacian-form Hessian and elimination,
 // step clamp 3 with Newton-decrement damping from the fifth step), written
-// for any n.  Tokens are staged through shared memory with plain coalesced
+// for any n; for n = 2 the single free dual variable has a closed form,
+// which the forward uses instead.  Tokens are staged through shared memory with plain coalesced
 // loads: n x n rows of n^2 * 4 bytes are not all multiples of 16 bytes, which
 // TMA tiles need.
 #pragma once
@@ -125,6 +126,33 @@ __device__ __forceinline__ void nxn_solve(float w[N][N], const float g[N - 1], f
 template <int N>
 __device__ __forceinline__ bool nxn_newton(const float* xs, float p[N * N], float beta[N],
                                            int& evals, const NewtonCfg& cfg) {
+  if constexpr (N == 2) {
+    // closed form: P = [[q, 1 - q], [1 - q, q]], q = sigma(u) with
+    // u = (x00 + x11 - x01 - x10) / 2 (the one free dual variable solves a
+    // scalar equation); b0 = (x01 + x11 - x00 - x10) / 2, b1 = 0
+    const float x00 = xs[0], x01 = xs[1], x10 = xs[2], x11 = xs[3];
+    if (!isfinite(x00 + x01 + x10 + x11)) {
+      const float nan = __int_as_float(0x7fffffff);
+      p[0] = p[1] = p[2] = p[3] = nan;
+      beta[0] = beta[1] = nan;
+      evals = 0;
+      return false;
+    }
+    const float u = 0.5f * ((x00 + x11) - (x01 + x10));
+    const float e = ex2(-fabsf(u) * LOG2E);  // exp(-|u|)
+    const float big = rcp(1.0f + e);        // sigma(|u|)
+    const float small = e * big;            // 1 - sigma(|u|), without cancellation
+    const float q = u >= 0.0f ? big : small;
+    const float qc = u >= 0.0f ? small : big;
+    p[0] = q;
+    p[1] = qc;
+    p[2] = qc;
+    p[3] = q;
+    beta[0] = 0.5f * ((x01 + x11) - (x00 + x10)) * LOG2E;
+    beta[1] = 0.0f;
+    evals = 1;
+    return true;
+  }
   float cs[N];
   float all = 0.0f;
 #pragma unroll
