@@ -293,8 +293,21 @@ struct NxnParams {
 
 // Persistent kernel over tiles of TILE tokens: coalesced copy into shared
 // memory, per-token compute, coalesced copy out.
+// Resident CTAs per SM the register allocation aims at (launch-bounds
+// minimum): for n >= 5 the per-token state would otherwise take 128-255
+// registers and leave 2-4 CTAs per SM.  Chosen by a sweep on GB300 (2^28
+// bytes of tokens per n): forward 128-thread CTAs 3 / 4 / 4 / 3 and backward
+// 64-thread CTAs 6 / 8 / 8 / 6 for n = 5 / 6 / 7 / 8 (n = 7: forward 1.63 ->
+// 1.00 ms, backward 2.35 -> 1.37 ms; a cap of 8 backward CTAs at n = 8
+// spills and is slower).
+template <int N, bool FWD>
+constexpr int nxn_minb() {
+  return N == 5 ? (FWD ? 3 : 6) : N == 6 ? (FWD ? 4 : 8) : N == 7 ? (FWD ? 4 : 8)
+       : N == 8 ? (FWD ? 3 : 6) : 1;
+}
+
 template <int N, int TILE, bool FWD>
-__global__ void __launch_bounds__(TILE) nxn_kernel(const NxnParams a) {
+__global__ void __launch_bounds__(TILE, (nxn_minb<N, FWD>())) nxn_kernel(const NxnParams a) {
   using S = NxnShape<N>;
   extern __shared__ float sm[];
   float* s0 = sm;                     // X or P tile, reused for the output
