@@ -178,7 +178,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   unsigned char* qk_sm = smem;
   unsigned char* v_sm = smem + NQK * QK_BYTES;
   __shared__ uint64_t qk_full[NQK], qk_empty[NQK], v_full[NV_MAX], v_empty[NV_MAX];
-  __shared__ uint64_t acc_full[NBUF_MAX], acc_empty[NBUF_MAX], p_full, o_full, o_empty, mma_done;
+  // p_full is per S / P buffer: one barrier shared by all tiles could see
+  // the epilogue complete tile T + 1's phase before the MMA thread had
+  // observed tile T's, and the parity wait would then miss it.  Per buffer,
+  // the next arrival needs S(T + nbuf), which the MMA thread issues only
+  // after it has consumed tile T's phase.
+  __shared__ uint64_t acc_full[NBUF_MAX], acc_empty[NBUF_MAX], p_full[NBUF_MAX];
+  __shared__ uint64_t o_full, o_empty, mma_done;
   __shared__ uint64_t bias_full[NBIAS], bias_empty[NBIAS];
   __shared__ __align__(16) float bias_sm[NBIAS][BN];
   __shared__ float mass_sh[GROUPS > 1 ? GROUPS - 1 : 1][BM];
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       b4::mbar_init(&bias_full[b], 1);
       b4::mbar_init(&bias_empty[b], NEPI);
     }
-    b4::mbar_init(&p_full, NEPI);
+    for (int b = 0; b < NBUF_MAX; ++b) b4::mbar_init(&p_full[b], NEPI);
     b4::mbar_init(&o_full, 1);
     b4::mbar_init(&o_empty, NEPI);
     b4::mbar_init(&mma_done, 1);
@@ -314,7 +320,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
             const uint32_t rbl = static_cast<uint32_t>(U / p.n_kt);
             if (!(ok = wait_bar(&o_empty, (rbl & 1u) ^ 1u, abort_flag, p.fault))) break;
           }
-          if (!(ok = wait_bar(&p_full, static_cast<uint32_t>(U) & 1u, abort_flag, p.fault))) break;
+          if (!(ok = wait_bar(&p_full[static_cast<uint32_t>(U) % nbuf],
+                              (static_cast<uint32_t>(U) / nbuf) & 1u, abort_flag, p.fault)))
+            break;
           tc_fence_after();
           for (int c = 0; c < BN / KC; ++c, ++iv) {
             const uint32_t s = iv % nv;
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&p_full);
+          mbar_arrive(&p_full[buf]);
           mbar_arrive(&bias_empty[slot]);
         }
       }
