@@ -171,7 +171,15 @@ __device__ __forceinline__ float p_chunk(uint32_t (&v)[32], const float4* kb, fl
 //          group (w - 2) / 4 (32 keys of each tile): p = 2^(S c1 + bias +
 //          rowterm) stored over its S columns in TMEM, the row mass, and at
 //          the end of a row block its chunks of O.
+template <int BN_>
 __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_constant__ Params p) {
+  // key-tile width: 128 (two or three S / P buffers) or 256 (one buffer)
+  constexpr int BN = BN_;
+  constexpr int B_BYTES = BN * KC * 4;
+  constexpr int QK_BYTES = A_BYTES + B_BYTES;
+  constexpr int NQK = BN == 256 ? 2 : 3;
+  constexpr int CPG = BN / KC / GROUPS;
+  static_assert(NQK * QK_BYTES + V_REGION + 1024 <= 227 * 1024 - 8192, "shared memory");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -288,59 +296,70 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       const uint32_t vbytes = static_cast<uint32_t>(p.dv) * KC * 4;
       const uint32_t nv = static_cast<uint32_t>(p.nv);
       uint32_t iq = 0, iv = 0;
+      // S(T) = Q K^T into buffer T % nbuf, once that buffer's P has been used
+      auto issue_s = [&](int T) -> bool {
+        const int buf = static_cast<int>(static_cast<uint32_t>(T) % nbuf);
+        const uint32_t use = static_cast<uint32_t>(T) / nbuf;
+        if (!wait_bar(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.fault)) return false;
+        tc_fence_after();
+        const uint32_t d_s = tmem + static_cast<uint32_t>(buf * BN);
+        for (int kc = 0; kc < p.n_kc; ++kc, ++iq) {
+          const int s = static_cast<int>(iq % NQK);
+          if (!wait_bar(&qk_full[s], (iq / NQK) & 1u, abort_flag, p.fault)) return false;
+          tc_fence_after();
+          const uint32_t a = b4::smem_addr(qk_sm + s * QK_BYTES);
+          const uint64_t da = desc_sw128_kmajor(a), db = desc_sw128_kmajor(a + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < KC / KSTEP; ++kk) {
+            const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
+            mma_tf32(d_s, da + adv, db + adv, id_s, (kc | kk) != 0);
+          }
+          mma_commit(&qk_empty[s]);
+        }
+        mma_commit(&acc_full[buf]);
+        return true;
+      };
+      // O += P(U) V(U)^T with P(U) read from its TMEM buffer
+      auto issue_pv = [&](int U) -> bool {
+        const int kt = U % p.n_kt;
+        const bool first = kt == 0, last = kt == p.n_kt - 1;
+        if (first) {
+          const uint32_t rbl = static_cast<uint32_t>(U / p.n_kt);
+          if (!wait_bar(&o_empty, (rbl & 1u) ^ 1u, abort_flag, p.fault)) return false;
+        }
+        const uint32_t buf = static_cast<uint32_t>(U) % nbuf;
+        if (!wait_bar(&p_full[buf], (static_cast<uint32_t>(U) / nbuf) & 1u, abort_flag, p.fault))
+          return false;
+        tc_fence_after();
+        for (int c = 0; c < BN / KC; ++c, ++iv) {
+          const uint32_t s = iv % nv;
+          if (!wait_bar(&v_full[s], (iv / nv) & 1u, abort_flag, p.fault)) return false;
+          tc_fence_after();
+          const uint32_t pa = tmem + buf * BN + c * KC;
+          const uint64_t dv = desc_sw128_kmajor(b4::smem_addr(v_sm + s * vbytes));
+#pragma unroll
+          for (int kk = 0; kk < KC / KSTEP; ++kk) {
+            const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
+            mma_tf32_ts(tmem + o_col, pa + static_cast<uint32_t>(kk * KSTEP), dv + adv, id_o,
+                        !(first && c == 0 && kk == 0));
+          }
+          mma_commit(&v_empty[s]);
+        }
+        mma_commit(&acc_empty[buf]);  // the S / P buffer is free once these MMAs are done
+        if (last) mma_commit(&o_full);
+        return true;
+      };
+      // with two or three buffers S(T) goes first, so it runs while the
+      // epilogue turns S(T - 1) into P; with one buffer S(T) needs P(T - 1)
+      // consumed first
       bool ok = true;
       for (int T = 0; T <= ntiles && ok; ++T) {
-        if (T < ntiles) {
-          const int buf = static_cast<int>(static_cast<uint32_t>(T) % nbuf);
-          const uint32_t use = static_cast<uint32_t>(T) / nbuf;
-          if (!(ok = wait_bar(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.fault))) break;
-          tc_fence_after();
-          const uint32_t d_s = tmem + static_cast<uint32_t>(buf * BN);
-          for (int kc = 0; kc < p.n_kc; ++kc, ++iq) {
-            const int s = static_cast<int>(iq % NQK);
-            if (!(ok = wait_bar(&qk_full[s], (iq / NQK) & 1u, abort_flag, p.fault))) break;
-            tc_fence_after();
-            const uint32_t a = b4::smem_addr(qk_sm + s * QK_BYTES);
-            const uint64_t da = desc_sw128_kmajor(a), db = desc_sw128_kmajor(a + A_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < KC / KSTEP; ++kk) {
-              const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
-              mma_tf32(d_s, da + adv, db + adv, id_s, (kc | kk) != 0);
-            }
-            mma_commit(&qk_empty[s]);
-          }
-          if (!ok) break;
-          mma_commit(&acc_full[buf]);
-        }
-        if (T > 0) {
-          const int U = T - 1;
-          const int kt = U % p.n_kt;
-          const bool first = kt == 0, last = kt == p.n_kt - 1;
-          if (first) {
-            const uint32_t rbl = static_cast<uint32_t>(U / p.n_kt);
-            if (!(ok = wait_bar(&o_empty, (rbl & 1u) ^ 1u, abort_flag, p.fault))) break;
-          }
-          if (!(ok = wait_bar(&p_full[static_cast<uint32_t>(U) % nbuf],
-                              (static_cast<uint32_t>(U) / nbuf) & 1u, abort_flag, p.fault)))
-            break;
-          tc_fence_after();
-          for (int c = 0; c < BN / KC; ++c, ++iv) {
-            const uint32_t s = iv % nv;
-            if (!(ok = wait_bar(&v_full[s], (iv / nv) & 1u, abort_flag, p.fault))) break;
-            tc_fence_after();
-            const uint32_t pa = tmem + (static_cast<uint32_t>(U) % nbuf) * BN + c * KC;
-            const uint64_t dv = desc_sw128_kmajor(b4::smem_addr(v_sm + s * vbytes));
-#pragma unroll
-            for (int kk = 0; kk < KC / KSTEP; ++kk) {
-              const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
-              mma_tf32_ts(tmem + o_col, pa + static_cast<uint32_t>(kk * KSTEP), dv + adv, id_o,
-                          !(first && c == 0 && kk == 0));
-            }
-            mma_commit(&v_empty[s]);
-          }
-          if (!ok) break;
-          mma_commit(&acc_empty[static_cast<uint32_t>(U) % nbuf]);  // the S / P buffer is free once these MMAs are done
-          if (last) mma_commit(&o_full);
+        if (nbuf == 1) {
+          if (T > 0) ok = issue_pv(T - 1);
+          if (ok && T < ntiles) ok = issue_s(T);
+        } else {
+          if (T < ntiles) ok = issue_s(T);
+          if (ok && T > 0) ok = issue_pv(T - 1);
         }
       }
       // all MMAs issued by this thread complete before TMEM is released
@@ -482,6 +501,15 @@ bool tr_sizes_ok(int64_t n, int64_t m, int32_t d, int32_t dv) {
          dv >= 1 && dv <= 16384;
 }
 
+// Key-tile width of the transport kernel: 256 (one S / P buffer; S as
+// 128 x 256 MMAs) measured about 15% faster than 128 (three buffers, 128 x
+// 128 MMAs) at d = 64 and 512 on GB300.
+#ifndef EOT_TR_BN
+#define EOT_TR_BN 256
+#endif
+constexpr int kTrBn = EOT_TR_BN;
+constexpr int kTrSmem = (kTrBn == 256 ? 2 : 3) * (tr::A_BYTES + kTrBn * KC * 4) + tr::V_REGION + 1024;
+
 cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const float* yt, int32_t v0,
                              int32_t dv, float* mass, cudaStream_t stream) {
   int dev = 0;
@@ -491,8 +519,8 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const fl
   if (nsm <= 0) return cudaErrorInvalidDevice;
   static std::atomic<int> attr_done[64];
   if (dev < 64 && attr_done[dev].load(std::memory_order_acquire) == 0) {
-    err = cudaFuncSetAttribute(tr::transport_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               tr::SMEM);
+    err = cudaFuncSetAttribute(tr::transport_kernel<kTrBn>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTrSmem);
     if (err != cudaSuccess) return err;
     attr_done[dev].store(1, std::memory_order_release);
   }
@@ -513,10 +541,10 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const fl
   p.v0 = v0;
   p.dv = dv;
   p.nv = std::min(tr::NV_MAX, tr::V_REGION / (dv * eot::KC * 4));
-  p.nbuf = (EOT_TR_NBUF3 != 0 && dv <= 128) ? 3 : 2;
+  p.nbuf = kTrBn == 256 ? 1 : ((EOT_TR_NBUF3 != 0 && dv <= 128) ? 3 : 2);
   p.mass = mass;
   const int grid = std::min(p.n_rb, nsm);
-  tr::transport_kernel<<<grid, tr::NTHREADS, tr::SMEM, stream>>>(p);
+  tr::transport_kernel<kTrBn><<<grid, tr::NTHREADS, kTrSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -563,7 +591,7 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   if (e != cudaSuccess) return b4::record_cuda_error(e);
   tr::Params p;
   if (!encode_rows128(&p.qmap, xp, L.n_pad, L.d_pad, BM) ||
-      !encode_rows128(&p.kmap, yp, L.m_pad, L.d_pad, tr::BN))
+      !encode_rows128(&p.kmap, yp, L.m_pad, L.d_pad, kTrBn))
     return b4::record_cuda_error(cudaErrorInvalidValue);
   p.kbias = kb;
   p.rowterm = rt;
@@ -572,7 +600,7 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   p.nq = n;
   p.d = dv;
   p.n_rb = static_cast<int32_t>(L.n_pad / BM);
-  p.n_kt = static_cast<int32_t>(L.m_pad / tr::BN);
+  p.n_kt = static_cast<int32_t>(L.m_pad / kTrBn);
   p.n_kc = L.d_pad / KC;
   p.c1 = static_cast<float>(2.0 * 1.4426950408889634 / eps);
   p.fault = fault;
