@@ -137,3 +137,34 @@ def apply_plan64(X, Y, f, g, log_a, log_b, eps, V):
     """The plan of (f, g) applied to values V [m, dv]: (pi V, pi 1)."""
     P = plan64(X, Y, f, g, log_a, log_b, eps)
     return P @ np.asarray(V, dtype=np.float64), P.sum(1)
+
+
+def hvp64(X, Y, f, g, log_a, log_b, eps, V):
+    """Hessian-vector product of the entropic OT cost with respect to X at
+    converged potentials ("FlashSinkhorn", Methodik s3: the HVP as transport
+    products), written out densely.
+
+    With pi the plan, the row marginals fixed (sum_j dpi_ij = 0) and
+    dC_ij = 2 (x_i - y_j).v_i:
+        (H v)_i = 2 a_i v_i - 2 sum_j dpi_ij y_j,
+        dpi_ij = pi_ij (df_i + dg_j - dC_ij) / eps,
+    where (df, dg) solve the linearised marginal conditions
+        a_i df_i + (pi dg)_i = sum_j pi_ij dC_ij,
+        (pi^T df)_j + b_j dg_j = sum_i pi_ij dC_ij
+    (a singular symmetric system with null vector (1, -1), solved here by
+    least squares).  Returns H v [n, d]."""
+    X = _as64(X, "X", 2)
+    Y = _as64(Y, "Y", 2)
+    V = _as64(V, "V", 2)
+    n = X.shape[0]
+    a = np.exp(_as64(log_a, "log_a", 1))
+    b = np.exp(_as64(log_b, "log_b", 1))
+    P = plan64(X, Y, f, g, log_a, log_b, eps)
+    dC = 2.0 * ((X * V).sum(1)[:, None] - V @ Y.T)
+    r = (P * dC).sum(1)
+    c = (P * dC).sum(0)
+    A = np.block([[np.diag(a), P], [P.T, np.diag(b)]])
+    sol = np.linalg.lstsq(A, np.r_[r, c], rcond=None)[0]
+    df, dg = sol[:n], sol[n:]
+    dP = P * (df[:, None] + dg[None, :] - dC) / eps
+    return 2.0 * a[:, None] * V - 2.0 * dP @ Y

@@ -247,3 +247,54 @@ def test_apply_plan_is_linear_and_matches_transport():
     assert np.array_equal(PV, PY) and np.array_equal(r, r2)
     ones, _ = eot.apply_plan64(X, Y, f, g, la, lb, 0.4, np.ones((11, 1)))
     assert np.abs(ones[:, 0] - r).max() <= 1e-15
+
+
+def test_hvp_matches_finite_differences_of_the_gradient():
+    """hvp64 (dense implicit differentiation) against central differences of
+    the gradient at re-converged potentials, which use no Hessian formula."""
+    X, Y = clouds(6, 7, 2, seed=31)
+    la, lb = uniform(6), uniform(7)
+    eps, iters, h = 0.5, 4000, 1e-5
+    V = R(32).standard_normal(X.shape)
+    f, g = eot.sinkhorn64(X, Y, la, lb, eps, iters)
+    Hv = eot.hvp64(X, Y, f, g, la, lb, eps, V)
+
+    def grad(Xs):
+        fs, gs = eot.sinkhorn64(Xs, Y, la, lb, eps, iters)
+        return eot.grad_x64(Xs, Y, fs, gs, la, lb, eps)
+
+    fd = (grad(X + h * V) - grad(X - h * V)) / (2 * h)
+    assert np.abs(Hv - fd).max() <= 1e-6 * max(1.0, np.abs(fd).max())
+
+
+def test_hvp_along_a_common_translation_sums_to_2t():
+    """Moving every x_i by t changes sum_i grad_i = 2 (sum_i a_i x_i - sum_j b_j y_j)
+    by 2 t (total mass 1), so sum_i (H v)_i = 2 t for v_i = t."""
+    X, Y = clouds(9, 12, 3, seed=33)
+    r = R(34)
+    la = np.log(r.uniform(0.3, 1.0, 9))
+    la -= np.log(np.exp(la).sum())
+    lb = uniform(12)
+    f, g = eot.sinkhorn64(X, Y, la, lb, 0.3, 5000)
+    t = np.array([0.7, -1.1, 0.25])
+    Hv = eot.hvp64(X, Y, f, g, la, lb, 0.3, np.tile(t, (9, 1)))
+    assert np.abs(Hv.sum(0) - 2 * t).max() <= 1e-9
+
+
+def test_planted_hvp_mistake_fails():
+    """Dropping the implicit (df, dg) term breaks the finite-difference pin."""
+    X, Y = clouds(5, 6, 2, seed=35)
+    la, lb = uniform(5), uniform(6)
+    eps, iters, h = 0.5, 4000, 1e-5
+    V = R(36).standard_normal(X.shape)
+    f, g = eot.sinkhorn64(X, Y, la, lb, eps, iters)
+    P = eot.plan64(X, Y, f, g, la, lb, eps)
+    dC = 2.0 * ((X * V).sum(1)[:, None] - V @ Y.T)
+    bad = 2.0 * np.exp(la)[:, None] * V - 2.0 * (P * -dC / eps) @ Y
+
+    def grad(Xs):
+        fs, gs = eot.sinkhorn64(Xs, Y, la, lb, eps, iters)
+        return eot.grad_x64(Xs, Y, fs, gs, la, lb, eps)
+
+    fd = (grad(X + h * V) - grad(X - h * V)) / (2 * h)
+    assert np.abs(bad - fd).max() > 1e-2
