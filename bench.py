@@ -545,6 +545,16 @@ def run_eot(dev):
         del ws
         del X, Y
         torch.cuda.empty_cache()
+    # Hessian-vector product (20 CG steps) at n = m = 16384, d = 64
+    nh = 16384
+    X, Y, la, lb = workloads.eot_clouds(nh, nh, 64, seed=0, device=dev)
+    f, g = eot.sinkhorn(X, Y, la, lb, eps, 20)
+    V = torch.randn(nh, 64, device=dev)
+    ws = torch.empty(eot.lib().eot_hvp_workspace_bytes(nh, nh, 64), dtype=torch.uint8, device=dev)
+    th = time_device(lambda i: eot.hvp(X, Y, f, g, la, lb, V, eps, cg_iters=20, workspace=ws), 3, dev)
+    print(json.dumps({"eot_hvp": True, "n": nh, "m": nh, "d": 64, "eps": eps, "cg_iters": 20,
+                      "ms": th, "plan_passes": 2 * 20 + 4,
+                      "ms_per_plan_pass": th / (2 * 20 + 4)}), flush=True)
 
 
 def ctypes_probe(b4, dev):

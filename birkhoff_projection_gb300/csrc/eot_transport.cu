@@ -58,7 +58,6 @@ static_assert(DV % KC == 0 && DV <= 256 && V_REGION >= 3 * DV * KC * 4, "value s
 constexpr int TMEM_COLS = 512;             // S / P buffers of 128 columns, then O
 constexpr int NBUF_MAX = 3;                // 3 S / P buffers when O needs <= 128 columns
 constexpr int GROUPS = NEPI / 4;           // key groups per tile (one per epilogue warp of a quarter)
-constexpr int CPG = BN / KC / GROUPS;      // 32-key chunks per group
 static_assert(NEPI % 4 == 0 && (BN / KC) % GROUPS == 0, "whole chunks per epilogue warp");
 static_assert(SMEM <= 227 * 1024 - 4096, "shared memory");
 
@@ -66,6 +65,7 @@ struct Params {
   CUtensorMap qmap;      // query points [nq_pad, d_pad], box {32, 128}
   CUtensorMap kmap;      // key points [nk_pad, d_pad], box {32, 128}
   CUtensorMap vmap;      // key points transposed [d_pad, nk_pad], box {32 keys, dv}
+  CUtensorMap wmap;      // moment form: the query directions [nq_pad, d_pad], box {32, 128}
   const float* kbias;    // [nk_pad] (g_j - ||y_j||^2) log2(e)/eps + log2 b_j; -inf past nk
   const float* rowterm;  // [nq_pad] (f_i - ||x_i||^2) log2(e)/eps + log2 a_i; -inf past nq
   float* out;            // [nq, d]: columns v0 .. v0 + dv - 1 (those below d) written
@@ -128,6 +128,137 @@ __global__ void grad_kernel(const float* __restrict__ X, const float* __restrict
     grad[e] = 2.0f * fmaf(mass[e / d], X[e], -PY[e]);
 }
 
+// ---------------------------------------------------------------------------
+// Hessian-vector product helpers (one thread per row / element)
+// ---------------------------------------------------------------------------
+// xv_i = x_i . v_i;  r_i = 2 (a_i xv_i - (pi Y)_i . v_i);  W_i = [xv_i, v_i]
+__global__ void hvp_prep_kernel(const float* __restrict__ X, const float* __restrict__ V,
+                                const float* __restrict__ PY, const float* __restrict__ log_a,
+                                int64_t n, int32_t d, float* __restrict__ xv, float* __restrict__ r,
+                                float* __restrict__ W) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float sx = 0.0f, sp = 0.0f;
+  for (int k = 0; k < d; ++k) {
+    const float v = V[i * d + k];
+    sx = fmaf(X[i * d + k], v, sx);
+    sp = fmaf(PY[i * d + k], v, sp);
+    W[i * (d + 1) + 1 + k] = v;
+  }
+  xv[i] = sx;
+  W[i * (d + 1)] = sx;
+  r[i] = 2.0f * fmaf(__expf(log_a[i]), sx, -sp);
+}
+
+// c_j = 2 ((pi^T xv)_j - y_j . (pi^T V)_j) from Mr = pi^T [xv, V]
+__global__ void hvp_col_kernel(const float* __restrict__ Y, const float* __restrict__ Mr,
+                               int64_t m, int32_t d, float* __restrict__ c) {
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (j >= m) return;
+  float s = 0.0f;
+  for (int k = 0; k < d; ++k) s = fmaf(Y[j * d + k], Mr[j * (d + 1) + 1 + k], s);
+  c[j] = 2.0f * (Mr[j * (d + 1)] - s);
+}
+
+// U_j = [dg_j, dg_j y_j]
+__global__ void hvp_values_kernel(const float* __restrict__ Y, const float* __restrict__ dg, int64_t m,
+                                  int32_t d, float* __restrict__ U) {
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (j >= m) return;
+  U[j * (d + 1)] = dg[j];
+  for (int k = 0; k < d; ++k) U[j * (d + 1) + 1 + k] = dg[j] * Y[j * d + k];
+}
+
+// (H v)_ik = 2 a_i v_ik - (2/eps) (df_i PY_ik + G2_i,1+k - 2 xv_i PY_ik + 2 MV_ik)
+__global__ void hvp_final_kernel(const float* __restrict__ V, const float* __restrict__ PY,
+                                 const float* __restrict__ xv, const float* __restrict__ df,
+                                 const float* __restrict__ G2, const float* __restrict__ MV,
+                                 const float* __restrict__ log_a, int64_t n, int32_t d,
+                                 float two_over_eps, float* __restrict__ out) {
+  const int64_t total = n * d;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = e / d;
+    const int64_t k = e - i * d;
+    const float t = fmaf(df[i] - 2.0f * xv[i], PY[e], G2[i * (d + 1) + 1 + k] + 2.0f * MV[e]);
+    out[e] = fmaf(2.0f * __expf(log_a[i]), V[e], -two_over_eps * t);
+  }
+}
+
+// Conjugate gradients on [[diag(a), pi], [pi^T, diag(b)]] z = rhs, with the
+// diagonal as preconditioner; vectors are [n | m] concatenated.  Dot products
+// reduce in two fixed passes (deterministic), scalars stay on the device.
+constexpr int kDotBlocks = 256;
+__global__ void dot_partial_kernel(const float* __restrict__ x, const float* __restrict__ y,
+                                   int64_t N, double* __restrict__ part) {
+  __shared__ double sh[256];
+  double acc = 0.0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < N;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    acc += static_cast<double>(x[i]) * static_cast<double>(y[i]);
+  sh[threadIdx.x] = acc;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) part[blockIdx.x] = sh[0];
+}
+__global__ void dot_final_kernel(const double* __restrict__ part, double* __restrict__ out) {
+  __shared__ double sh[kDotBlocks];
+  sh[threadIdx.x] = part[threadIdx.x];
+  __syncthreads();
+  for (int o = kDotBlocks / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *out = sh[0];
+}
+// Ap = diag * p + [pi p2 ; pi^T p1] (the two products already in Pp)
+__global__ void cg_matvec_kernel(const float* __restrict__ diag, const float* __restrict__ p,
+                                 const float* __restrict__ Pp, int64_t N, float* __restrict__ Ap) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < N) Ap[i] = fmaf(diag[i], p[i], Pp[i]);
+}
+// z += alpha p, res -= alpha Ap, s = res / diag; alpha = rs / pAp (0 once
+// the residual has vanished)
+__global__ void cg_step_kernel(const double* __restrict__ rs, const double* __restrict__ pAp,
+                               const float* __restrict__ p, const float* __restrict__ Ap,
+                               const float* __restrict__ diag, int64_t N, float* __restrict__ z,
+                               float* __restrict__ res, float* __restrict__ sv) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const double den = *pAp;
+  const float alpha = den > 1e-300 ? static_cast<float>(*rs / den) : 0.0f;
+  z[i] = fmaf(alpha, p[i], z[i]);
+  res[i] = fmaf(-alpha, Ap[i], res[i]);
+  sv[i] = res[i] / diag[i];
+}
+// p = s + beta p, beta = rs_new / rs
+__global__ void cg_dir_kernel(const double* __restrict__ rs, const double* __restrict__ rs_new,
+                              const float* __restrict__ sv, int64_t N, float* __restrict__ p) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const double r0 = *rs;
+  const float beta = r0 > 1e-300 ? static_cast<float>(*rs_new / r0) : 0.0f;
+  p[i] = fmaf(beta, p[i], sv[i]);
+}
+// z = 0, res = rhs, s = res / diag, p = s; diag = [a ; b]
+__global__ void cg_init_kernel(const float* __restrict__ rhs, const float* __restrict__ log_a,
+                               const float* __restrict__ log_b, int64_t n, int64_t N,
+                               float* __restrict__ diag, float* __restrict__ z,
+                               float* __restrict__ res, float* __restrict__ sv,
+                               float* __restrict__ p) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const float dg = __expf(i < n ? log_a[i] : log_b[i - n]);
+  diag[i] = dg;
+  z[i] = 0.0f;
+  res[i] = rhs[i];
+  sv[i] = rhs[i] / dg;
+  p[i] = sv[i];
+}
+
 // p = 2^(acc c1 + bias_j + rt) for one 32-key chunk of a row, in place over
 // the accumulator bits; returns the chunk's sum.
 __device__ __forceinline__ float p_chunk(uint32_t (&v)[32], const float4* kb, float c1, float rt) {
@@ -171,13 +302,20 @@ __device__ __forceinline__ float p_chunk(uint32_t (&v)[32], const float4* kb, fl
 //          group (w - 2) / 4 (32 keys of each tile): p = 2^(S c1 + bias +
 //          rowterm) stored over its S columns in TMEM, the row mass, and at
 //          the end of a row block its chunks of O.
-template <int BN_>
+// MOMENT: the second-moment form used by the Hessian-vector product: with a
+// direction w_i per query, the weights become pi_ij (w_i . y_j), so O_i =
+// sum_j pi_ij (w_i . y_j) y_j.  A second MMA per K chunk (the packed
+// directions as A, the same key tile as B) writes S' = W Y^T beside S
+// (128-key tiles, one S / S' buffer pair), and the epilogue multiplies.
+template <int BN_, bool MOMENT>
 __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_constant__ Params p) {
   // key-tile width: 128 (two or three S / P buffers) or 256 (one buffer)
   constexpr int BN = BN_;
+  static_assert(!MOMENT || BN == 128, "the moment form keeps S, S' and O in TMEM");
   constexpr int B_BYTES = BN * KC * 4;
-  constexpr int QK_BYTES = A_BYTES + B_BYTES;
-  constexpr int NQK = BN == 256 ? 2 : 3;
+  constexpr int NA = MOMENT ? 2 : 1;  // query operands per K chunk
+  constexpr int QK_BYTES = NA * A_BYTES + B_BYTES;
+  constexpr int NQK = (BN == 256 || MOMENT) ? 2 : 3;
   constexpr int CPG = BN / KC / GROUPS;
   static_assert(NQK * QK_BYTES + V_REGION + 1024 <= 227 * 1024 - 8192, "shared memory");
   extern __shared__ unsigned char smem_raw[];
@@ -232,6 +370,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     b4::prefetch_tmap(&p.qmap);
     b4::prefetch_tmap(&p.kmap);
     b4::prefetch_tmap(&p.vmap);
+    if (MOMENT) b4::prefetch_tmap(&p.wmap);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, TMEM_COLS);
@@ -242,7 +381,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t nbuf = static_cast<uint32_t>(p.nbuf);
-  const uint32_t o_col = nbuf * BN;
+  const uint32_t o_col = MOMENT ? 2 * BN : nbuf * BN;  // O after the S (and S') columns
 
   if (warp == 0) {
     // ---------------- producers ----------------
@@ -265,7 +404,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
           unsigned char* st = qk_sm + s * QK_BYTES;
           b4::mbar_arrive_expect_tx(&qk_full[s], QK_BYTES);
           b4::tma_load_2d(st, &p.qmap, &qk_full[s], kc * KC, rb * BM);
-          b4::tma_load_2d(st + A_BYTES, &p.kmap, &qk_full[s], kc * KC, kt * BN);
+          if (MOMENT) b4::tma_load_2d(st + A_BYTES, &p.wmap, &qk_full[s], kc * KC, rb * BM);
+          b4::tma_load_2d(st + NA * A_BYTES, &p.kmap, &qk_full[s], kc * KC, kt * BN);
         }
       }
       // every issued copy lands before the CTA may exit
@@ -308,11 +448,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
           if (!wait_bar(&qk_full[s], (iq / NQK) & 1u, abort_flag, p.fault)) return false;
           tc_fence_after();
           const uint32_t a = b4::smem_addr(qk_sm + s * QK_BYTES);
-          const uint64_t da = desc_sw128_kmajor(a), db = desc_sw128_kmajor(a + A_BYTES);
+          const uint64_t da = desc_sw128_kmajor(a), db = desc_sw128_kmajor(a + NA * A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < KC / KSTEP; ++kk) {
             const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
             mma_tf32(d_s, da + adv, db + adv, id_s, (kc | kk) != 0);
+            if (MOMENT)  // S' = W Y^T into the columns after S
+              mma_tf32(d_s + BN, desc_sw128_kmajor(a + A_BYTES) + adv, db + adv, id_s,
+                       (kc | kk) != 0);
           }
           mma_commit(&qk_empty[s]);
         }
@@ -399,6 +542,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         for (int ch = 0; ch < CPG; ++ch) {
           if (ch + 1 < CPG) tmem_ld32(taddr + static_cast<uint32_t>((ch + 1) * KC), w);
           mass += p_chunk(v, kb + ch * 8, p.c1, rt);
+          if (MOMENT) {  // weight pi_ij (w_i . y_j): S' sits BN columns after S
+            uint32_t sp[32];
+            tmem_ld32(taddr + static_cast<uint32_t>(BN + ch * KC), sp);
+            tmem_wait32(sp);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              v[i] = __float_as_uint(__uint_as_float(v[i]) * __uint_as_float(sp[i]));
+          }
           tmem_st32(taddr + static_cast<uint32_t>(ch * KC), v);
           if (ch + 1 < CPG) {
             tmem_wait32(w);
@@ -468,10 +619,11 @@ namespace {
 struct TrLayout {
   int64_t n_pad, m_pad;
   int32_t d_pad, v_pad;
-  size_t x, y, yt, xn, yn, kb, rt, total;  // byte offsets (yt: the values, transposed)
+  size_t x, y, yt, xn, yn, kb, rt, wq, wn, total;  // byte offsets (yt: the values, transposed)
 };
 
-TrLayout tr_layout(int64_t n, int64_t m, int32_t d, int32_t dv) {
+// moment: also room for the packed query directions (wq) and their norms
+TrLayout tr_layout(int64_t n, int64_t m, int32_t d, int32_t dv, bool moment = false) {
   TrLayout L;
   L.n_pad = round_up(std::max<int64_t>(n, 1), ROW_PAD);
   L.m_pad = round_up(std::max<int64_t>(m, 1), ROW_PAD);
@@ -492,6 +644,13 @@ TrLayout tr_layout(int64_t n, int64_t m, int32_t d, int32_t dv) {
   o += align_bytes(static_cast<size_t>(L.m_pad) * 4);
   L.rt = o;
   o += align_bytes(static_cast<size_t>(L.n_pad) * 4);
+  L.wq = L.wn = 0;
+  if (moment) {
+    L.wq = o;
+    o += align_bytes(static_cast<size_t>(L.n_pad) * L.d_pad * 4);
+    L.wn = o;
+    o += align_bytes(static_cast<size_t>(L.n_pad) * 4);
+  }
   L.total = o;
   return L;
 }
@@ -509,20 +668,27 @@ bool tr_sizes_ok(int64_t n, int64_t m, int32_t d, int32_t dv) {
 #endif
 constexpr int kTrBn = EOT_TR_BN;
 constexpr int kTrSmem = (kTrBn == 256 ? 2 : 3) * (tr::A_BYTES + kTrBn * KC * 4) + tr::V_REGION + 1024;
+constexpr int kMomSmem = 2 * (2 * tr::A_BYTES + 128 * KC * 4) + tr::V_REGION + 1024;
+
+// Key-tile width of a launch: the moment form needs 128 (S, S' and O in TMEM).
+int tile_keys(bool moment) { return moment ? 128 : kTrBn; }
 
 cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const float* yt, int32_t v0,
-                             int32_t dv, float* mass, cudaStream_t stream) {
+                             int32_t dv, float* mass, bool moment, cudaStream_t stream) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   const int nsm = b4::sm_count(dev);
   if (nsm <= 0) return cudaErrorInvalidDevice;
-  static std::atomic<int> attr_done[64];
-  if (dev < 64 && attr_done[dev].load(std::memory_order_acquire) == 0) {
-    err = cudaFuncSetAttribute(tr::transport_kernel<kTrBn>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTrSmem);
+  static std::atomic<int> attr_done[64], attr_mom[64];
+  std::atomic<int>* done = moment ? attr_mom : attr_done;
+  if (dev < 64 && done[dev].load(std::memory_order_acquire) == 0) {
+    err = moment ? cudaFuncSetAttribute(tr::transport_kernel<128, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kMomSmem)
+                 : cudaFuncSetAttribute(tr::transport_kernel<kTrBn, false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kTrSmem);
     if (err != cudaSuccess) return err;
-    attr_done[dev].store(1, std::memory_order_release);
+    done[dev].store(1, std::memory_order_release);
   }
   tr::Params p = base;
   // value operand: rows v0 .. v0 + dv - 1 of the transposed key points
@@ -541,31 +707,37 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const fl
   p.v0 = v0;
   p.dv = dv;
   p.nv = std::min(tr::NV_MAX, tr::V_REGION / (dv * eot::KC * 4));
-  p.nbuf = kTrBn == 256 ? 1 : ((EOT_TR_NBUF3 != 0 && dv <= 128) ? 3 : 2);
+  p.nbuf = (moment || kTrBn == 256) ? 1 : ((EOT_TR_NBUF3 != 0 && dv <= 128) ? 3 : 2);
   p.mass = mass;
   const int grid = std::min(p.n_rb, nsm);
-  tr::transport_kernel<kTrBn><<<grid, tr::NTHREADS, kTrSmem, stream>>>(p);
+  if (moment)
+    tr::transport_kernel<128, true><<<grid, tr::NTHREADS, kMomSmem, stream>>>(p);
+  else
+    tr::transport_kernel<kTrBn, false><<<grid, tr::NTHREADS, kTrSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
 // The plan of (f, g) applied to the values V [m, dv]: out = pi V, mass =
-// pi 1.
+// pi 1.  With directions Wd [n, d] (moment form) the weights are
+// pi_ij (w_i . y_j) instead: out_i = sum_j pi_ij (w_i . y_j) v_j.
 int apply_impl(const float* X, const float* Y, const float* f, const float* g, const float* log_a,
                const float* log_b, const float* V, int32_t dv, float* out, float* mass, int64_t n,
                int64_t m, int32_t d, float eps, void* workspace, size_t workspace_bytes,
-               cudaStream_t s) {
+               cudaStream_t s, const float* Wd = nullptr) {
+  const bool moment = Wd != nullptr;
   if (!tr_sizes_ok(n, m, d, dv) || !(eps > 0.0f) || !std::isfinite(eps)) return B4_EINVAL;
   if (n == 0) return B4_OK;
   if (m == 0) return B4_EINVAL;
   if (X == nullptr || Y == nullptr || f == nullptr || g == nullptr || log_a == nullptr ||
       log_b == nullptr || V == nullptr || out == nullptr || mass == nullptr)
     return B4_EINVAL;
-  const TrLayout L = tr_layout(n, m, d, dv);
+  const TrLayout L = tr_layout(n, m, d, dv, moment);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < L.total)
     return B4_EINVAL;
   cudaError_t e = cudaSuccess;
   unsigned int* fault = b4::device_fault_latch(&e);
+  const int bn = tile_keys(moment);
   if (e != cudaSuccess) return b4::record_cuda_error(e);
   unsigned char* w = static_cast<unsigned char*>(workspace);
   float* xp = reinterpret_cast<float*>(w + L.x);
@@ -577,6 +749,9 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   float* rt = reinterpret_cast<float*>(w + L.rt);
   e = pack(X, n, d, L.n_pad, L.d_pad, xp, nullptr, xn, s);
   if (e == cudaSuccess) e = pack(Y, m, d, L.m_pad, L.d_pad, yp, nullptr, yn, s);
+  float* wq = moment ? reinterpret_cast<float*>(w + L.wq) : nullptr;
+  if (e == cudaSuccess && moment)
+    e = pack(Wd, n, d, L.n_pad, L.d_pad, wq, nullptr, reinterpret_cast<float*>(w + L.wn), s);
   if (e == cudaSuccess) {
     const dim3 grid(static_cast<unsigned>(L.m_pad / 32), static_cast<unsigned>(L.v_pad / 32));
     tr::pack_transposed_kernel<<<grid, dim3(32, 8), 0, s>>>(V, m, dv, L.m_pad, L.v_pad, vt);
@@ -591,8 +766,10 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   if (e != cudaSuccess) return b4::record_cuda_error(e);
   tr::Params p;
   if (!encode_rows128(&p.qmap, xp, L.n_pad, L.d_pad, BM) ||
-      !encode_rows128(&p.kmap, yp, L.m_pad, L.d_pad, kTrBn))
+      !encode_rows128(&p.kmap, yp, L.m_pad, L.d_pad, bn) ||
+      (moment && !encode_rows128(&p.wmap, wq, L.n_pad, L.d_pad, BM)))
     return b4::record_cuda_error(cudaErrorInvalidValue);
+  if (!moment) p.wmap = p.qmap;
   p.kbias = kb;
   p.rowterm = rt;
   p.out = out;
@@ -600,7 +777,7 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   p.nq = n;
   p.d = dv;
   p.n_rb = static_cast<int32_t>(L.n_pad / BM);
-  p.n_kt = static_cast<int32_t>(L.m_pad / kTrBn);
+  p.n_kt = static_cast<int32_t>(L.m_pad / bn);
   p.n_kc = L.d_pad / KC;
   p.c1 = static_cast<float>(2.0 * 1.4426950408889634 / eps);
   p.fault = fault;
@@ -608,9 +785,125 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   // writes the row masses
   for (int32_t v0 = 0; v0 < L.v_pad && e == cudaSuccess; v0 += tr::DV) {
     const int32_t w_slice = std::min<int32_t>(tr::DV, L.v_pad - v0);
-    e = launch_transport(p, L, vt, v0, w_slice, v0 == 0 ? mass : nullptr, s);
+    e = launch_transport(p, L, vt, v0, w_slice, v0 == 0 ? mass : nullptr, moment, s);
   }
   return b4::record_cuda_error(e);
+}
+
+// Workspace of the Hessian-vector product: one region for the plan
+// applications (run one after another), then the vectors.
+struct HvpLayout {
+  size_t apply, py, xv, rhs, w, mr, z, res, sv, pv, ap, pp, diag, mass, u, g2, mv, part, scal, total;
+};
+
+HvpLayout hvp_layout(int64_t n, int64_t m, int32_t d) {
+  HvpLayout H;
+  const size_t ap = std::max({tr_layout(n, m, d, d + 1).total, tr_layout(m, n, d, d + 1).total,
+                              tr_layout(n, m, d, d, true).total});
+  const size_t N = static_cast<size_t>(n + m);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_bytes(bytes);
+    return at;
+  };
+  H.apply = take(ap);
+  H.py = take(static_cast<size_t>(n) * d * 4);
+  H.xv = take(static_cast<size_t>(n) * 4);
+  H.rhs = take(N * 4);
+  H.w = take(static_cast<size_t>(n) * (d + 1) * 4);
+  H.mr = take(static_cast<size_t>(m) * (d + 1) * 4);
+  H.z = take(N * 4);
+  H.res = take(N * 4);
+  H.sv = take(N * 4);
+  H.pv = take(N * 4);
+  H.ap = take(N * 4);
+  H.pp = take(N * 4);
+  H.diag = take(N * 4);
+  H.mass = take(static_cast<size_t>(std::max(n, m)) * 4);
+  H.u = take(static_cast<size_t>(m) * (d + 1) * 4);
+  H.g2 = take(static_cast<size_t>(n) * (d + 1) * 4);
+  H.mv = take(static_cast<size_t>(n) * d * 4);
+  H.part = take(tr::kDotBlocks * sizeof(double));
+  H.scal = take(4 * sizeof(double));
+  H.total = o;
+  return H;
+}
+
+// (H v) for the entropic OT cost at potentials (f, g): see eot_hvp.
+int hvp_impl(const float* X, const float* Y, const float* f, const float* g, const float* log_a,
+             const float* log_b, const float* V, float* out, int64_t n, int64_t m, int32_t d,
+             float eps, int32_t cg_iters, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+  if (!tr_sizes_ok(n, m, d, d + 1) || !(eps > 0.0f) || !std::isfinite(eps) || cg_iters < 0 ||
+      cg_iters > 100000)
+    return B4_EINVAL;
+  if (n == 0) return B4_OK;
+  if (m == 0) return B4_EINVAL;
+  if (X == nullptr || Y == nullptr || f == nullptr || g == nullptr || log_a == nullptr ||
+      log_b == nullptr || V == nullptr || out == nullptr)
+    return B4_EINVAL;
+  const HvpLayout H = hvp_layout(n, m, d);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < H.total)
+    return B4_EINVAL;
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(w + off); };
+  void* aw = w + H.apply;
+  const size_t ab = H.py - H.apply;
+  const int64_t N = n + m;
+  float *PY = F(H.py), *xv = F(H.xv), *rhs = F(H.rhs), *W = F(H.w), *Mr = F(H.mr), *z = F(H.z);
+  float *res = F(H.res), *sv = F(H.sv), *pv = F(H.pv), *Ap = F(H.ap), *Pp = F(H.pp);
+  float *diag = F(H.diag), *mass = F(H.mass), *U = F(H.u), *G2 = F(H.g2), *MV = F(H.mv);
+  double* part = reinterpret_cast<double*>(w + H.part);
+  double* scal = reinterpret_cast<double*>(w + H.scal);  // rs[2], pAp
+  const unsigned bn = static_cast<unsigned>((N + 255) / 256);
+  const unsigned bq = static_cast<unsigned>((n + 255) / 256);
+  const unsigned bk = static_cast<unsigned>((m + 255) / 256);
+  auto dot = [&](const float* x, const float* y, double* outp) {
+    tr::dot_partial_kernel<<<tr::kDotBlocks, 256, 0, s>>>(x, y, N, part);
+    tr::dot_final_kernel<<<1, tr::kDotBlocks, 0, s>>>(part, outp);
+    return cudaGetLastError();
+  };
+  int st;
+  // pi Y, then r and the values [x.v, V]
+  if ((st = apply_impl(X, Y, f, g, log_a, log_b, Y, d, PY, mass, n, m, d, eps, aw, ab, s)) != B4_OK)
+    return st;
+  tr::hvp_prep_kernel<<<bq, 256, 0, s>>>(X, V, PY, log_a, n, d, xv, rhs, W);
+  // pi^T [x.v, V], then c
+  if ((st = apply_impl(Y, X, g, f, log_b, log_a, W, d + 1, Mr, mass, m, n, d, eps, aw, ab, s)) != B4_OK)
+    return st;
+  tr::hvp_col_kernel<<<bk, 256, 0, s>>>(Y, Mr, m, d, rhs + n);
+  // conjugate gradients for (df, dg)
+  tr::cg_init_kernel<<<bn, 256, 0, s>>>(rhs, log_a, log_b, n, N, diag, z, res, sv, pv);
+  cudaError_t e = dot(res, sv, scal + 0);
+  if (e != cudaSuccess) return b4::record_cuda_error(e);
+  for (int32_t k = 0; k < cg_iters; ++k) {
+    double* rs = scal + (k & 1);
+    double* rs_next = scal + ((k + 1) & 1);
+    if ((st = apply_impl(X, Y, f, g, log_a, log_b, pv + n, 1, Pp, mass, n, m, d, eps, aw, ab, s)) !=
+        B4_OK)
+      return st;
+    if ((st = apply_impl(Y, X, g, f, log_b, log_a, pv, 1, Pp + n, mass, m, n, d, eps, aw, ab, s)) !=
+        B4_OK)
+      return st;
+    tr::cg_matvec_kernel<<<bn, 256, 0, s>>>(diag, pv, Pp, N, Ap);
+    if ((e = dot(pv, Ap, scal + 2)) != cudaSuccess) return b4::record_cuda_error(e);
+    tr::cg_step_kernel<<<bn, 256, 0, s>>>(rs, scal + 2, pv, Ap, diag, N, z, res, sv);
+    if ((e = dot(res, sv, rs_next)) != cudaSuccess) return b4::record_cuda_error(e);
+    tr::cg_dir_kernel<<<bn, 256, 0, s>>>(rs, rs_next, sv, N, pv);
+  }
+  // pi [dg, dg y], the second moment, and the combination
+  tr::hvp_values_kernel<<<bk, 256, 0, s>>>(Y, z + n, m, d, U);
+  if ((st = apply_impl(X, Y, f, g, log_a, log_b, U, d + 1, G2, mass, n, m, d, eps, aw, ab, s)) != B4_OK)
+    return st;
+  if ((st = apply_impl(X, Y, f, g, log_a, log_b, Y, d, MV, mass, n, m, d, eps, aw, ab, s, V)) !=
+      B4_OK)
+    return st;
+  const int64_t tot = n * static_cast<int64_t>(d);
+  const int64_t blocks = std::min<int64_t>((tot + 255) / 256, 1 << 20);
+  tr::hvp_final_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      V, PY, xv, z, G2, MV, log_a, n, d, 2.0f / eps, out);
+  return b4::record_cuda_error(cudaGetLastError());
 }
 
 }  // namespace
@@ -646,4 +939,17 @@ extern "C" int eot_transport(const float* X, const float* Y, const float* f, con
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, 1 << 20);
   eot::tr::grad_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(X, PY, mass, n, d, grad);
   return b4::record_cuda_error(cudaGetLastError());
+}
+
+extern "C" size_t eot_hvp_workspace_bytes(int64_t n, int64_t m, int32_t d) {
+  if (!eot::tr_sizes_ok(n, m, d, d + 1)) return 0;
+  return eot::hvp_layout(n, m, d).total;
+}
+
+extern "C" int eot_hvp(const float* X, const float* Y, const float* f, const float* g,
+                       const float* log_a, const float* log_b, const float* V, float* out,
+                       int64_t n, int64_t m, int32_t d, float eps, int32_t cg_iters,
+                       void* workspace, size_t workspace_bytes, birkhoff4_stream_t stream) {
+  return eot::hvp_impl(X, Y, f, g, log_a, log_b, V, out, n, m, d, eps, cg_iters, workspace,
+                       workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }

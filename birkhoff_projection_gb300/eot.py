@@ -160,3 +160,33 @@ def apply_plan(X: torch.Tensor, Y: torch.Tensor, f: torch.Tensor, g: torch.Tenso
                                    _ptr(ws), ws.numel(), _stream(X)),
               "eot_apply_plan")
     return out, mass
+
+
+def hvp(X: torch.Tensor, Y: torch.Tensor, f: torch.Tensor, g: torch.Tensor,
+        log_a: torch.Tensor, log_b: torch.Tensor, V: torch.Tensor, eps: float,
+        cg_iters: int = 50, workspace: torch.Tensor = None) -> torch.Tensor:
+    """Hessian-vector product H V [n, d] of the entropic OT cost with respect
+    to X, at Sinkhorn-converged potentials (f, g)."""
+    n = _points(X, "X")
+    m = _points(Y, "Y")
+    if Y.device != X.device or Y.shape[1] != X.shape[1]:
+        raise ValueError("X and Y must share the device and the dimension")
+    if V.shape != X.shape or V.dtype != torch.float32 or V.device != X.device or not V.is_contiguous():
+        raise ValueError("V must be a contiguous float32 tensor shaped like X")
+    for t, name, k in ((f, "f", n), (g, "g", m), (log_a, "log_a", n), (log_b, "log_b", m)):
+        _vector(t, name, k, X.device)
+    d = X.shape[1]
+    need = lib().eot_hvp_workspace_bytes(n, m, d)
+    if need == 0:
+        raise ValueError("invalid sizes")
+    ws = workspace if workspace is not None else torch.empty(need, dtype=torch.uint8,
+                                                             device=X.device)
+    if ws.numel() < need or ws.device != X.device:
+        raise ValueError("workspace needs %d bytes on %s" % (need, X.device))
+    out = torch.empty_like(X)
+    with _on_device(X):
+        check(lib().eot_hvp(_ptr(X), _ptr(Y), _ptr(f), _ptr(g), _ptr(log_a), _ptr(log_b), _ptr(V),
+                            _ptr(out), n, m, d, float(eps), int(cg_iters), _ptr(ws), ws.numel(),
+                            _stream(X)),
+              "eot_hvp")
+    return out

@@ -113,6 +113,30 @@ int eot_transport(const float *X, const float *Y, const float *f, const float *g
                   int64_t n, int64_t m, int32_t d, float eps, void *workspace,
                   size_t workspace_bytes, birkhoff4_stream_t stream);
 
+/* Hessian-vector product of the entropic OT cost with respect to the points
+ * X [FlashSinkhorn, Methodik s3: the HVP as a sequence of transport-vector
+ * and transport-matrix products, the n d x n d Hessian never formed]: out
+ * [n, d] = H V for a direction V [n, d], at potentials (f, g) that
+ * Sinkhorn has converged.  With pi the plan, dC_ij = 2 (x_i - y_j).v_i and
+ * the row marginals fixed:
+ *     (H V)_i = 2 a_i v_i - 2 sum_j dpi_ij y_j,
+ *     dpi_ij = pi_ij (df_i + dg_j - dC_ij) / eps,
+ * where (df, dg) solve the linearised marginal conditions
+ *     [[diag(a), pi], [pi^T, diag(b)]] [df; dg] = [pi dC 1; pi^T dC 1]
+ * by cg_iters steps of conjugate gradients with the diagonal as
+ * preconditioner.  Each step applies pi and pi^T once (two streaming passes
+ * over the n x m scores); the remaining terms are plan applications
+ * (pi Y, pi^T [x.v, V], pi [dg, dg y]) and one second-moment pass
+ * sum_j pi_ij (v_i . y_j) y_j.  All products are one TF32 pass; the CG runs
+ * in fp32 with fp64 dot products, with no host synchronisation.
+ * Workspace: eot_hvp_workspace_bytes(n, m, d), 256-byte aligned.  Errors as
+ * for eot_update, and B4_EINVAL for cg_iters outside 0..100000. */
+size_t eot_hvp_workspace_bytes(int64_t n, int64_t m, int32_t d);
+int eot_hvp(const float *X, const float *Y, const float *f, const float *g, const float *log_a,
+            const float *log_b, const float *V, float *out, int64_t n, int64_t m, int32_t d,
+            float eps, int32_t cg_iters, void *workspace, size_t workspace_bytes,
+            birkhoff4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

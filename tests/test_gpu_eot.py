@@ -275,3 +275,45 @@ def test_sinkhorn_iterations_capture_into_a_cuda_graph():
     torch.cuda.synchronize()
     fe, ge = eot.sinkhorn(X, Y, log_a, log_b, 0.1, 6, workspace=ws)
     assert torch.equal(f, fe) and torch.equal(g, ge)
+
+
+def _hvp_case(n, m, d, eps, seed):
+    X, Y, log_a, log_b = workloads.eot_clouds(n, m, d, seed=seed, device=DEV, random_weights=True)
+    f64, g64 = oeot.sinkhorn64(np64(X), np64(Y), np64(log_a), np64(log_b), eps, 3000)
+    f = torch.tensor(f64, dtype=torch.float32, device=DEV)
+    g = torch.tensor(g64, dtype=torch.float32, device=DEV)
+    return X, Y, log_a, log_b, f, g
+
+
+@pytest.mark.parametrize("n,m,d,eps", [(300, 400, 8, 0.5), (500, 350, 32, 1.0), (200, 600, 3, 0.5)])
+def test_hvp_parity(n, m, d, eps):
+    """eot_hvp against the dense oracle at the same potentials.  Tolerance:
+    relative Frobenius error at most 10x the largest per-entry relative error
+    bound of the plan (the transport bound: every HVP term is a plan
+    application or a solve against plan applications; CG runs long enough
+    to converge at these sizes)."""
+    X, Y, log_a, log_b, f, g = _hvp_case(n, m, d, eps, seed=n + m + d)
+    V = torch.randn(n, d, generator=torch.Generator().manual_seed(d)).to(DEV)
+    Hv = eot.hvp(X, Y, f, g, log_a, log_b, V, eps, cg_iters=150)
+    ref = oeot.hvp64(np64(X), np64(Y), np64(f), np64(g), np64(log_a), np64(log_b), eps, np64(V))
+    fr = np.abs(np64(f)) + eps * np.abs(np64(log_a))
+    rel = np.expm1(row_bound(np64(X), np64(Y), np64(g), np64(log_b), fr, eps, eot.TF32) / 2.0 / eps
+                   + 2.0 ** -20).max() + 2.0 ** -9
+    err = np.linalg.norm(np64(Hv) - ref) / np.linalg.norm(ref)
+    assert np.all(np.isfinite(np64(Hv)))
+    assert err <= 10 * rel, (err, rel)
+
+
+def test_hvp_translation_identity_and_zero_direction():
+    """Along a common translation v_i = t the cost's gradient sum moves by
+    2 t, so sum_i (H v)_i = 2 t; and H 0 = 0 exactly."""
+    n, m, d, eps = 400, 300, 4, 0.5
+    X, Y, log_a, log_b, f, g = _hvp_case(n, m, d, eps, seed=77)
+    t = torch.tensor([0.6, -0.9, 0.3, 1.2], device=DEV)
+    Hv = eot.hvp(X, Y, f, g, log_a, log_b, t.expand(n, d).contiguous(), eps, cg_iters=150)
+    ref = oeot.hvp64(np64(X), np64(Y), np64(f), np64(g), np64(log_a), np64(log_b), eps,
+                     np.tile(np64(t), (n, 1)))
+    s = np64(Hv).sum(0)
+    assert np.abs(s - 2 * np64(t)).max() <= 2e-2 * np.abs(ref).sum(0).max() / n + 1e-3
+    Z = eot.hvp(X, Y, f, g, log_a, log_b, torch.zeros(n, d, device=DEV), eps, cg_iters=10)
+    assert torch.count_nonzero(Z) == 0
