@@ -354,6 +354,9 @@ def main():
         copies = e2e_host(b4, X, G, dev, steps=3)
         best, other = (mapped, copies) if mapped["value"] >= copies["value"] else (copies, mapped)
         best["other_path"] = {k: other[k] for k in ("api", "value", "ms_per_step", "host_link_gbs")}
+        ceiling = host_link_ceiling(dev)
+        best["link_ceiling"] = ceiling
+        best["link_frac"] = best["host_link_gbs"] / ceiling["both_gbs"]
         line["e2e"] = best
     if not args.no_cpu_baseline:
         idx = slice(0, 1 << 22)
@@ -625,6 +628,47 @@ def e2e_mapped(b4, X, G, dev, steps=3):
             "d2h_bytes_per_step": 2 * nbytes, "ms_per_step": ms, "steps": steps,
             "host_link_gbs": 4 * nbytes / (ms * 1e-3) / 1e9,
             "api": "birkhoff4_forward_backward_mapped (zero copy, fused pass)", "numa": numa}
+
+
+def host_link_ceiling(dev, nbytes=1 << 30, reps=3):
+    """What the host link itself moves: copy-engine copies of `nbytes`
+    between pinned host memory and the device, one direction at a time and
+    both at once (two streams).  The e2e step moves as many bytes each way,
+    so `both_gbs` is its ceiling."""
+    import torch
+
+    n = nbytes // 4
+    a = torch.ones(n, dtype=torch.float32, pin_memory=True)
+    b = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    da = torch.empty(n, dtype=torch.float32, device=dev)
+    db = torch.ones(n, dtype=torch.float32, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    cur = torch.cuda.current_stream(dev)
+
+    def timed(h2d, d2h):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            s1.wait_event(e0)
+            s2.wait_event(e0)
+            if h2d:
+                with torch.cuda.stream(s1):
+                    da.copy_(a, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s2):
+                    b.copy_(db, non_blocking=True)
+            cur.wait_stream(s1)
+            cur.wait_stream(s2)
+            e1.record(cur)
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return (int(h2d) + int(d2h)) * nbytes / (best * 1e-3) / 1e9
+
+    return {"h2d_gbs": timed(True, False), "d2h_gbs": timed(False, True),
+            "both_gbs": timed(True, True), "bytes_per_direction": nbytes,
+            "method": "cudaMemcpyAsync pinned<->device, best of %d" % reps}
 
 
 def e2e_host(b4, X, G, dev, steps=3, nstreams=4, chunk=1 << 21):
