@@ -52,7 +52,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose else []
     # tile-shape and pipeline macros for measurement sweeps, e.g.
-    # B4_NVCC_DEFINES="EOT_TR_NEPI=16 B4_FWD_TILE=256"
+    # B4_NVCC_DEFINES="B4_FWD_TILE=256 B4_FWD_NSTAGE=3"
     extra += ["-D" + d for d in os.environ.get("B4_NVCC_DEFINES", "").split()]
 
     def compile_one(src):

@@ -33,51 +33,78 @@ unsigned int* device_fault_latch(cudaError_t* e);  // birkhoff4_api.cu
 namespace eot {
 namespace tr {
 
-#ifndef EOT_TR_DV
-#define EOT_TR_DV 256
-#endif
-constexpr int BN = 128;                    // keys per tile (S = 128 x 128)
-constexpr int DV = EOT_TR_DV;              // value coordinates per launch (O columns)
-#ifndef EOT_TR_NBUF3
-#define EOT_TR_NBUF3 1
-#endif
-#ifndef EOT_TR_NEPI
-#define EOT_TR_NEPI 8
-#endif
-constexpr int NEPI = EOT_TR_NEPI;          // epilogue warps: NEPI / 4 per TMEM lane quarter
+constexpr int DV = 256;                    // value coordinates per launch, at most (O columns)
+constexpr int NEPI = 8;                    // epilogue warps: NEPI / 4 per TMEM lane quarter
 constexpr int NTHREADS = 64 + 32 * NEPI;   // + producer warp + MMA warp
-constexpr int NQK = 3;                     // Q/K chunk stages
-constexpr int NV_MAX = 24;                 // value chunk stages (run time: the region / chunk size)
 constexpr int NBIAS = 4;                   // key-tile bias slots
 constexpr int A_BYTES = BM * KC * 4;       // 16 KB: 128 query rows x 32 coordinates
-constexpr int B_BYTES = BN * KC * 4;       // 16 KB: 128 key rows x 32 coordinates
-constexpr int QK_BYTES = A_BYTES + B_BYTES;
-constexpr int V_REGION = 96 * 1024;       // value chunks of dv coordinates x 32 keys
-constexpr int SMEM = NQK * QK_BYTES + V_REGION + 1024;
-static_assert(DV % KC == 0 && DV <= 256 && V_REGION >= 3 * DV * KC * 4, "value slices");
-constexpr int TMEM_COLS = 512;             // S / P buffers of 128 columns, then O
-constexpr int NBUF_MAX = 3;                // 3 S / P buffers when O needs <= 128 columns
+constexpr int RING_BYTES = 200 * 1024;     // operand ring: Q/K chunks and value chunks
+constexpr int NSLOT_MAX = 8;
+constexpr int TMEM_COLS = 512;             // S / P buffers, then O
+constexpr int NBUF_MAX = 2;
 constexpr int GROUPS = NEPI / 4;           // key groups per tile (one per epilogue warp of a quarter)
-static_assert(NEPI % 4 == 0 && (BN / KC) % GROUPS == 0, "whole chunks per epilogue warp");
-static_assert(SMEM <= 227 * 1024 - 4096, "shared memory");
+constexpr int KEY_PAD = 768;               // key counts padded to a multiple of every tile width
+constexpr int MAX_CTAS = 256;              // partial-result slots are sized for this many CTAs
+static_assert(NEPI % 4 == 0, "whole lane quarters");
+
+// Shapes of one kernel instance: BN keys per tile; two S / P buffers for
+// 192-key tiles (value slices of at most 128 columns: 2 x 192 + 128 TMEM
+// columns), one for 256-key tiles and for the moment form (which keeps S'
+// beside S).  Each ring slot holds one K chunk of S (query and key
+// coordinates) or a group of value chunks.
+template <int BN_, bool MOMENT>
+struct Shape {
+  static constexpr int BN = BN_;
+  static constexpr int NBUF = (BN_ == 192 && !MOMENT) ? 2 : 1;
+  static constexpr int NA = MOMENT ? 2 : 1;  // query operands per K chunk
+  static constexpr int SLOT = NA * A_BYTES + BN * KC * 4;
+  static constexpr int NSLOT = RING_BYTES / SLOT;
+  static constexpr int CPT = BN / KC;          // value chunks per tile
+  static constexpr int CPG = CPT / GROUPS;     // chunks per epilogue warp
+  static constexpr int O_COL = MOMENT ? 2 * BN : NBUF * BN;
+  static constexpr int MAX_DV = TMEM_COLS - O_COL;
+  static constexpr int SMEM = NSLOT * SLOT + 1024;
+  static_assert(NSLOT >= 3 && NSLOT <= NSLOT_MAX, "ring depth");
+  static_assert(CPT % GROUPS == 0, "whole chunks per epilogue warp");
+  static_assert(MAX_DV >= 128, "O columns");
+  static_assert(SLOT % 1024 == 0, "slots keep the 1024-byte swizzle alignment");
+  static_assert(SMEM + NBIAS * BN * 4 + 4096 <= 227 * 1024, "shared memory");
+};
 
 struct Params {
   CUtensorMap qmap;      // query points [nq_pad, d_pad], box {32, 128}
-  CUtensorMap kmap;      // key points [nk_pad, d_pad], box {32, 128}
+  CUtensorMap kmap;      // key points [nk_pad, d_pad], box {32, BN}
   CUtensorMap vmap;      // key points transposed [d_pad, nk_pad], box {32 keys, dv}
   CUtensorMap wmap;      // moment form: the query directions [nq_pad, d_pad], box {32, 128}
   const float* kbias;    // [nk_pad] (g_j - ||y_j||^2) log2(e)/eps + log2 b_j; -inf past nk
   const float* rowterm;  // [nq_pad] (f_i - ||x_i||^2) log2(e)/eps + log2 a_i; -inf past nq
   float* out;            // [nq, d]: columns v0 .. v0 + dv - 1 (those below d) written
   float* mass;           // [nq] row masses, or NULL
+  float* part_o;         // [ctas][2][128][dv]: O of row blocks this CTA covers in part
+  float* part_mass;      // [ctas][2][128]: their row masses
   int64_t nq;
   int32_t d, v0, dv;
-  int32_t nv;            // value stages: V_REGION / (dv * 128), at most NV_MAX
-  int32_t nbuf;          // S / P buffers in TMEM: 3 if dv <= 128, else 2; O follows them
-  int32_t n_rb, n_kt, n_kc;
+  int32_t vg;            // value chunks per ring slot
+  int32_t n_kt, n_kc;
+  // Tiles T = row block * n_kt + key tile, cut into one contiguous run per
+  // CTA: CTA b takes t_base tiles, one more if b < t_rem.
+  int64_t t_base, t_rem;
   float c1;              // 2 log2(e) / eps
   unsigned int* fault;
 };
+
+// First tile and tile count of CTA b.
+__host__ __device__ __forceinline__ int64_t run_start(const Params& p, int64_t b) {
+  return b * p.t_base + (b < p.t_rem ? b : p.t_rem);
+}
+__host__ __device__ __forceinline__ int64_t run_count(const Params& p, int64_t b) {
+  return p.t_base + (b < p.t_rem ? 1 : 0);
+}
+// The CTA whose run holds tile T.
+__host__ __device__ __forceinline__ int64_t run_owner(const Params& p, int64_t T) {
+  const int64_t cut = p.t_rem * (p.t_base + 1);
+  return T < cut ? T / (p.t_base + 1) : p.t_rem + (T - cut) / p.t_base;
+}
 
 // MMA instruction descriptor (kind::tf32, fp32 accumulation, both operands
 // K-major) for M = 128 and a run-time N.
@@ -126,6 +153,34 @@ __global__ void grad_kernel(const float* __restrict__ X, const float* __restrict
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x)
     grad[e] = 2.0f * fmaf(mass[e / d], X[e], -PY[e]);
+}
+
+// Row blocks whose key tiles were split between CTAs: the sum of the
+// partial O (and row masses) those CTAs left in their slots, in CTA order
+// (deterministic).  One CTA per row block; blocks that one CTA covered
+// whole were written by the transport kernel and are skipped.
+__global__ void fixup_kernel(const __grid_constant__ Params p) {
+  const int64_t rb = blockIdx.x;
+  const int64_t b_lo = run_owner(p, rb * p.n_kt), b_hi = run_owner(p, rb * p.n_kt + p.n_kt - 1);
+  if (b_lo == b_hi) return;
+  // slot 0 holds a CTA's first row block, slot 1 its last
+  auto slot = [&](int64_t b) { return b * 2 + (run_start(p, b) / p.n_kt == rb ? 0 : 1); };
+  const int dv = p.dv;
+  for (int e = threadIdx.x; e < BM * dv; e += blockDim.x) {
+    const int row = e / dv, c = e - row * dv;
+    float acc = 0.0f;
+    for (int64_t b = b_lo; b <= b_hi; ++b) acc += p.part_o[(slot(b) * BM + row) * dv + c];
+    const int64_t r = rb * BM + row;
+    if (r < p.nq && p.v0 + c < p.d) p.out[r * p.d + p.v0 + c] = acc;
+  }
+  if (p.mass != nullptr) {
+    for (int row = threadIdx.x; row < BM; row += blockDim.x) {
+      float acc = 0.0f;
+      for (int64_t b = b_lo; b <= b_hi; ++b) acc += p.part_mass[slot(b) * BM + row];
+      const int64_t r = rb * BM + row;
+      if (r < p.nq) p.mass[r] = acc;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -288,46 +343,47 @@ __device__ __forceinline__ float p_chunk(uint32_t (&v)[32], const float4* kb, fl
   return t.x + t.y;
 }
 
-// One CTA per SM, persistent over this CTA's row blocks; its tiles are
-// numbered T = 0, 1, ... (row block major, key tile minor).  Warp roles:
-//   0      producers: lane 0 per tile T the key biases (bulk copy) and the
-//          Q/K chunks of S(T); lane 1 the value chunks of every tile, on a
-//          ring of its own (neither producer can hold the other up);
-//   1      TMEM owner and MMA issuer: S(T) into TMEM buffer T % 2, then
-//          O += P(T - 1) V(T - 1)^T into the O columns with P(T - 1) read
-//          from its TMEM buffer (the order in which the producer loads, so
-//          neither ring can stall the other); the buffer is released when
-//          those MMAs complete;
-//   2..17  epilogue: thread t of warp w owns query row 32 (w % 4) + t and key
-//          group (w - 2) / 4 (32 keys of each tile): p = 2^(S c1 + bias +
+// One CTA per SM.  The tiles T = row block * n_kt + key tile are cut into
+// one contiguous run per CTA (equal counts, so the last wave is full); a
+// run's tiles of one row block form a segment, and a segment that is not
+// the whole row block leaves its O and row masses in the CTA's partial
+// slots for fixup_kernel.  Warp roles:
+//   0      producer (lane 0): per tile the key biases (bulk copy, a ring of
+//          their own), and the operand ring in the order the MMA thread
+//          reads it: the K chunks of S(T) (query and key coordinates) and
+//          the value chunks of P V(T), vg chunks per slot;
+//   1      TMEM owner and MMA issuer (lane 0): S(T) into S / P buffer
+//          T % NBUF; O += P(T) V(T)^T with P(T) read from that buffer, which
+//          is released when those MMAs complete.  With two buffers S(T) is
+//          issued before P V(T - 1), so the epilogue of one tile overlaps the
+//          products of its neighbours; with one, P V(T - 1) goes first;
+//   2..9   epilogue: thread t of warp w owns query row 32 (w % 4) + t and key
+//          group (w - 2) / 4 (BN / 2 keys of each tile): p = 2^(S c1 + bias +
 //          rowterm) stored over its S columns in TMEM, the row mass, and at
-//          the end of a row block its chunks of O.
+//          the end of a segment its chunks of O.
 // MOMENT: the second-moment form used by the Hessian-vector product: with a
 // direction w_i per query, the weights become pi_ij (w_i . y_j), so O_i =
 // sum_j pi_ij (w_i . y_j) y_j.  A second MMA per K chunk (the packed
-// directions as A, the same key tile as B) writes S' = W Y^T beside S
-// (128-key tiles, one S / S' buffer pair), and the epilogue multiplies.
+// directions as A, the same key tile as B) writes S' = W Y^T beside S, and
+// the epilogue multiplies.
 template <int BN_, bool MOMENT>
 __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_constant__ Params p) {
-  // key-tile width: 128 (two or three S / P buffers) or 256 (one buffer)
-  constexpr int BN = BN_;
-  static_assert(!MOMENT || BN == 128, "the moment form keeps S, S' and O in TMEM");
-  constexpr int B_BYTES = BN * KC * 4;
-  constexpr int NA = MOMENT ? 2 : 1;  // query operands per K chunk
-  constexpr int QK_BYTES = NA * A_BYTES + B_BYTES;
-  constexpr int NQK = (BN == 256 || MOMENT) ? 2 : 3;
-  constexpr int CPG = BN / KC / GROUPS;
-  static_assert(NQK * QK_BYTES + V_REGION + 1024 <= 227 * 1024 - 8192, "shared memory");
+  using C = Shape<BN_, MOMENT>;
+  constexpr int BN = C::BN;
+  constexpr int NBUF = C::NBUF;
+  constexpr int SLOT = C::SLOT;
+  constexpr int NSLOT = C::NSLOT;
+  constexpr int CPT = C::CPT;
+  constexpr int CPG = C::CPG;
+  constexpr uint32_t O_COL = C::O_COL;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
+  unsigned char* ring = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  unsigned char* qk_sm = smem;
-  unsigned char* v_sm = smem + NQK * QK_BYTES;
-  __shared__ uint64_t qk_full[NQK], qk_empty[NQK], v_full[NV_MAX], v_empty[NV_MAX];
+  __shared__ uint64_t slot_full[NSLOT_MAX], slot_empty[NSLOT_MAX];
   // p_full is per S / P buffer: one barrier shared by all tiles could see
   // the epilogue complete tile T + 1's phase before the MMA thread had
   // observed tile T's, and the parity wait would then miss it.  Per buffer,
-  // the next arrival needs S(T + nbuf), which the MMA thread issues only
+  // the next arrival needs S(T + NBUF), which the MMA thread issues only
   // after it has consumed tile T's phase.
   __shared__ uint64_t acc_full[NBUF_MAX], acc_empty[NBUF_MAX], p_full[NBUF_MAX];
   __shared__ uint64_t o_full, o_empty, mma_done;
@@ -338,28 +394,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   __shared__ int abort_sh;
   volatile int* abort_flag = &abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int my_rb = (p.n_rb - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                    static_cast<int>(gridDim.x);
-  const int ntiles = my_rb * p.n_kt;
+  const int64_t t0 = run_start(p, blockIdx.x);
+  const int64_t cnt = run_count(p, blockIdx.x);
+  const int64_t n_kt = p.n_kt;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NQK; ++s) {
-      b4::mbar_init(&qk_full[s], 1);
-      b4::mbar_init(&qk_empty[s], 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      b4::mbar_init(&slot_full[s], 1);
+      b4::mbar_init(&slot_empty[s], 1);
     }
-    for (int s = 0; s < p.nv; ++s) {
-      b4::mbar_init(&v_full[s], 1);
-      b4::mbar_init(&v_empty[s], 1);
-    }
-    for (int b = 0; b < NBUF_MAX; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       b4::mbar_init(&acc_full[b], 1);
       b4::mbar_init(&acc_empty[b], 1);
+      b4::mbar_init(&p_full[b], NEPI);
     }
     for (int b = 0; b < NBIAS; ++b) {
       b4::mbar_init(&bias_full[b], 1);
       b4::mbar_init(&bias_empty[b], NEPI);
     }
-    for (int b = 0; b < NBUF_MAX; ++b) b4::mbar_init(&p_full[b], NEPI);
     b4::mbar_init(&o_full, 1);
     b4::mbar_init(&o_empty, NEPI);
     b4::mbar_init(&mma_done, 1);
@@ -380,75 +432,84 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t nbuf = static_cast<uint32_t>(p.nbuf);
-  const uint32_t o_col = MOMENT ? 2 * BN : nbuf * BN;  // O after the S (and S') columns
+  const uint32_t vbytes = static_cast<uint32_t>(p.dv) * KC * 4;
+  const int vg = p.vg;
 
   if (warp == 0) {
-    // ---------------- producers ----------------
-    const uint32_t vbytes = static_cast<uint32_t>(p.dv) * KC * 4;
-    const uint32_t nv = static_cast<uint32_t>(p.nv);
+    // ---------------- producer ----------------
     if (lane == 0) {
-      uint32_t iq = 0, nb = 0;
-      bool ok = true;
-      for (int T = 0; T < ntiles && ok; ++T) {
-        const int rb = static_cast<int>(blockIdx.x) + (T / p.n_kt) * static_cast<int>(gridDim.x);
-        const int kt = T % p.n_kt;
-        const int slot = T % NBIAS;
-        if (!(ok = wait_bar(&bias_empty[slot], ((T / NBIAS) & 1) ^ 1u, abort_flag, p.fault))) break;
-        b4::mbar_arrive_expect_tx(&bias_full[slot], BN * 4);
-        bulk_load_1d(bias_sm[slot], p.kbias + static_cast<int64_t>(kt) * BN, BN * 4, &bias_full[slot]);
+      uint32_t it = 0, nb = 0;  // ring slots and bias slots filled
+      // the K chunks of S(T), after the biases of tile T (local index u)
+      auto load_s = [&](int64_t T, int64_t u) -> bool {
+        const int rb = static_cast<int>(T / n_kt);
+        const int kt = static_cast<int>(T % n_kt);
+        const int bs = static_cast<int>(u % NBIAS);
+        if (!wait_bar(&bias_empty[bs], (static_cast<uint32_t>(u / NBIAS) & 1u) ^ 1u, abort_flag,
+                      p.fault))
+          return false;
+        b4::mbar_arrive_expect_tx(&bias_full[bs], BN * 4);
+        bulk_load_1d(bias_sm[bs], p.kbias + static_cast<int64_t>(kt) * BN, BN * 4, &bias_full[bs]);
         ++nb;
-        for (int kc = 0; kc < p.n_kc; ++kc, ++iq) {
-          const int s = static_cast<int>(iq % NQK);
-          if (!(ok = wait_bar(&qk_empty[s], ((iq / NQK) & 1u) ^ 1u, abort_flag, p.fault))) break;
-          unsigned char* st = qk_sm + s * QK_BYTES;
-          b4::mbar_arrive_expect_tx(&qk_full[s], QK_BYTES);
-          b4::tma_load_2d(st, &p.qmap, &qk_full[s], kc * KC, rb * BM);
-          if (MOMENT) b4::tma_load_2d(st + A_BYTES, &p.wmap, &qk_full[s], kc * KC, rb * BM);
-          b4::tma_load_2d(st + NA * A_BYTES, &p.kmap, &qk_full[s], kc * KC, kt * BN);
+        for (int kc = 0; kc < p.n_kc; ++kc, ++it) {
+          const int s = static_cast<int>(it % NSLOT);
+          if (!wait_bar(&slot_empty[s], ((it / NSLOT) & 1u) ^ 1u, abort_flag, p.fault)) return false;
+          unsigned char* st = ring + s * SLOT;
+          b4::mbar_arrive_expect_tx(&slot_full[s], SLOT);
+          b4::tma_load_2d(st, &p.qmap, &slot_full[s], kc * KC, rb * BM);
+          if (MOMENT) b4::tma_load_2d(st + A_BYTES, &p.wmap, &slot_full[s], kc * KC, rb * BM);
+          b4::tma_load_2d(st + C::NA * A_BYTES, &p.kmap, &slot_full[s], kc * KC, kt * BN);
+        }
+        return true;
+      };
+      // the value chunks of P V(T), vg per slot
+      auto load_v = [&](int64_t T) -> bool {
+        const int kt = static_cast<int>(T % n_kt);
+        for (int c = 0; c < CPT; c += vg, ++it) {
+          const int s = static_cast<int>(it % NSLOT);
+          if (!wait_bar(&slot_empty[s], ((it / NSLOT) & 1u) ^ 1u, abort_flag, p.fault)) return false;
+          unsigned char* st = ring + s * SLOT;
+          b4::mbar_arrive_expect_tx(&slot_full[s], static_cast<uint32_t>(vg) * vbytes);
+          for (int g = 0; g < vg; ++g)
+            b4::tma_load_2d(st + g * vbytes, &p.vmap, &slot_full[s], kt * BN + (c + g) * KC, p.v0);
+        }
+        return true;
+      };
+      bool ok = true;
+      for (int64_t k = 0; k <= cnt && ok; ++k) {
+        if (NBUF == 1) {
+          if (k > 0) ok = load_v(t0 + k - 1);
+          if (ok && k < cnt) ok = load_s(t0 + k, k);
+        } else {
+          if (k < cnt) ok = load_s(t0 + k, k);
+          if (ok && k > 0) ok = load_v(t0 + k - 1);
         }
       }
       // every issued copy lands before the CTA may exit
-      for (uint32_t j = iq > NQK ? iq - NQK : 0u; j < iq; ++j)
-        b4::mbar_wait(&qk_full[j % NQK], (j / NQK) & 1u, kWaitLimitNs);
-      for (uint32_t j = nb > NBIAS ? nb - NBIAS : 0u; j < nb; ++j)
+      for (uint32_t j = it > static_cast<uint32_t>(NSLOT) ? it - NSLOT : 0u; j < it; ++j)
+        b4::mbar_wait(&slot_full[j % NSLOT], (j / NSLOT) & 1u, kWaitLimitNs);
+      for (uint32_t j = nb > static_cast<uint32_t>(NBIAS) ? nb - NBIAS : 0u; j < nb; ++j)
         b4::mbar_wait(&bias_full[j % NBIAS], (j / NBIAS) & 1u, kWaitLimitNs);
-    } else if (lane == 1) {
-      uint32_t iv = 0;
-      bool ok = true;
-      for (int T = 0; T < ntiles && ok; ++T) {
-        const int kt = T % p.n_kt;
-        for (int c = 0; c < BN / KC; ++c, ++iv) {
-          const uint32_t s = iv % nv;
-          if (!(ok = wait_bar(&v_empty[s], ((iv / nv) & 1u) ^ 1u, abort_flag, p.fault))) break;
-          b4::mbar_arrive_expect_tx(&v_full[s], vbytes);
-          b4::tma_load_2d(v_sm + s * vbytes, &p.vmap, &v_full[s], kt * BN + c * KC, p.v0);
-        }
-      }
-      for (uint32_t j = iv > nv ? iv - nv : 0u; j < iv; ++j)
-        b4::mbar_wait(&v_full[j % nv], (j / nv) & 1u, kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t id_s = idesc_tf32_n(BN), id_o = idesc_tf32_n(p.dv);
-      const uint32_t vbytes = static_cast<uint32_t>(p.dv) * KC * 4;
-      const uint32_t nv = static_cast<uint32_t>(p.nv);
-      uint32_t iq = 0, iv = 0;
-      // S(T) = Q K^T into buffer T % nbuf, once that buffer's P has been used
-      auto issue_s = [&](int T) -> bool {
-        const int buf = static_cast<int>(static_cast<uint32_t>(T) % nbuf);
-        const uint32_t use = static_cast<uint32_t>(T) / nbuf;
+      uint32_t it = 0;   // ring slots consumed
+      uint32_t seg = 0;  // segments (runs of one row block) begun
+      // S(T) = Q K^T into buffer u % NBUF, once that buffer's P has been used
+      auto issue_s = [&](int64_t u) -> bool {
+        const int buf = static_cast<int>(u % NBUF);
+        const uint32_t use = static_cast<uint32_t>(u / NBUF);
         if (!wait_bar(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.fault)) return false;
         tc_fence_after();
         const uint32_t d_s = tmem + static_cast<uint32_t>(buf * BN);
-        for (int kc = 0; kc < p.n_kc; ++kc, ++iq) {
-          const int s = static_cast<int>(iq % NQK);
-          if (!wait_bar(&qk_full[s], (iq / NQK) & 1u, abort_flag, p.fault)) return false;
+        for (int kc = 0; kc < p.n_kc; ++kc, ++it) {
+          const int s = static_cast<int>(it % NSLOT);
+          if (!wait_bar(&slot_full[s], (it / NSLOT) & 1u, abort_flag, p.fault)) return false;
           tc_fence_after();
-          const uint32_t a = b4::smem_addr(qk_sm + s * QK_BYTES);
-          const uint64_t da = desc_sw128_kmajor(a), db = desc_sw128_kmajor(a + NA * A_BYTES);
+          const uint32_t a = b4::smem_addr(ring + s * SLOT);
+          const uint64_t da = desc_sw128_kmajor(a), db = desc_sw128_kmajor(a + C::NA * A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < KC / KSTEP; ++kk) {
             const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
@@ -457,52 +518,51 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
               mma_tf32(d_s + BN, desc_sw128_kmajor(a + A_BYTES) + adv, db + adv, id_s,
                        (kc | kk) != 0);
           }
-          mma_commit(&qk_empty[s]);
+          mma_commit(&slot_empty[s]);
         }
         mma_commit(&acc_full[buf]);
         return true;
       };
-      // O += P(U) V(U)^T with P(U) read from its TMEM buffer
-      auto issue_pv = [&](int U) -> bool {
-        const int kt = U % p.n_kt;
-        const bool first = kt == 0, last = kt == p.n_kt - 1;
-        if (first) {
-          const uint32_t rbl = static_cast<uint32_t>(U / p.n_kt);
-          if (!wait_bar(&o_empty, (rbl & 1u) ^ 1u, abort_flag, p.fault)) return false;
-        }
-        const uint32_t buf = static_cast<uint32_t>(U) % nbuf;
-        if (!wait_bar(&p_full[buf], (static_cast<uint32_t>(U) / nbuf) & 1u, abort_flag, p.fault))
+      // O += P(T) V(T)^T with P(T) read from its TMEM buffer
+      auto issue_pv = [&](int64_t T, int64_t u) -> bool {
+        const int64_t kt = T % n_kt;
+        const bool first = kt == 0 || u == 0, last = kt == n_kt - 1 || u == cnt - 1;
+        if (first && !wait_bar(&o_empty, (seg & 1u) ^ 1u, abort_flag, p.fault)) return false;
+        const int buf = static_cast<int>(u % NBUF);
+        if (!wait_bar(&p_full[buf], static_cast<uint32_t>(u / NBUF) & 1u, abort_flag, p.fault))
           return false;
         tc_fence_after();
-        for (int c = 0; c < BN / KC; ++c, ++iv) {
-          const uint32_t s = iv % nv;
-          if (!wait_bar(&v_full[s], (iv / nv) & 1u, abort_flag, p.fault)) return false;
+        for (int c = 0; c < CPT; c += vg, ++it) {
+          const int s = static_cast<int>(it % NSLOT);
+          if (!wait_bar(&slot_full[s], (it / NSLOT) & 1u, abort_flag, p.fault)) return false;
           tc_fence_after();
-          const uint32_t pa = tmem + buf * BN + c * KC;
-          const uint64_t dv = desc_sw128_kmajor(b4::smem_addr(v_sm + s * vbytes));
+          for (int g = 0; g < vg; ++g) {
+            const uint32_t pa = tmem + static_cast<uint32_t>(buf * BN + (c + g) * KC);
+            const uint64_t dvd = desc_sw128_kmajor(b4::smem_addr(ring + s * SLOT + g * vbytes));
 #pragma unroll
-          for (int kk = 0; kk < KC / KSTEP; ++kk) {
-            const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
-            mma_tf32_ts(tmem + o_col, pa + static_cast<uint32_t>(kk * KSTEP), dv + adv, id_o,
-                        !(first && c == 0 && kk == 0));
+            for (int kk = 0; kk < KC / KSTEP; ++kk) {
+              const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
+              mma_tf32_ts(tmem + O_COL, pa + static_cast<uint32_t>(kk * KSTEP), dvd + adv, id_o,
+                          !(first && c + g == 0 && kk == 0));
+            }
           }
-          mma_commit(&v_empty[s]);
+          mma_commit(&slot_empty[s]);
         }
         mma_commit(&acc_empty[buf]);  // the S / P buffer is free once these MMAs are done
-        if (last) mma_commit(&o_full);
+        if (last) {
+          mma_commit(&o_full);
+          ++seg;
+        }
         return true;
       };
-      // with two or three buffers S(T) goes first, so it runs while the
-      // epilogue turns S(T - 1) into P; with one buffer S(T) needs P(T - 1)
-      // consumed first
       bool ok = true;
-      for (int T = 0; T <= ntiles && ok; ++T) {
-        if (nbuf == 1) {
-          if (T > 0) ok = issue_pv(T - 1);
-          if (ok && T < ntiles) ok = issue_s(T);
+      for (int64_t k = 0; k <= cnt && ok; ++k) {
+        if (NBUF == 1) {
+          if (k > 0) ok = issue_pv(t0 + k - 1, k - 1);
+          if (ok && k < cnt) ok = issue_s(k);
         } else {
-          if (T < ntiles) ok = issue_s(T);
-          if (ok && T > 0) ok = issue_pv(T - 1);
+          if (k < cnt) ok = issue_s(k);
+          if (ok && k > 0) ok = issue_pv(t0 + k - 1, k - 1);
         }
       }
       // all MMAs issued by this thread complete before TMEM is released
@@ -516,25 +576,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     const int grp = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t T = 0;
-    for (int rbl = 0; rbl < my_rb; ++rbl) {
-      const int rb = static_cast<int>(blockIdx.x) + rbl * static_cast<int>(gridDim.x);
-      const int64_t r = static_cast<int64_t>(rb) * BM + row;
-      const float rt = p.rowterm[r];
-      float mass = 0.0f;
-      bool ok = true;
-      for (int kt = 0; kt < p.n_kt; ++kt, ++T) {
-        const int buf = static_cast<int>(T % nbuf);
-        const int slot = static_cast<int>(T % NBIAS);
-        ok = wait_bar(&acc_full[buf], (T / nbuf) & 1u, abort_flag, p.fault) &&
-             wait_bar(&bias_full[slot], (T / NBIAS) & 1u, abort_flag, p.fault);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
+    uint32_t sg = 0;  // segments finished
+    int64_t r = 0, kt0 = 0;
+    float rt = 0.0f, mass = 0.0f;
+    bool ok = true;
+    for (int64_t u = 0; u < cnt; ++u) {
+      const int64_t T = t0 + u;
+      const int64_t kt = T % n_kt;
+      if (u == 0 || kt == 0) {  // a segment begins
+        r = (T / n_kt) * BM + row;
+        rt = p.rowterm[r];
+        mass = 0.0f;
+        kt0 = kt;
+      }
+      const int buf = static_cast<int>(u % NBUF);
+      const int bs = static_cast<int>(u % NBIAS);
+      ok = wait_bar(&acc_full[buf], static_cast<uint32_t>(u / NBUF) & 1u, abort_flag, p.fault) &&
+           wait_bar(&bias_full[bs], static_cast<uint32_t>(u / NBIAS) & 1u, abort_flag, p.fault);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
         tc_fence_after();
         // this warp's CPG chunks: the next chunk's TMEM load overlaps the
         // current one's arithmetic; P is stored over S in place
         const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(buf * BN + grp * CPG * KC);
-        const float4* kb = reinterpret_cast<const float4*>(&bias_sm[slot][grp * CPG * KC]);
+        const float4* kb = reinterpret_cast<const float4*>(&bias_sm[bs][grp * CPG * KC]);
         uint32_t v[32], w[32];
         tmem_ld32(taddr, v);
         tmem_wait32(v);
@@ -561,44 +626,61 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&p_full[buf]);
-          mbar_arrive(&bias_empty[slot]);
+          mbar_arrive(&bias_empty[bs]);
         }
       }
-      if (ok) {
-        ok = wait_bar(&o_full, static_cast<uint32_t>(rbl) & 1u, abort_flag, p.fault);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      if (ok) {
-        tc_fence_after();
-        for (int c = grp; c * KC < p.dv; c += GROUPS) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_base + o_col + static_cast<uint32_t>(c * KC), o);
-          tmem_wait32(o);
-          if (r < p.nq) {
-            float* orow = p.out + r * p.d;
-            const int c0 = p.v0 + c * KC;
+      // end of a segment (or a failed wait): O and the row masses.  Every
+      // epilogue warp reaches the two named barriers below once per segment,
+      // or once more when it gives up, so none waits for a warp that left.
+      if (!ok || kt == n_kt - 1 || u == cnt - 1) {
+        const bool whole = kt0 == 0 && kt == n_kt - 1;  // the segment is the whole row block
+        const int64_t pslot = static_cast<int64_t>(blockIdx.x) * 2 + (sg == 0 ? 0 : 1);
+        if (ok) {
+          ok = wait_bar(&o_full, sg & 1u, abort_flag, p.fault);
+          ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+          tc_fence_after();
+          for (int c = grp; c * KC < p.dv; c += GROUPS) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + O_COL + static_cast<uint32_t>(c * KC), o);
+            tmem_wait32(o);
+            if (whole) {
+              if (r < p.nq) {
+                float* orow = p.out + r * p.d;
+                const int c0 = p.v0 + c * KC;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c0 + i < p.d) orow[c0 + i] = __uint_as_float(o[i]);
+                for (int i = 0; i < 32; ++i)
+                  if (c0 + i < p.d) orow[c0 + i] = __uint_as_float(o[i]);
+              }
+            } else {
+              float4* prow = reinterpret_cast<float4*>(p.part_o + (pslot * BM + row) * p.dv + c * KC);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                prow[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                      __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+            }
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&o_empty);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&o_empty);
-      }
-      // row masses: the four key groups of a row (every epilogue warp reaches
-      // both barriers; an abort is seen by all of them after the first)
-      if (grp > 0) mass_sh[grp - 1][row] = mass;
-      named_bar_sync(1, 32 * NEPI);
-      if (grp == 0 && ok && !*abort_flag && p.mass != nullptr && r < p.nq)
-        p.mass[r] = [&] {
+        // row masses: the key groups of a row
+        if (grp > 0) mass_sh[grp - 1][row] = mass;
+        named_bar_sync(1, 32 * NEPI);
+        if (grp == 0 && ok && !*abort_flag && p.mass != nullptr) {
           float m = mass;
 #pragma unroll
           for (int g = 0; g < GROUPS - 1; ++g) m += mass_sh[g][row];
-          return m;
-        }();
-      named_bar_sync(1, 32 * NEPI);
-      if (*abort_flag) break;
+          if (!whole)
+            p.part_mass[pslot * BM + row] = m;
+          else if (r < p.nq)
+            p.mass[r] = m;
+        }
+        named_bar_sync(1, 32 * NEPI);
+        ++sg;
+        if (*abort_flag || !ok) break;
+      }
     }
   }
   tc_fence_before();
@@ -617,40 +699,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
 namespace {
 
 struct TrLayout {
-  int64_t n_pad, m_pad;
+  int64_t n_pad, m_pad, n_rb, ctas;
   int32_t d_pad, v_pad;
-  size_t x, y, yt, xn, yn, kb, rt, wq, wn, total;  // byte offsets (yt: the values, transposed)
+  // byte offsets (yt: the values, transposed; po, pm: partial O and masses)
+  size_t x, y, yt, xn, yn, kb, rt, wq, wn, po, pm, total;
 };
 
 // moment: also room for the packed query directions (wq) and their norms
 TrLayout tr_layout(int64_t n, int64_t m, int32_t d, int32_t dv, bool moment = false) {
   TrLayout L;
   L.n_pad = round_up(std::max<int64_t>(n, 1), ROW_PAD);
-  L.m_pad = round_up(std::max<int64_t>(m, 1), ROW_PAD);
+  L.m_pad = round_up(std::max<int64_t>(m, 1), tr::KEY_PAD);
+  L.n_rb = L.n_pad / BM;
   L.d_pad = static_cast<int32_t>(round_up(d, KC));
   L.v_pad = static_cast<int32_t>(round_up(dv, KC));
+  // partial slots for at most one CTA per 128-key tile (the narrowest tiles)
+  L.ctas = std::min<int64_t>(tr::MAX_CTAS, L.n_rb * (L.m_pad / 128));
+  const int64_t dvs = std::min<int64_t>(tr::DV, L.v_pad);
   size_t o = 0;
-  L.x = o;
-  o += align_bytes(static_cast<size_t>(L.n_pad) * L.d_pad * 4);
-  L.y = o;
-  o += align_bytes(static_cast<size_t>(L.m_pad) * L.d_pad * 4);
-  L.yt = o;
-  o += align_bytes(static_cast<size_t>(L.m_pad) * L.v_pad * 4);
-  L.xn = o;
-  o += align_bytes(static_cast<size_t>(L.n_pad) * 4);
-  L.yn = o;
-  o += align_bytes(static_cast<size_t>(L.m_pad) * 4);
-  L.kb = o;
-  o += align_bytes(static_cast<size_t>(L.m_pad) * 4);
-  L.rt = o;
-  o += align_bytes(static_cast<size_t>(L.n_pad) * 4);
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_bytes(bytes);
+    return at;
+  };
+  L.x = take(static_cast<size_t>(L.n_pad) * L.d_pad * 4);
+  L.y = take(static_cast<size_t>(L.m_pad) * L.d_pad * 4);
+  L.yt = take(static_cast<size_t>(L.m_pad) * L.v_pad * 4);
+  L.xn = take(static_cast<size_t>(L.n_pad) * 4);
+  L.yn = take(static_cast<size_t>(L.m_pad) * 4);
+  L.kb = take(static_cast<size_t>(L.m_pad) * 4);
+  L.rt = take(static_cast<size_t>(L.n_pad) * 4);
   L.wq = L.wn = 0;
   if (moment) {
-    L.wq = o;
-    o += align_bytes(static_cast<size_t>(L.n_pad) * L.d_pad * 4);
-    L.wn = o;
-    o += align_bytes(static_cast<size_t>(L.n_pad) * 4);
+    L.wq = take(static_cast<size_t>(L.n_pad) * L.d_pad * 4);
+    L.wn = take(static_cast<size_t>(L.n_pad) * 4);
   }
+  L.po = take(static_cast<size_t>(L.ctas) * 2 * BM * dvs * 4);
+  L.pm = take(static_cast<size_t>(L.ctas) * 2 * BM * 4);
   L.total = o;
   return L;
 }
@@ -660,36 +745,54 @@ bool tr_sizes_ok(int64_t n, int64_t m, int32_t d, int32_t dv) {
          dv >= 1 && dv <= 16384;
 }
 
-// Key-tile width of the transport kernel: 256 (one S / P buffer; S as
-// 128 x 256 MMAs) measured about 15% faster than 128 (three buffers, 128 x
-// 128 MMAs) at d = 64 and 512 on GB300.
-#ifndef EOT_TR_BN
-#define EOT_TR_BN 256
-#endif
-constexpr int kTrBn = EOT_TR_BN;
-constexpr int kTrSmem = (kTrBn == 256 ? 2 : 3) * (tr::A_BYTES + kTrBn * KC * 4) + tr::V_REGION + 1024;
-constexpr int kMomSmem = 2 * (2 * tr::A_BYTES + 128 * KC * 4) + tr::V_REGION + 1024;
+// One launch of transport_kernel<BN, MOMENT> for the value slice in p
+// (v0, dv), then the fix-up of the row blocks that were split between CTAs.
+template <int BN, bool MOMENT>
+cudaError_t launch_shape(tr::Params& p, const TrLayout& L, const float* yp, int dev, int nsm,
+                         cudaStream_t stream) {
+  using C = tr::Shape<BN, MOMENT>;
+  static std::atomic<int> attr_done[64];
+  if (dev >= 64 || attr_done[dev].load(std::memory_order_acquire) == 0) {
+    const cudaError_t err = cudaFuncSetAttribute(tr::transport_kernel<BN, MOMENT>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) attr_done[dev].store(1, std::memory_order_release);
+  }
+  if (p.dv > C::MAX_DV || !encode_rows128(&p.kmap, yp, L.m_pad, L.d_pad, BN))
+    return cudaErrorInvalidValue;
+  // value chunks per ring slot: the largest divisor of the chunks per tile
+  // that fits
+  const int vbytes = p.dv * KC * 4;
+  p.vg = 1;
+  for (int g = C::CPT; g >= 1; --g)
+    if (C::CPT % g == 0 && g * vbytes <= C::SLOT) {
+      p.vg = g;
+      break;
+    }
+  p.n_kt = static_cast<int32_t>(L.m_pad / BN);
+  const int64_t tiles = L.n_rb * p.n_kt;
+  const int64_t ctas = std::min<int64_t>(std::min<int64_t>(nsm, tiles), L.ctas);
+  p.t_base = tiles / ctas;
+  p.t_rem = tiles % ctas;
+  tr::transport_kernel<BN, MOMENT><<<static_cast<unsigned>(ctas), tr::NTHREADS, C::SMEM, stream>>>(p);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  tr::fixup_kernel<<<static_cast<unsigned>(L.n_rb), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
-// Key-tile width of a launch: the moment form needs 128 (S, S' and O in TMEM).
-int tile_keys(bool moment) { return moment ? 128 : kTrBn; }
-
-cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const float* yt, int32_t v0,
-                             int32_t dv, float* mass, bool moment, cudaStream_t stream) {
+// Key-tile shape of a slice: 192-key tiles with two S / P buffers when the
+// slice has at most 128 value columns (the epilogue of one tile overlaps the
+// products of the next), else 256-key tiles with one; the moment form keeps
+// S' beside S in 128-key tiles.
+cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const float* yp,
+                             const float* yt, int32_t v0, int32_t dv, float* mass, bool moment,
+                             cudaStream_t stream) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   const int nsm = b4::sm_count(dev);
   if (nsm <= 0) return cudaErrorInvalidDevice;
-  static std::atomic<int> attr_done[64], attr_mom[64];
-  std::atomic<int>* done = moment ? attr_mom : attr_done;
-  if (dev < 64 && done[dev].load(std::memory_order_acquire) == 0) {
-    err = moment ? cudaFuncSetAttribute(tr::transport_kernel<128, true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kMomSmem)
-                 : cudaFuncSetAttribute(tr::transport_kernel<kTrBn, false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kTrSmem);
-    if (err != cudaSuccess) return err;
-    done[dev].store(1, std::memory_order_release);
-  }
   tr::Params p = base;
   // value operand: rows v0 .. v0 + dv - 1 of the transposed key points
   {
@@ -706,15 +809,10 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const fl
   }
   p.v0 = v0;
   p.dv = dv;
-  p.nv = std::min(tr::NV_MAX, tr::V_REGION / (dv * eot::KC * 4));
-  p.nbuf = (moment || kTrBn == 256) ? 1 : ((EOT_TR_NBUF3 != 0 && dv <= 128) ? 3 : 2);
   p.mass = mass;
-  const int grid = std::min(p.n_rb, nsm);
-  if (moment)
-    tr::transport_kernel<128, true><<<grid, tr::NTHREADS, kMomSmem, stream>>>(p);
-  else
-    tr::transport_kernel<kTrBn, false><<<grid, tr::NTHREADS, kTrSmem, stream>>>(p);
-  return cudaGetLastError();
+  if (moment) return launch_shape<128, true>(p, L, yp, dev, nsm, stream);
+  if (dv <= 128) return launch_shape<192, false>(p, L, yp, dev, nsm, stream);
+  return launch_shape<256, false>(p, L, yp, dev, nsm, stream);
 }
 
 // The plan of (f, g) applied to the values V [m, dv]: out = pi V, mass =
@@ -737,7 +835,6 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
     return B4_EINVAL;
   cudaError_t e = cudaSuccess;
   unsigned int* fault = b4::device_fault_latch(&e);
-  const int bn = tile_keys(moment);
   if (e != cudaSuccess) return b4::record_cuda_error(e);
   unsigned char* w = static_cast<unsigned char*>(workspace);
   float* xp = reinterpret_cast<float*>(w + L.x);
@@ -766,7 +863,6 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   if (e != cudaSuccess) return b4::record_cuda_error(e);
   tr::Params p;
   if (!encode_rows128(&p.qmap, xp, L.n_pad, L.d_pad, BM) ||
-      !encode_rows128(&p.kmap, yp, L.m_pad, L.d_pad, bn) ||
       (moment && !encode_rows128(&p.wmap, wq, L.n_pad, L.d_pad, BM)))
     return b4::record_cuda_error(cudaErrorInvalidValue);
   if (!moment) p.wmap = p.qmap;
@@ -774,10 +870,10 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   p.rowterm = rt;
   p.out = out;
   p.mass = nullptr;
+  p.part_o = reinterpret_cast<float*>(w + L.po);
+  p.part_mass = reinterpret_cast<float*>(w + L.pm);
   p.nq = n;
   p.d = dv;
-  p.n_rb = static_cast<int32_t>(L.n_pad / BM);
-  p.n_kt = static_cast<int32_t>(L.m_pad / bn);
   p.n_kc = L.d_pad / KC;
   p.c1 = static_cast<float>(2.0 * 1.4426950408889634 / eps);
   p.fault = fault;
@@ -785,7 +881,7 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   // writes the row masses
   for (int32_t v0 = 0; v0 < L.v_pad && e == cudaSuccess; v0 += tr::DV) {
     const int32_t w_slice = std::min<int32_t>(tr::DV, L.v_pad - v0);
-    e = launch_transport(p, L, vt, v0, w_slice, v0 == 0 ? mass : nullptr, moment, s);
+    e = launch_transport(p, L, yp, vt, v0, w_slice, v0 == 0 ? mass : nullptr, moment, s);
   }
   return b4::record_cuda_error(e);
 }

@@ -167,6 +167,7 @@ TRANSPORT_CASES = [
     (129, 257, 160),   # two value slices, ragged everything
     (1, 1, 1),
     (20000, 300, 8),   # more row blocks than SMs
+    (40000, 200, 4),   # CTA runs spanning two or three row blocks: whole and split ones
     (300, 400, 520),   # five value slices
 ]
 
