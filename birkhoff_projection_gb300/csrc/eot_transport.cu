@@ -47,28 +47,36 @@ constexpr int KEY_PAD = 768;               // key counts padded to a multiple of
 constexpr int MAX_CTAS = 256;              // partial-result slots are sized for this many CTAs
 static_assert(NEPI % 4 == 0, "whole lane quarters");
 
+// What a launch computes:
+//   VALUES  O = P V on the tensor cores (P from TMEM, V^T from shared memory);
+//   MOMENT  the same with P weighted by S' = W Y^T (see transport_kernel);
+//   VECTOR  one value column: o_i = sum_j p_ij v_j on the CUDA cores of the
+//           epilogue, which leaves the tensor pipe to S alone.
+enum Mode : int { VALUES = 0, MOMENT = 1, VECTOR = 2 };
+
 // Shapes of one kernel instance: BN keys per tile; two S / P buffers for
-// 192-key tiles (value slices of at most 128 columns: 2 x 192 + 128 TMEM
-// columns), one for 256-key tiles and for the moment form (which keeps S'
-// beside S).  Each ring slot holds one K chunk of S (query and key
-// coordinates) or a group of value chunks.
-template <int BN_, bool MOMENT>
+// 192-key value tiles (slices of at most 128 columns: 2 x 192 + 128 TMEM
+// columns) and for 256-key vector tiles (no O in TMEM), one for 256-key
+// value tiles and for the moment form (which keeps S' beside S).  Each ring
+// slot holds one K chunk of S (query and key coordinates) or a group of
+// value chunks.
+template <int BN_, int MODE>
 struct Shape {
   static constexpr int BN = BN_;
-  static constexpr int NBUF = (BN_ == 192 && !MOMENT) ? 2 : 1;
-  static constexpr int NA = MOMENT ? 2 : 1;  // query operands per K chunk
+  static constexpr int NBUF = ((BN_ == 192 && MODE == VALUES) || MODE == VECTOR) ? 2 : 1;
+  static constexpr int NA = MODE == MOMENT ? 2 : 1;  // query operands per K chunk
   static constexpr int SLOT = NA * A_BYTES + BN * KC * 4;
   static constexpr int NSLOT = RING_BYTES / SLOT;
   static constexpr int CPT = BN / KC;          // value chunks per tile
   static constexpr int CPG = CPT / GROUPS;     // chunks per epilogue warp
-  static constexpr int O_COL = MOMENT ? 2 * BN : NBUF * BN;
-  static constexpr int MAX_DV = TMEM_COLS - O_COL;
+  static constexpr int O_COL = MODE == MOMENT ? 2 * BN : NBUF * BN;
+  static constexpr int MAX_DV = MODE == VECTOR ? 1 : TMEM_COLS - O_COL;
   static constexpr int SMEM = NSLOT * SLOT + 1024;
   static_assert(NSLOT >= 3 && NSLOT <= NSLOT_MAX, "ring depth");
   static_assert(CPT % GROUPS == 0, "whole chunks per epilogue warp");
-  static_assert(MAX_DV >= 128, "O columns");
+  static_assert(O_COL <= TMEM_COLS && (MODE == VECTOR || MAX_DV >= 128), "O columns");
   static_assert(SLOT % 1024 == 0, "slots keep the 1024-byte swizzle alignment");
-  static_assert(SMEM + NBIAS * BN * 4 + 4096 <= 227 * 1024, "shared memory");
+  static_assert(SMEM + 2 * NBIAS * BN * 4 + 4096 <= 227 * 1024, "shared memory");
 };
 
 struct Params {
@@ -78,6 +86,7 @@ struct Params {
   CUtensorMap wmap;      // moment form: the query directions [nq_pad, d_pad], box {32, 128}
   const float* kbias;    // [nk_pad] (g_j - ||y_j||^2) log2(e)/eps + log2 b_j; -inf past nk
   const float* rowterm;  // [nq_pad] (f_i - ||x_i||^2) log2(e)/eps + log2 a_i; -inf past nq
+  const float* kval;     // VECTOR: the value column [nk_pad], zero past nk
   float* out;            // [nq, d]: columns v0 .. v0 + dv - 1 (those below d) written
   float* mass;           // [nq] row masses, or NULL
   float* part_o;         // [ctas][2][128][dv]: O of row blocks this CTA covers in part
@@ -275,40 +284,101 @@ __global__ void cg_matvec_kernel(const float* __restrict__ diag, const float* __
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i < N) Ap[i] = fmaf(diag[i], p[i], Pp[i]);
 }
+// The two plan products of a step are computed separately and each carries
+// the rounding of its scores, so the operator CG sees is symmetric only to
+// about 1e-3: the residual r^T D^-1 r levels off near 1e-8 of its first
+// value and, iterated further, grows again.  So the iteration stops (alpha =
+// beta = 0 from then on) once r^T D^-1 r is 1e-8 of its first value or has
+// risen 1e4-fold above the smallest value seen, and the iterate with the
+// smallest value is the one returned.
+constexpr double kCgRelTol2 = 1e-8;
+constexpr double kCgRise = 1e4;
+__device__ __forceinline__ bool cg_live(const double* rs, const double* rs0, const double* best) {
+  return *rs > 1e-300 && *rs > kCgRelTol2 * *rs0 && *rs <= kCgRise * *best;
+}
 // z += alpha p, res -= alpha Ap, s = res / diag; alpha = rs / pAp (0 once
-// the residual has vanished)
+// the iteration has stopped)
 __global__ void cg_step_kernel(const double* __restrict__ rs, const double* __restrict__ pAp,
-                               const float* __restrict__ p, const float* __restrict__ Ap,
-                               const float* __restrict__ diag, int64_t N, float* __restrict__ z,
-                               float* __restrict__ res, float* __restrict__ sv) {
+                               const double* __restrict__ rs0, const double* __restrict__ best,
+                               const float* __restrict__ p,
+                               const float* __restrict__ Ap, const float* __restrict__ diag,
+                               int64_t N, float* __restrict__ z, float* __restrict__ res,
+                               float* __restrict__ sv) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= N) return;
   const double den = *pAp;
-  const float alpha = den > 1e-300 ? static_cast<float>(*rs / den) : 0.0f;
+  const float alpha =
+      (den > 1e-300 && cg_live(rs, rs0, best)) ? static_cast<float>(*rs / den) : 0.0f;
   z[i] = fmaf(alpha, p[i], z[i]);
   res[i] = fmaf(-alpha, Ap[i], res[i]);
   sv[i] = res[i] / diag[i];
 }
 // p = s + beta p, beta = rs_new / rs
 __global__ void cg_dir_kernel(const double* __restrict__ rs, const double* __restrict__ rs_new,
+                              const double* __restrict__ rs0, const double* __restrict__ best,
                               const float* __restrict__ sv, int64_t N, float* __restrict__ p) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= N) return;
-  const double r0 = *rs;
-  const float beta = r0 > 1e-300 ? static_cast<float>(*rs_new / r0) : 0.0f;
+  const float beta = (cg_live(rs, rs0, best) && cg_live(rs_new, rs0, best))
+                         ? static_cast<float>(*rs_new / *rs)
+                         : 0.0f;
   p[i] = fmaf(beta, p[i], sv[i]);
 }
-// z = 0, res = rhs, s = res / diag, p = s; diag = [a ; b]
+// One thread: keep = (rs < best), and best = min(best, rs).
+__global__ void cg_best_kernel(const double* __restrict__ rs, double* __restrict__ best,
+                               double* __restrict__ keep) {
+  const bool b = *rs < *best;
+  *keep = b ? 1.0 : 0.0;
+  if (b) *best = *rs;
+}
+// zb = z where the iterate just made is the best so far.
+__global__ void cg_keep_kernel(const double* __restrict__ keep, const float* __restrict__ z,
+                               int64_t N, float* __restrict__ zb) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < N && *keep != 0.0) zb[i] = z[i];
+}
+__global__ void copy_scalar_kernel(const double* __restrict__ src, double* __restrict__ dst) {
+  *dst = *src;
+}
+// Partial sums of z . n0 with n0 = (1 on the first n entries, -1 on the
+// rest): the direction along which (df, dg) leave pi's perturbation, and so
+// H v, unchanged (df_i + dg_j is what enters).
+__global__ void null_partial_kernel(const float* __restrict__ z, int64_t n, int64_t N,
+                                    double* __restrict__ part) {
+  __shared__ double sh[256];
+  double acc = 0.0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < N;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    acc += i < n ? static_cast<double>(z[i]) : -static_cast<double>(z[i]);
+  sh[threadIdx.x] = acc;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) part[blockIdx.x] = sh[0];
+}
+// z -= (z . n0 / N) n0: the drift CG accumulates along n0 is removed, so
+// the final combination does not cancel large equal and opposite offsets.
+__global__ void null_remove_kernel(const double* __restrict__ zn, int64_t n, int64_t N,
+                                   float* __restrict__ z) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const float c = static_cast<float>(*zn / static_cast<double>(N));
+  z[i] -= i < n ? c : -c;
+}
+// z = zb = 0, res = rhs, s = res / diag, p = s; diag = [a ; b]
 __global__ void cg_init_kernel(const float* __restrict__ rhs, const float* __restrict__ log_a,
                                const float* __restrict__ log_b, int64_t n, int64_t N,
                                float* __restrict__ diag, float* __restrict__ z,
-                               float* __restrict__ res, float* __restrict__ sv,
-                               float* __restrict__ p) {
+                               float* __restrict__ zb, float* __restrict__ res,
+                               float* __restrict__ sv, float* __restrict__ p) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= N) return;
   const float dg = __expf(i < n ? log_a[i] : log_b[i - n]);
   diag[i] = dg;
   z[i] = 0.0f;
+  zb[i] = 0.0f;
   res[i] = rhs[i];
   sv[i] = rhs[i] / dg;
   p[i] = sv[i];
@@ -366,9 +436,14 @@ __device__ __forceinline__ float p_chunk(uint32_t (&v)[32], const float4* kb, fl
 // sum_j pi_ij (w_i . y_j) y_j.  A second MMA per K chunk (the packed
 // directions as A, the same key tile as B) writes S' = W Y^T beside S, and
 // the epilogue multiplies.
-template <int BN_, bool MOMENT>
+// VECTOR: a single value column.  The producer copies each tile's values
+// beside its biases, the MMA thread issues S alone, and the epilogue forms
+// o_i = sum_j p_ij v_j in registers and releases the S buffer itself.
+template <int BN_, int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_constant__ Params p) {
-  using C = Shape<BN_, MOMENT>;
+  using C = Shape<BN_, MODE>;
+  constexpr bool MOMENT = MODE == tr::MOMENT;
+  constexpr bool VEC = MODE == VECTOR;
   constexpr int BN = C::BN;
   constexpr int NBUF = C::NBUF;
   constexpr int SLOT = C::SLOT;
@@ -389,7 +464,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   __shared__ uint64_t o_full, o_empty, mma_done;
   __shared__ uint64_t bias_full[NBIAS], bias_empty[NBIAS];
   __shared__ __align__(16) float bias_sm[NBIAS][BN];
+  __shared__ __align__(16) float val_sm[VEC ? NBIAS : 1][VEC ? BN : 4];
   __shared__ float mass_sh[GROUPS > 1 ? GROUPS - 1 : 1][BM];
+  __shared__ float vec_sh[VEC && GROUPS > 1 ? GROUPS - 1 : 1][VEC ? BM : 1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   volatile int* abort_flag = &abort_sh;
@@ -405,7 +482,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     }
     for (int b = 0; b < NBUF; ++b) {
       b4::mbar_init(&acc_full[b], 1);
-      b4::mbar_init(&acc_empty[b], 1);
+      b4::mbar_init(&acc_empty[b], VEC ? NEPI : 1);  // VECTOR: released by the epilogue warps
       b4::mbar_init(&p_full[b], NEPI);
     }
     for (int b = 0; b < NBIAS; ++b) {
@@ -447,8 +524,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         if (!wait_bar(&bias_empty[bs], (static_cast<uint32_t>(u / NBIAS) & 1u) ^ 1u, abort_flag,
                       p.fault))
           return false;
-        b4::mbar_arrive_expect_tx(&bias_full[bs], BN * 4);
+        b4::mbar_arrive_expect_tx(&bias_full[bs], (VEC ? 2 : 1) * BN * 4);
         bulk_load_1d(bias_sm[bs], p.kbias + static_cast<int64_t>(kt) * BN, BN * 4, &bias_full[bs]);
+        if (VEC)
+          bulk_load_1d(val_sm[bs], p.kval + static_cast<int64_t>(kt) * BN, BN * 4, &bias_full[bs]);
         ++nb;
         for (int kc = 0; kc < p.n_kc; ++kc, ++it) {
           const int s = static_cast<int>(it % NSLOT);
@@ -476,7 +555,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       };
       bool ok = true;
       for (int64_t k = 0; k <= cnt && ok; ++k) {
-        if (NBUF == 1) {
+        if (VEC) {
+          if (k < cnt) ok = load_s(t0 + k, k);
+        } else if (NBUF == 1) {
           if (k > 0) ok = load_v(t0 + k - 1);
           if (ok && k < cnt) ok = load_s(t0 + k, k);
         } else {
@@ -557,7 +638,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       };
       bool ok = true;
       for (int64_t k = 0; k <= cnt && ok; ++k) {
-        if (NBUF == 1) {
+        if (VEC) {
+          if (k < cnt) ok = issue_s(k);
+        } else if (NBUF == 1) {
           if (k > 0) ok = issue_pv(t0 + k - 1, k - 1);
           if (ok && k < cnt) ok = issue_s(k);
         } else {
@@ -578,7 +661,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t sg = 0;  // segments finished
     int64_t r = 0, kt0 = 0;
-    float rt = 0.0f, mass = 0.0f;
+    float rt = 0.0f, mass = 0.0f, ov = 0.0f;  // ov: VECTOR's sum_j p_ij v_j
     bool ok = true;
     for (int64_t u = 0; u < cnt; ++u) {
       const int64_t T = t0 + u;
@@ -587,6 +670,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         r = (T / n_kt) * BM + row;
         rt = p.rowterm[r];
         mass = 0.0f;
+        ov = 0.0f;
         kt0 = kt;
       }
       const int buf = static_cast<int>(u % NBUF);
@@ -607,6 +691,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         for (int ch = 0; ch < CPG; ++ch) {
           if (ch + 1 < CPG) tmem_ld32(taddr + static_cast<uint32_t>((ch + 1) * KC), w);
           mass += p_chunk(v, kb + ch * 8, p.c1, rt);
+          if (VEC) {  // the value column on the CUDA cores; S is not written back
+            const float4* vv = reinterpret_cast<const float4*>(&val_sm[bs][(grp * CPG + ch) * KC]);
+            float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 x = vv[i];
+              a0 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])),
+                              make_float2(x.x, x.y), a0);
+              a1 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
+                              make_float2(x.z, x.w), a1);
+            }
+            const float2 a = __fadd2_rn(a0, a1);
+            ov += a.x + a.y;
+          }
           if (MOMENT) {  // weight pi_ij (w_i . y_j): S' sits BN columns after S
             uint32_t sp[32];
             tmem_ld32(taddr + static_cast<uint32_t>(BN + ch * KC), sp);
@@ -615,7 +713,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
             for (int i = 0; i < 32; ++i)
               v[i] = __float_as_uint(__uint_as_float(v[i]) * __uint_as_float(sp[i]));
           }
-          tmem_st32(taddr + static_cast<uint32_t>(ch * KC), v);
+          if (!VEC) tmem_st32(taddr + static_cast<uint32_t>(ch * KC), v);
           if (ch + 1 < CPG) {
             tmem_wait32(w);
 #pragma unroll
@@ -625,7 +723,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&p_full[buf]);
+          mbar_arrive(VEC ? &acc_empty[buf] : &p_full[buf]);
           mbar_arrive(&bias_empty[bs]);
         }
       }
@@ -635,11 +733,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       if (!ok || kt == n_kt - 1 || u == cnt - 1) {
         const bool whole = kt0 == 0 && kt == n_kt - 1;  // the segment is the whole row block
         const int64_t pslot = static_cast<int64_t>(blockIdx.x) * 2 + (sg == 0 ? 0 : 1);
-        if (ok) {
+        if (ok && !VEC) {
           ok = wait_bar(&o_full, sg & 1u, abort_flag, p.fault);
           ok = __all_sync(0xffffffffu, ok);
         }
-        if (ok) {
+        if (ok && !VEC) {
           tc_fence_after();
           for (int c = grp; c * KC < p.dv; c += GROUPS) {
             uint32_t o[32];
@@ -665,17 +763,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
           __syncwarp();
           if (lane == 0) mbar_arrive(&o_empty);
         }
-        // row masses: the key groups of a row
-        if (grp > 0) mass_sh[grp - 1][row] = mass;
+        // row masses (and VECTOR's o_i): the key groups of a row
+        if (grp > 0) {
+          mass_sh[grp - 1][row] = mass;
+          if (VEC) vec_sh[grp - 1][row] = ov;
+        }
         named_bar_sync(1, 32 * NEPI);
-        if (grp == 0 && ok && !*abort_flag && p.mass != nullptr) {
-          float m = mass;
+        if (grp == 0 && ok && !*abort_flag) {
+          if (p.mass != nullptr) {
+            float m = mass;
 #pragma unroll
-          for (int g = 0; g < GROUPS - 1; ++g) m += mass_sh[g][row];
-          if (!whole)
-            p.part_mass[pslot * BM + row] = m;
-          else if (r < p.nq)
-            p.mass[r] = m;
+            for (int g = 0; g < GROUPS - 1; ++g) m += mass_sh[g][row];
+            if (!whole)
+              p.part_mass[pslot * BM + row] = m;
+            else if (r < p.nq)
+              p.mass[r] = m;
+          }
+          if (VEC) {
+            float o = ov;
+#pragma unroll
+            for (int g = 0; g < GROUPS - 1; ++g) o += vec_sh[g][row];
+            if (!whole)
+              p.part_o[pslot * BM + row] = o;
+            else if (r < p.nq)
+              p.out[r * p.d + p.v0] = o;
+          }
         }
         named_bar_sync(1, 32 * NEPI);
         ++sg;
@@ -745,15 +857,15 @@ bool tr_sizes_ok(int64_t n, int64_t m, int32_t d, int32_t dv) {
          dv >= 1 && dv <= 16384;
 }
 
-// One launch of transport_kernel<BN, MOMENT> for the value slice in p
+// One launch of transport_kernel<BN, MODE> for the value slice in p
 // (v0, dv), then the fix-up of the row blocks that were split between CTAs.
-template <int BN, bool MOMENT>
+template <int BN, int MODE>
 cudaError_t launch_shape(tr::Params& p, const TrLayout& L, const float* yp, int dev, int nsm,
                          cudaStream_t stream) {
-  using C = tr::Shape<BN, MOMENT>;
+  using C = tr::Shape<BN, MODE>;
   static std::atomic<int> attr_done[64];
   if (dev >= 64 || attr_done[dev].load(std::memory_order_acquire) == 0) {
-    const cudaError_t err = cudaFuncSetAttribute(tr::transport_kernel<BN, MOMENT>,
+    const cudaError_t err = cudaFuncSetAttribute(tr::transport_kernel<BN, MODE>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_done[dev].store(1, std::memory_order_release);
@@ -774,7 +886,7 @@ cudaError_t launch_shape(tr::Params& p, const TrLayout& L, const float* yp, int 
   const int64_t ctas = std::min<int64_t>(std::min<int64_t>(nsm, tiles), L.ctas);
   p.t_base = tiles / ctas;
   p.t_rem = tiles % ctas;
-  tr::transport_kernel<BN, MOMENT><<<static_cast<unsigned>(ctas), tr::NTHREADS, C::SMEM, stream>>>(p);
+  tr::transport_kernel<BN, MODE><<<static_cast<unsigned>(ctas), tr::NTHREADS, C::SMEM, stream>>>(p);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   tr::fixup_kernel<<<static_cast<unsigned>(L.n_rb), 256, 0, stream>>>(p);
@@ -784,7 +896,9 @@ cudaError_t launch_shape(tr::Params& p, const TrLayout& L, const float* yp, int 
 // Key-tile shape of a slice: 192-key tiles with two S / P buffers when the
 // slice has at most 128 value columns (the epilogue of one tile overlaps the
 // products of the next), else 256-key tiles with one; the moment form keeps
-// S' beside S in 128-key tiles.
+// S' beside S in 128-key tiles.  A single value column goes to the CUDA
+// cores (VECTOR, 256-key tiles, two S buffers): as a tensor product it
+// would cost as many MMA instructions per tile as 64 columns.
 cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const float* yp,
                              const float* yt, int32_t v0, int32_t dv, float* mass, bool moment,
                              cudaStream_t stream) {
@@ -810,9 +924,14 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const fl
   p.v0 = v0;
   p.dv = dv;
   p.mass = mass;
-  if (moment) return launch_shape<128, true>(p, L, yp, dev, nsm, stream);
-  if (dv <= 128) return launch_shape<192, false>(p, L, yp, dev, nsm, stream);
-  return launch_shape<256, false>(p, L, yp, dev, nsm, stream);
+  if (moment) return launch_shape<128, tr::MOMENT>(p, L, yp, dev, nsm, stream);
+  if (base.d == 1) {
+    p.dv = 1;
+    p.kval = yt;  // row 0 of the transposed values: v_j, zero past m
+    return launch_shape<256, tr::VECTOR>(p, L, yp, dev, nsm, stream);
+  }
+  if (dv <= 128) return launch_shape<192, tr::VALUES>(p, L, yp, dev, nsm, stream);
+  return launch_shape<256, tr::VALUES>(p, L, yp, dev, nsm, stream);
 }
 
 // The plan of (f, g) applied to the values V [m, dv]: out = pi V, mass =
@@ -868,6 +987,7 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   if (!moment) p.wmap = p.qmap;
   p.kbias = kb;
   p.rowterm = rt;
+  p.kval = nullptr;
   p.out = out;
   p.mass = nullptr;
   p.part_o = reinterpret_cast<float*>(w + L.po);
@@ -889,7 +1009,7 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
 // Workspace of the Hessian-vector product: one region for the plan
 // applications (run one after another), then the vectors.
 struct HvpLayout {
-  size_t apply, py, xv, rhs, w, mr, z, res, sv, pv, ap, pp, diag, mass, u, g2, mv, part, scal, total;
+  size_t apply, py, xv, rhs, w, mr, z, zb, res, sv, pv, ap, pp, diag, mass, u, g2, mv, part, scal, total;
 };
 
 HvpLayout hvp_layout(int64_t n, int64_t m, int32_t d) {
@@ -910,6 +1030,7 @@ HvpLayout hvp_layout(int64_t n, int64_t m, int32_t d) {
   H.w = take(static_cast<size_t>(n) * (d + 1) * 4);
   H.mr = take(static_cast<size_t>(m) * (d + 1) * 4);
   H.z = take(N * 4);
+  H.zb = take(N * 4);
   H.res = take(N * 4);
   H.sv = take(N * 4);
   H.pv = take(N * 4);
@@ -921,7 +1042,7 @@ HvpLayout hvp_layout(int64_t n, int64_t m, int32_t d) {
   H.g2 = take(static_cast<size_t>(n) * (d + 1) * 4);
   H.mv = take(static_cast<size_t>(n) * d * 4);
   H.part = take(tr::kDotBlocks * sizeof(double));
-  H.scal = take(4 * sizeof(double));
+  H.scal = take(8 * sizeof(double));
   H.total = o;
   return H;
 }
@@ -948,10 +1069,10 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
   const size_t ab = H.py - H.apply;
   const int64_t N = n + m;
   float *PY = F(H.py), *xv = F(H.xv), *rhs = F(H.rhs), *W = F(H.w), *Mr = F(H.mr), *z = F(H.z);
-  float *res = F(H.res), *sv = F(H.sv), *pv = F(H.pv), *Ap = F(H.ap), *Pp = F(H.pp);
+  float *zb = F(H.zb), *res = F(H.res), *sv = F(H.sv), *pv = F(H.pv), *Ap = F(H.ap), *Pp = F(H.pp);
   float *diag = F(H.diag), *mass = F(H.mass), *U = F(H.u), *G2 = F(H.g2), *MV = F(H.mv);
   double* part = reinterpret_cast<double*>(w + H.part);
-  double* scal = reinterpret_cast<double*>(w + H.scal);  // rs[2], pAp
+  double* scal = reinterpret_cast<double*>(w + H.scal);  // rs[2], pAp, rs0, z . n0, best, keep
   const unsigned bn = static_cast<unsigned>((N + 255) / 256);
   const unsigned bq = static_cast<unsigned>((n + 255) / 256);
   const unsigned bk = static_cast<unsigned>((m + 255) / 256);
@@ -970,9 +1091,11 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
     return st;
   tr::hvp_col_kernel<<<bk, 256, 0, s>>>(Y, Mr, m, d, rhs + n);
   // conjugate gradients for (df, dg)
-  tr::cg_init_kernel<<<bn, 256, 0, s>>>(rhs, log_a, log_b, n, N, diag, z, res, sv, pv);
+  tr::cg_init_kernel<<<bn, 256, 0, s>>>(rhs, log_a, log_b, n, N, diag, z, zb, res, sv, pv);
   cudaError_t e = dot(res, sv, scal + 0);
   if (e != cudaSuccess) return b4::record_cuda_error(e);
+  tr::copy_scalar_kernel<<<1, 1, 0, s>>>(scal + 0, scal + 3);
+  tr::copy_scalar_kernel<<<1, 1, 0, s>>>(scal + 0, scal + 5);
   for (int32_t k = 0; k < cg_iters; ++k) {
     double* rs = scal + (k & 1);
     double* rs_next = scal + ((k + 1) & 1);
@@ -984,12 +1107,19 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
       return st;
     tr::cg_matvec_kernel<<<bn, 256, 0, s>>>(diag, pv, Pp, N, Ap);
     if ((e = dot(pv, Ap, scal + 2)) != cudaSuccess) return b4::record_cuda_error(e);
-    tr::cg_step_kernel<<<bn, 256, 0, s>>>(rs, scal + 2, pv, Ap, diag, N, z, res, sv);
+    tr::cg_step_kernel<<<bn, 256, 0, s>>>(rs, scal + 2, scal + 3, scal + 5, pv, Ap, diag, N, z,
+                                          res, sv);
     if ((e = dot(res, sv, rs_next)) != cudaSuccess) return b4::record_cuda_error(e);
-    tr::cg_dir_kernel<<<bn, 256, 0, s>>>(rs, rs_next, sv, N, pv);
+    tr::cg_best_kernel<<<1, 1, 0, s>>>(rs_next, scal + 5, scal + 6);
+    tr::cg_keep_kernel<<<bn, 256, 0, s>>>(scal + 6, z, N, zb);
+    tr::cg_dir_kernel<<<bn, 256, 0, s>>>(rs, rs_next, scal + 3, scal + 5, sv, N, pv);
   }
+  // the best iterate, without its component along n0
+  tr::null_partial_kernel<<<tr::kDotBlocks, 256, 0, s>>>(zb, n, N, part);
+  tr::dot_final_kernel<<<1, tr::kDotBlocks, 0, s>>>(part, scal + 4);
+  tr::null_remove_kernel<<<bn, 256, 0, s>>>(scal + 4, n, N, zb);
   // pi [dg, dg y], the second moment, and the combination
-  tr::hvp_values_kernel<<<bk, 256, 0, s>>>(Y, z + n, m, d, U);
+  tr::hvp_values_kernel<<<bk, 256, 0, s>>>(Y, zb + n, m, d, U);
   if ((st = apply_impl(X, Y, f, g, log_a, log_b, U, d + 1, G2, mass, n, m, d, eps, aw, ab, s)) != B4_OK)
     return st;
   if ((st = apply_impl(X, Y, f, g, log_a, log_b, Y, d, MV, mass, n, m, d, eps, aw, ab, s, V)) !=
@@ -998,7 +1128,7 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
   const int64_t tot = n * static_cast<int64_t>(d);
   const int64_t blocks = std::min<int64_t>((tot + 255) / 256, 1 << 20);
   tr::hvp_final_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      V, PY, xv, z, G2, MV, log_a, n, d, 2.0f / eps, out);
+      V, PY, xv, zb, G2, MV, log_a, n, d, 2.0f / eps, out);
   return b4::record_cuda_error(cudaGetLastError());
 }
 

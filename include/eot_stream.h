@@ -123,12 +123,18 @@ int eot_transport(const float *X, const float *Y, const float *f, const float *g
  *     dpi_ij = pi_ij (df_i + dg_j - dC_ij) / eps,
  * where (df, dg) solve the linearised marginal conditions
  *     [[diag(a), pi], [pi^T, diag(b)]] [df; dg] = [pi dC 1; pi^T dC 1]
- * by cg_iters steps of conjugate gradients with the diagonal as
- * preconditioner.  Each step applies pi and pi^T once (two streaming passes
- * over the n x m scores); the remaining terms are plan applications
- * (pi Y, pi^T [x.v, V], pi [dg, dg y]) and one second-moment pass
- * sum_j pi_ij (v_i . y_j) y_j.  All products are one TF32 pass; the CG runs
- * in fp32 with fp64 dot products, with no host synchronisation.
+ * by at most cg_iters steps of conjugate gradients with the diagonal as
+ * preconditioner.  The two plan products of a step carry their own score
+ * rounding, so the operator is symmetric only to about 1e-3 and the
+ * residual levels off: the iteration stops, on the device, once
+ * r^T diag^-1 r is 1e-8 of its first value or has risen 1e4-fold above its
+ * smallest value, and the iterate with the smallest value is used.  Its
+ * component along (1, -1), which leaves H V unchanged, is removed.  Each step applies pi and pi^T once
+ * to one column (two streaming passes over the n x m scores); the
+ * remaining terms are plan applications (pi Y, pi^T [x.v, V],
+ * pi [dg, dg y]) and one second-moment pass sum_j pi_ij (v_i . y_j) y_j.
+ * The scores are one TF32 pass; the CG runs in fp32 with fp64 dot
+ * products, with no host synchronisation.
  * Workspace: eot_hvp_workspace_bytes(n, m, d), 256-byte aligned.  Errors as
  * for eot_update, and B4_EINVAL for cg_iters outside 0..100000. */
 size_t eot_hvp_workspace_bytes(int64_t n, int64_t m, int32_t d);
