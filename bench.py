@@ -232,9 +232,16 @@ def main():
                     help="streaming entropic OT: n = m = 65536 points, d = 64 and 512, both precisions")
     ap.add_argument("--nxn", action="store_true",
                     help="n x n kernels, n = 2..8, 1 GiB of fp32 X per n (one JSON line each)")
+    ap.add_argument("--eot-profile", choices=["update", "transport", "hvp"],
+                    help="profiling target (not a measurement): three calls of one streaming "
+                         "EOT op on seeded clouds, n = m = --eot-n points of dimension --eot-d")
+    ap.add_argument("--eot-n", type=int, default=16384)
+    ap.add_argument("--eot-d", type=int, default=64)
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.eot_profile:
+        return run_eot_profile(args)
     if args.sweep or args.mhc or args.nxn or args.eot:
         return run_extra(args)
 
@@ -558,6 +565,42 @@ def run_eot(dev):
     print(json.dumps({"eot_hvp": True, "n": nh, "m": nh, "d": 64, "eps": eps, "cg_iters": 20,
                       "ms": th, "plan_passes": 2 * 20 + 4,
                       "ms_per_plan_pass": th / (2 * 20 + 4)}), flush=True)
+
+
+def run_eot_profile(args):
+    """Three calls of one streaming EOT op, for an ncu capture of its kernel
+    (update: lse_kernel; transport: transport_kernel, one launch per 256
+    value coordinates; hvp: the plan passes of 5 CG steps)."""
+    import torch
+
+    from birkhoff_projection_gb300 import eot, workloads
+
+    dev = torch.device("cuda:0")
+    n = m = args.eot_n
+    d = args.eot_d
+    eps = workloads.EOT_EPS
+    X, Y, la, lb = workloads.eot_clouds(n, m, d, seed=0, device=dev)
+    g = torch.zeros(m, device=dev)
+    if args.eot_profile == "update":
+        ws = torch.empty(eot.workspace_bytes(n, m, d, eot.TF32), dtype=torch.uint8, device=dev)
+        calls = [lambda: eot.update(X, Y, g, lb, eps, passes=eot.TF32, workspace=ws)] * 3
+    elif args.eot_profile == "transport":
+        f = eot.update(X, Y, g, lb, eps)
+        ws = torch.empty(lib_tr_bytes(n, m, d), dtype=torch.uint8, device=dev)
+        calls = [lambda: eot.transport(X, Y, f, g, la, lb, eps, workspace=ws)] * 3
+    else:
+        f, g = eot.sinkhorn(X, Y, la, lb, eps, 20)
+        V = torch.randn(n, d, device=dev, generator=torch.Generator(device=dev).manual_seed(1))
+        ws = torch.empty(eot.lib().eot_hvp_workspace_bytes(n, m, d), dtype=torch.uint8, device=dev)
+        calls = [lambda: eot.hvp(X, Y, f, g, la, lb, V, eps, cg_iters=5, workspace=ws)] * 3
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for c in calls:
+        c()
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"eot_profile": args.eot_profile, "n": n, "m": m, "d": d, "calls": len(calls),
+                      "wall_s": time.perf_counter() - t0, "note": "profiling target, not a measurement"}),
+          flush=True)
 
 
 def ctypes_probe(b4, dev):
