@@ -95,21 +95,25 @@ struct Params {
   int32_t d, v0, dv;
   int32_t vg;            // value chunks per ring slot
   int32_t n_kt, n_kc;
-  // Tiles T = row block * n_kt + key tile, cut into one contiguous run per
-  // CTA: CTA b takes t_base tiles, one more if b < t_rem.
+  // Work of CTA b: first n_full whole row blocks b, b + ctas, ... (every
+  // CTA sweeps the same key tiles at about the same time, so they share
+  // them in L2); then the row blocks from full_rb on, whose tiles
+  // T = (row block - full_rb) * n_kt + key tile are cut into one contiguous
+  // run per CTA: t_base tiles, one more if b < t_rem.
+  int64_t n_full, full_rb;
   int64_t t_base, t_rem;
   float c1;              // 2 log2(e) / eps
   unsigned int* fault;
 };
 
-// First tile and tile count of CTA b.
+// First tile and tile count of CTA b's run of the last row blocks.
 __host__ __device__ __forceinline__ int64_t run_start(const Params& p, int64_t b) {
   return b * p.t_base + (b < p.t_rem ? b : p.t_rem);
 }
 __host__ __device__ __forceinline__ int64_t run_count(const Params& p, int64_t b) {
   return p.t_base + (b < p.t_rem ? 1 : 0);
 }
-// The CTA whose run holds tile T.
+// The CTA whose run holds tile T of the last row blocks.
 __host__ __device__ __forceinline__ int64_t run_owner(const Params& p, int64_t T) {
   const int64_t cut = p.t_rem * (p.t_base + 1);
   return T < cut ? T / (p.t_base + 1) : p.t_rem + (T - cut) / p.t_base;
@@ -169,11 +173,12 @@ __global__ void grad_kernel(const float* __restrict__ X, const float* __restrict
 // (deterministic).  One CTA per row block; blocks that one CTA covered
 // whole were written by the transport kernel and are skipped.
 __global__ void fixup_kernel(const __grid_constant__ Params p) {
-  const int64_t rb = blockIdx.x;
-  const int64_t b_lo = run_owner(p, rb * p.n_kt), b_hi = run_owner(p, rb * p.n_kt + p.n_kt - 1);
+  const int64_t rb = p.full_rb + blockIdx.x;  // a row block of the runs
+  const int64_t tr = blockIdx.x;                // its index among them
+  const int64_t b_lo = run_owner(p, tr * p.n_kt), b_hi = run_owner(p, tr * p.n_kt + p.n_kt - 1);
   if (b_lo == b_hi) return;
-  // slot 0 holds a CTA's first row block, slot 1 its last
-  auto slot = [&](int64_t b) { return b * 2 + (run_start(p, b) / p.n_kt == rb ? 0 : 1); };
+  // slot 0 holds the first row block of a CTA's run, slot 1 its last
+  auto slot = [&](int64_t b) { return b * 2 + (run_start(p, b) / p.n_kt == tr ? 0 : 1); };
   const int dv = p.dv;
   for (int e = threadIdx.x; e < BM * dv; e += blockDim.x) {
     const int row = e / dv, c = e - row * dv;
@@ -471,9 +476,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   __shared__ int abort_sh;
   volatile int* abort_flag = &abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t t0 = run_start(p, blockIdx.x);
-  const int64_t cnt = run_count(p, blockIdx.x);
   const int64_t n_kt = p.n_kt;
+  const int64_t u_run = p.n_full * n_kt;  // local index of this CTA's first run tile
+  const int64_t t0 = run_start(p, blockIdx.x);
+  const int64_t cnt = u_run + run_count(p, blockIdx.x);
+  // row block and key tile of local tile u
+  auto locate = [&](int64_t u, int64_t& rb, int64_t& kt) {
+    if (u < u_run) {
+      rb = static_cast<int64_t>(blockIdx.x) + (u / n_kt) * static_cast<int64_t>(gridDim.x);
+      kt = u % n_kt;
+    } else {
+      const int64_t T = t0 + (u - u_run);
+      rb = p.full_rb + T / n_kt;
+      kt = T % n_kt;
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSLOT; ++s) {
@@ -516,10 +533,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     // ---------------- producer ----------------
     if (lane == 0) {
       uint32_t it = 0, nb = 0;  // ring slots and bias slots filled
-      // the K chunks of S(T), after the biases of tile T (local index u)
-      auto load_s = [&](int64_t T, int64_t u) -> bool {
-        const int rb = static_cast<int>(T / n_kt);
-        const int kt = static_cast<int>(T % n_kt);
+      // the K chunks of S(u), after the biases of tile u
+      auto load_s = [&](int64_t u) -> bool {
+        int64_t rb, kt;
+        locate(u, rb, kt);
         const int bs = static_cast<int>(u % NBIAS);
         if (!wait_bar(&bias_empty[bs], (static_cast<uint32_t>(u / NBIAS) & 1u) ^ 1u, abort_flag,
                       p.fault))
@@ -534,35 +551,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
           if (!wait_bar(&slot_empty[s], ((it / NSLOT) & 1u) ^ 1u, abort_flag, p.fault)) return false;
           unsigned char* st = ring + s * SLOT;
           b4::mbar_arrive_expect_tx(&slot_full[s], SLOT);
-          b4::tma_load_2d(st, &p.qmap, &slot_full[s], kc * KC, rb * BM);
-          if (MOMENT) b4::tma_load_2d(st + A_BYTES, &p.wmap, &slot_full[s], kc * KC, rb * BM);
-          b4::tma_load_2d(st + C::NA * A_BYTES, &p.kmap, &slot_full[s], kc * KC, kt * BN);
+          const int qy = static_cast<int>(rb * BM), ky = static_cast<int>(kt * BN);
+          b4::tma_load_2d(st, &p.qmap, &slot_full[s], kc * KC, qy);
+          if (MOMENT) b4::tma_load_2d(st + A_BYTES, &p.wmap, &slot_full[s], kc * KC, qy);
+          b4::tma_load_2d(st + C::NA * A_BYTES, &p.kmap, &slot_full[s], kc * KC, ky);
         }
         return true;
       };
-      // the value chunks of P V(T), vg per slot
-      auto load_v = [&](int64_t T) -> bool {
-        const int kt = static_cast<int>(T % n_kt);
+      // the value chunks of P V(u), vg per slot
+      auto load_v = [&](int64_t u) -> bool {
+        int64_t rb, kt;
+        locate(u, rb, kt);
         for (int c = 0; c < CPT; c += vg, ++it) {
           const int s = static_cast<int>(it % NSLOT);
           if (!wait_bar(&slot_empty[s], ((it / NSLOT) & 1u) ^ 1u, abort_flag, p.fault)) return false;
           unsigned char* st = ring + s * SLOT;
           b4::mbar_arrive_expect_tx(&slot_full[s], static_cast<uint32_t>(vg) * vbytes);
           for (int g = 0; g < vg; ++g)
-            b4::tma_load_2d(st + g * vbytes, &p.vmap, &slot_full[s], kt * BN + (c + g) * KC, p.v0);
+            b4::tma_load_2d(st + g * vbytes, &p.vmap, &slot_full[s],
+                            static_cast<int>(kt * BN) + (c + g) * KC, p.v0);
         }
         return true;
       };
       bool ok = true;
       for (int64_t k = 0; k <= cnt && ok; ++k) {
         if (VEC) {
-          if (k < cnt) ok = load_s(t0 + k, k);
+          if (k < cnt) ok = load_s(k);
         } else if (NBUF == 1) {
-          if (k > 0) ok = load_v(t0 + k - 1);
-          if (ok && k < cnt) ok = load_s(t0 + k, k);
+          if (k > 0) ok = load_v(k - 1);
+          if (ok && k < cnt) ok = load_s(k);
         } else {
-          if (k < cnt) ok = load_s(t0 + k, k);
-          if (ok && k > 0) ok = load_v(t0 + k - 1);
+          if (k < cnt) ok = load_s(k);
+          if (ok && k > 0) ok = load_v(k - 1);
         }
       }
       // every issued copy lands before the CTA may exit
@@ -604,10 +624,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         mma_commit(&acc_full[buf]);
         return true;
       };
-      // O += P(T) V(T)^T with P(T) read from its TMEM buffer
-      auto issue_pv = [&](int64_t T, int64_t u) -> bool {
-        const int64_t kt = T % n_kt;
-        const bool first = kt == 0 || u == 0, last = kt == n_kt - 1 || u == cnt - 1;
+      // O += P(u) V(u)^T with P(u) read from its TMEM buffer
+      auto issue_pv = [&](int64_t u) -> bool {
+        int64_t rb, kt;
+        locate(u, rb, kt);
+        const bool first = kt == 0 || u == 0 || u == u_run, last = kt == n_kt - 1 || u == cnt - 1;
         if (first && !wait_bar(&o_empty, (seg & 1u) ^ 1u, abort_flag, p.fault)) return false;
         const int buf = static_cast<int>(u % NBUF);
         if (!wait_bar(&p_full[buf], static_cast<uint32_t>(u / NBUF) & 1u, abort_flag, p.fault))
@@ -641,11 +662,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         if (VEC) {
           if (k < cnt) ok = issue_s(k);
         } else if (NBUF == 1) {
-          if (k > 0) ok = issue_pv(t0 + k - 1, k - 1);
+          if (k > 0) ok = issue_pv(k - 1);
           if (ok && k < cnt) ok = issue_s(k);
         } else {
           if (k < cnt) ok = issue_s(k);
-          if (ok && k > 0) ok = issue_pv(t0 + k - 1, k - 1);
+          if (ok && k > 0) ok = issue_pv(k - 1);
         }
       }
       // all MMAs issued by this thread complete before TMEM is released
@@ -664,10 +685,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     float rt = 0.0f, mass = 0.0f, ov = 0.0f;  // ov: VECTOR's sum_j p_ij v_j
     bool ok = true;
     for (int64_t u = 0; u < cnt; ++u) {
-      const int64_t T = t0 + u;
-      const int64_t kt = T % n_kt;
-      if (u == 0 || kt == 0) {  // a segment begins
-        r = (T / n_kt) * BM + row;
+      int64_t rb, kt;
+      locate(u, rb, kt);
+      if (u == 0 || kt == 0 || u == u_run) {  // a segment begins
+        r = rb * BM + row;
         rt = p.rowterm[r];
         mass = 0.0f;
         ov = 0.0f;
@@ -732,7 +753,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       // or once more when it gives up, so none waits for a warp that left.
       if (!ok || kt == n_kt - 1 || u == cnt - 1) {
         const bool whole = kt0 == 0 && kt == n_kt - 1;  // the segment is the whole row block
-        const int64_t pslot = static_cast<int64_t>(blockIdx.x) * 2 + (sg == 0 ? 0 : 1);
+        // partial segments lie in the run: its first uses slot 0, its last slot 1
+        const int64_t pslot =
+            static_cast<int64_t>(blockIdx.x) * 2 + (sg == static_cast<uint32_t>(p.n_full) ? 0 : 1);
         if (ok && !VEC) {
           ok = wait_bar(&o_full, sg & 1u, abort_flag, p.fault);
           ok = __all_sync(0xffffffffu, ok);
@@ -884,12 +907,16 @@ cudaError_t launch_shape(tr::Params& p, const TrLayout& L, const float* yp, int 
   p.n_kt = static_cast<int32_t>(L.m_pad / BN);
   const int64_t tiles = L.n_rb * p.n_kt;
   const int64_t ctas = std::min<int64_t>(std::min<int64_t>(nsm, tiles), L.ctas);
-  p.t_base = tiles / ctas;
-  p.t_rem = tiles % ctas;
+  // whole waves of row blocks, one per CTA; the rest in equal runs
+  p.n_full = L.n_rb / ctas;
+  p.full_rb = p.n_full * ctas;
+  const int64_t run_tiles = (L.n_rb - p.full_rb) * p.n_kt;
+  p.t_base = run_tiles / ctas;
+  p.t_rem = run_tiles % ctas;
   tr::transport_kernel<BN, MODE><<<static_cast<unsigned>(ctas), tr::NTHREADS, C::SMEM, stream>>>(p);
   cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  tr::fixup_kernel<<<static_cast<unsigned>(L.n_rb), 256, 0, stream>>>(p);
+  if (err != cudaSuccess || L.n_rb == p.full_rb) return err;
+  tr::fixup_kernel<<<static_cast<unsigned>(L.n_rb - p.full_rb), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
