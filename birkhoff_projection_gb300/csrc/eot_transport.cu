@@ -12,6 +12,7 @@
 // cost with respect to X, 2 (r_i x_i - O_i), and the barycentric map O_i / r_i.
 // The extern "C" entries are declared and documented in eot_stream.h.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -51,8 +52,12 @@ static_assert(NEPI % 4 == 0, "whole lane quarters");
 //   VALUES  O = P V on the tensor cores (P from TMEM, V^T from shared memory);
 //   MOMENT  the same with P weighted by S' = W Y^T (see transport_kernel);
 //   VECTOR  one value column: o_i = sum_j p_ij v_j on the CUDA cores of the
-//           epilogue, which leaves the tensor pipe to S alone.
-enum Mode : int { VALUES = 0, MOMENT = 1, VECTOR = 2 };
+//           epilogue, which leaves the tensor pipe to S alone;
+//   HALF    VALUES with P and V as f16 operands (kind::f16, 16 keys per MMA
+//           instead of 8): P scaled per row by 2^15 / a_i, V by one power of
+//           two; a P entry past the f16 range sets a flag on which a VALUES
+//           launch of the same slice redoes the work.
+enum Mode : int { VALUES = 0, MOMENT = 1, VECTOR = 2, HALF = 3 };
 
 // Shapes of one kernel instance: BN keys per tile; two S / P buffers for
 // 192-key value tiles (slices of at most 128 columns: 2 x 192 + 128 TMEM
@@ -63,12 +68,15 @@ enum Mode : int { VALUES = 0, MOMENT = 1, VECTOR = 2 };
 template <int BN_, int MODE>
 struct Shape {
   static constexpr int BN = BN_;
-  static constexpr int NBUF = ((BN_ == 192 && MODE == VALUES) || MODE == VECTOR) ? 2 : 1;
+  static constexpr int NBUF =
+      ((BN_ == 192 && (MODE == VALUES || MODE == HALF)) || MODE == VECTOR) ? 2 : 1;
   static constexpr int NA = MODE == MOMENT ? 2 : 1;  // query operands per K chunk
   static constexpr int SLOT = NA * A_BYTES + BN * KC * 4;
   static constexpr int NSLOT = RING_BYTES / SLOT;
-  static constexpr int CPT = BN / KC;          // value chunks per tile
+  static constexpr int CPT = BN / KC;          // 32-key chunks per tile
   static constexpr int CPG = CPT / GROUPS;     // chunks per epilogue warp
+  static constexpr int VK = MODE == HALF ? 64 : KC;  // keys per value chunk (one 128-byte row)
+  static constexpr int VPT = BN / VK;          // value chunks per tile
   static constexpr int O_COL = MODE == MOMENT ? 2 * BN : NBUF * BN;
   static constexpr int MAX_DV = MODE == VECTOR ? 1 : TMEM_COLS - O_COL;
   static constexpr int SMEM = NSLOT * SLOT + 1024;
@@ -87,6 +95,11 @@ struct Params {
   const float* kbias;    // [nk_pad] (g_j - ||y_j||^2) log2(e)/eps + log2 b_j; -inf past nk
   const float* rowterm;  // [nq_pad] (f_i - ||x_i||^2) log2(e)/eps + log2 a_i; -inf past nq
   const float* kval;     // VECTOR: the value column [nk_pad], zero past nk
+  const float* rowterm16;  // HALF: (f_i - ||x_i||^2) log2(e)/eps + 15: exponent of p_ij 2^15 / a_i
+  const float* rowscale;   // HALF: a_i 2^-15, which takes a scaled p back to p
+  const float* vscale;   // HALF: {s_V, 1 / s_V}, the power of two V was scaled by
+  unsigned int* guard;   // HALF sets it when a scaled p leaves the f16 range
+  int32_t guard_mode;    // 1: run only if *guard is set (the VALUES redo)
   float* out;            // [nq, d]: columns v0 .. v0 + dv - 1 (those below d) written
   float* mass;           // [nq] row masses, or NULL
   float* part_o;         // [ctas][2][128][dv]: O of row blocks this CTA covers in part
@@ -125,6 +138,11 @@ __device__ __forceinline__ uint32_t idesc_tf32_n(int n) {
   return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(BM >> 4) << 24);
 }
+// The same for kind::f16 with A and B both f16 (format 0), fp32 accumulation.
+__device__ __forceinline__ uint32_t idesc_f16_n(int n) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
 
 // Transposed packing of the key points for the value operand:
 // dst[k][j] = tf32(src[j][k]) for j < rows, k < d, zero elsewhere in
@@ -158,6 +176,77 @@ __global__ void rowterm_kernel(const float* __restrict__ f, const float* __restr
   rt[i] = i < nq ? fmaf(f[i] - qnorm[i], scale, log_a[i] * b4::LOG2E) : -INFINITY;
 }
 
+// HALF mode: rt16_i = (f_i - ||x_i||^2) log2(e)/eps + 15 and rsc_i =
+// a_i 2^-15, so that 2^(S c1 + bias_j + rt16_i) = p_ij 2^15 / a_i; -inf and 0
+// for the padding rows.
+__global__ void rowterm16_kernel(const float* __restrict__ f, const float* __restrict__ log_a,
+                                 const float* __restrict__ qnorm, int64_t nq, int64_t nq_pad,
+                                 float scale, float* __restrict__ rt16, float* __restrict__ rsc) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= nq_pad) return;
+  rt16[i] = i < nq ? fmaf(f[i] - qnorm[i], scale, 15.0f) : -INFINITY;
+  rsc[i] = i < nq ? exp2f(fmaf(log_a[i], b4::LOG2E, -15.0f)) : 0.0f;
+}
+
+// max |V| over the whole array, as the bits of a non-negative float
+// (ordered like the values), into *vmax (zeroed by the caller).
+__global__ void vmax_kernel(const float* __restrict__ V, int64_t total, unsigned int* __restrict__ vmax) {
+  __shared__ unsigned int sh;
+  if (threadIdx.x == 0) sh = 0u;
+  __syncthreads();
+  unsigned int m = 0u;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float a = fabsf(V[e]);
+    const unsigned int b = a != a ? 0x7f800000u : __float_as_uint(a);  // NaN counts as inf
+    m = b > m ? b : m;
+  }
+  atomicMax(&sh, m);
+  __syncthreads();
+  if (threadIdx.x == 0) atomicMax(vmax, sh);
+}
+
+// The power of two s_V that puts max |V| in [2^14, 2^15) (1 for V = 0):
+// vscale = {s_V, 1 / s_V}, both exact.  A non-finite V sets the guard, so
+// the f16 pass is redone in TF32 (where it gives what TF32 gives).
+__global__ void vscale_kernel(const unsigned int* __restrict__ vmax, float* __restrict__ vscale,
+                              unsigned int* __restrict__ guard) {
+  const float m = __uint_as_float(*vmax);
+  int e = 0;
+  if (!(m <= 3.0e38f)) {
+    *guard = 1u;
+  } else if (m > 0.0f) {
+    frexpf(m, &e);  // m in [2^(e-1), 2^e)
+    e = e < -100 ? -100 : e;
+  } else {
+    e = 15;
+  }
+  vscale[0] = ldexpf(1.0f, 15 - e);
+  vscale[1] = ldexpf(1.0f, e - 15);
+}
+
+// f16 transposed packing of s_V V (the HALF value operand):
+// dst[k][j] = f16(s_V src[j][k]), zero padded to [d_pad, rows_pad].
+__global__ void pack_transposed_f16_kernel(const float* __restrict__ src, int64_t rows, int32_t d,
+                                           int64_t rows_pad, int32_t d_pad,
+                                           const float* __restrict__ vscale, __half* __restrict__ dst) {
+  __shared__ float t[32][33];
+  const float sv = vscale[0];
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int k0 = blockIdx.y * 32;
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int64_t j = j0 + r;
+    const int k = k0 + threadIdx.x;
+    t[r][threadIdx.x] = (j < rows && k < d) ? src[j * d + k] * sv : 0.0f;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int k = k0 + r;
+    const int64_t j = j0 + threadIdx.x;
+    if (k < d_pad && j < rows_pad) dst[static_cast<int64_t>(k) * rows_pad + j] = __float2half_rn(t[threadIdx.x][r]);
+  }
+}
+
 // grad_ik = 2 (r_i x_ik - (pi Y)_ik).
 __global__ void grad_kernel(const float* __restrict__ X, const float* __restrict__ PY,
                             const float* __restrict__ mass, int64_t n, int32_t d,
@@ -173,6 +262,7 @@ __global__ void grad_kernel(const float* __restrict__ X, const float* __restrict
 // (deterministic).  One CTA per row block; blocks that one CTA covered
 // whole were written by the transport kernel and are skipped.
 __global__ void fixup_kernel(const __grid_constant__ Params p) {
+  if (p.guard_mode != 0 && *reinterpret_cast<volatile unsigned int*>(p.guard) == 0u) return;
   const int64_t rb = p.full_rb + blockIdx.x;  // a row block of the runs
   const int64_t tr = blockIdx.x;                // its index among them
   const int64_t b_lo = run_owner(p, tr * p.n_kt), b_hi = run_owner(p, tr * p.n_kt + p.n_kt - 1);
@@ -449,11 +539,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   using C = Shape<BN_, MODE>;
   constexpr bool MOMENT = MODE == tr::MOMENT;
   constexpr bool VEC = MODE == VECTOR;
+  constexpr bool H16 = MODE == HALF;
+  constexpr int VK = C::VK;
+  constexpr int VPT = C::VPT;
+  // the VALUES redo of a HALF launch runs only if that launch overflowed
+  if (p.guard_mode != 0 && *reinterpret_cast<volatile unsigned int*>(p.guard) == 0u) return;
   constexpr int BN = C::BN;
   constexpr int NBUF = C::NBUF;
   constexpr int SLOT = C::SLOT;
   constexpr int NSLOT = C::NSLOT;
-  constexpr int CPT = C::CPT;
   constexpr int CPG = C::CPG;
   constexpr uint32_t O_COL = C::O_COL;
   extern __shared__ unsigned char smem_raw[];
@@ -480,15 +574,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   const int64_t u_run = p.n_full * n_kt;  // local index of this CTA's first run tile
   const int64_t t0 = run_start(p, blockIdx.x);
   const int64_t cnt = u_run + run_count(p, blockIdx.x);
-  // row block and key tile of local tile u
-  auto locate = [&](int64_t u, int64_t& rb, int64_t& kt) {
-    if (u < u_run) {
-      rb = static_cast<int64_t>(blockIdx.x) + (u / n_kt) * static_cast<int64_t>(gridDim.x);
-      kt = u % n_kt;
-    } else {
-      const int64_t T = t0 + (u - u_run);
-      rb = p.full_rb + T / n_kt;
-      kt = T % n_kt;
+  // Row block and key tile of this CTA's tiles, in order: each role walks
+  // them with a cursor (a division only where the run begins, not per tile).
+  struct Cursor {
+    int64_t u, rb, kt;
+  };
+  auto run_begin = [&](Cursor& c) {
+    c.rb = p.full_rb + t0 / n_kt;
+    c.kt = t0 % n_kt;
+  };
+  auto cursor0 = [&]() {
+    Cursor c{0, static_cast<int64_t>(blockIdx.x), 0};
+    if (u_run == 0) run_begin(c);
+    return c;
+  };
+  auto advance = [&](Cursor& c) {
+    ++c.u;
+    if (c.u == u_run) {
+      run_begin(c);
+    } else if (++c.kt == n_kt) {
+      c.kt = 0;
+      c.rb += c.u < u_run ? static_cast<int64_t>(gridDim.x) : 1;
     }
   };
 
@@ -533,10 +639,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     // ---------------- producer ----------------
     if (lane == 0) {
       uint32_t it = 0, nb = 0;  // ring slots and bias slots filled
+      Cursor cs = cursor0(), cv = cursor0();  // the tiles of S loads and of value loads
       // the K chunks of S(u), after the biases of tile u
       auto load_s = [&](int64_t u) -> bool {
-        int64_t rb, kt;
-        locate(u, rb, kt);
+        const int64_t rb = cs.rb, kt = cs.kt;
+        advance(cs);
         const int bs = static_cast<int>(u % NBIAS);
         if (!wait_bar(&bias_empty[bs], (static_cast<uint32_t>(u / NBIAS) & 1u) ^ 1u, abort_flag,
                       p.fault))
@@ -558,18 +665,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         }
         return true;
       };
-      // the value chunks of P V(u), vg per slot
-      auto load_v = [&](int64_t u) -> bool {
-        int64_t rb, kt;
-        locate(u, rb, kt);
-        for (int c = 0; c < CPT; c += vg, ++it) {
+      // the value chunks of P V(u), vg per slot (u in order)
+      auto load_v = [&](int64_t) -> bool {
+        const int64_t kt = cv.kt;
+        advance(cv);
+        for (int c = 0; c < VPT; c += vg, ++it) {
           const int s = static_cast<int>(it % NSLOT);
           if (!wait_bar(&slot_empty[s], ((it / NSLOT) & 1u) ^ 1u, abort_flag, p.fault)) return false;
           unsigned char* st = ring + s * SLOT;
           b4::mbar_arrive_expect_tx(&slot_full[s], static_cast<uint32_t>(vg) * vbytes);
           for (int g = 0; g < vg; ++g)
             b4::tma_load_2d(st + g * vbytes, &p.vmap, &slot_full[s],
-                            static_cast<int>(kt * BN) + (c + g) * KC, p.v0);
+                            static_cast<int>(kt * BN) + (c + g) * VK, p.v0);
         }
         return true;
       };
@@ -595,7 +702,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t id_s = idesc_tf32_n(BN), id_o = idesc_tf32_n(p.dv);
+      const uint32_t id_s = idesc_tf32_n(BN);
+      const uint32_t id_o = H16 ? idesc_f16_n(p.dv) : idesc_tf32_n(p.dv);
       uint32_t it = 0;   // ring slots consumed
       uint32_t seg = 0;  // segments (runs of one row block) begun
       // S(T) = Q K^T into buffer u % NBUF, once that buffer's P has been used
@@ -624,28 +732,42 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         mma_commit(&acc_full[buf]);
         return true;
       };
-      // O += P(u) V(u)^T with P(u) read from its TMEM buffer
+      // O += P(u) V(u)^T with P(u) read from its TMEM buffer (u in order)
+      Cursor cp = cursor0();
       auto issue_pv = [&](int64_t u) -> bool {
-        int64_t rb, kt;
-        locate(u, rb, kt);
+        const int64_t kt = cp.kt;
+        advance(cp);
         const bool first = kt == 0 || u == 0 || u == u_run, last = kt == n_kt - 1 || u == cnt - 1;
         if (first && !wait_bar(&o_empty, (seg & 1u) ^ 1u, abort_flag, p.fault)) return false;
         const int buf = static_cast<int>(u % NBUF);
         if (!wait_bar(&p_full[buf], static_cast<uint32_t>(u / NBUF) & 1u, abort_flag, p.fault))
           return false;
         tc_fence_after();
-        for (int c = 0; c < CPT; c += vg, ++it) {
+        for (int c = 0; c < VPT; c += vg, ++it) {
           const int s = static_cast<int>(it % NSLOT);
           if (!wait_bar(&slot_full[s], (it / NSLOT) & 1u, abort_flag, p.fault)) return false;
           tc_fence_after();
           for (int g = 0; g < vg; ++g) {
-            const uint32_t pa = tmem + static_cast<uint32_t>(buf * BN + (c + g) * KC);
             const uint64_t dvd = desc_sw128_kmajor(b4::smem_addr(ring + s * SLOT + g * vbytes));
+            if (H16) {
+              // 16 keys per MMA; P of key k sits in its epilogue group's
+              // columns, two keys per column
 #pragma unroll
-            for (int kk = 0; kk < KC / KSTEP; ++kk) {
-              const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
-              mma_tf32_ts(tmem + O_COL, pa + static_cast<uint32_t>(kk * KSTEP), dvd + adv, id_o,
-                          !(first && c + g == 0 && kk == 0));
+              for (int kk = 0; kk < 4; ++kk) {
+                const int k0 = (c + g) * 64 + kk * 16;
+                const int gk = (k0 / (CPG * KC)) * CPG * KC;  // first key of its group
+                const uint32_t pa = tmem + static_cast<uint32_t>(buf * BN + gk + (k0 - gk) / 2);
+                mma_f16_ts(tmem + O_COL, pa, dvd + static_cast<uint64_t>(kk * 2), id_o,
+                           !(first && c + g == 0 && kk == 0));
+              }
+            } else {
+              const uint32_t pa = tmem + static_cast<uint32_t>(buf * BN + (c + g) * KC);
+#pragma unroll
+              for (int kk = 0; kk < KC / KSTEP; ++kk) {
+                const uint64_t adv = static_cast<uint64_t>(kk * KSTEP * 4 / 16);
+                mma_tf32_ts(tmem + O_COL, pa + static_cast<uint32_t>(kk * KSTEP), dvd + adv, id_o,
+                            !(first && c + g == 0 && kk == 0));
+              }
             }
           }
           mma_commit(&slot_empty[s]);
@@ -683,13 +805,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     uint32_t sg = 0;  // segments finished
     int64_t r = 0, kt0 = 0;
     float rt = 0.0f, mass = 0.0f, ov = 0.0f;  // ov: VECTOR's sum_j p_ij v_j
+    float rsc = 1.0f;                         // HALF: a_i 2^-15 (scaled p -> p)
     bool ok = true;
-    for (int64_t u = 0; u < cnt; ++u) {
-      int64_t rb, kt;
-      locate(u, rb, kt);
+    Cursor ce = cursor0();
+    for (int64_t u = 0; u < cnt; ++u, advance(ce)) {
+      const int64_t rb = ce.rb, kt = ce.kt;
       if (u == 0 || kt == 0 || u == u_run) {  // a segment begins
         r = rb * BM + row;
-        rt = p.rowterm[r];
+        rt = H16 ? p.rowterm16[r] : p.rowterm[r];
+        if (H16) rsc = p.rowscale[r];
         mass = 0.0f;
         ov = 0.0f;
         kt0 = kt;
@@ -706,12 +830,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(buf * BN + grp * CPG * KC);
         const float4* kb = reinterpret_cast<const float4*>(&bias_sm[bs][grp * CPG * KC]);
         uint32_t v[32], w[32];
+        bool big = false;  // HALF: a chunk of scaled p reached the f16 range
         tmem_ld32(taddr, v);
         tmem_wait32(v);
 #pragma unroll
         for (int ch = 0; ch < CPG; ++ch) {
           if (ch + 1 < CPG) tmem_ld32(taddr + static_cast<uint32_t>((ch + 1) * KC), w);
-          mass += p_chunk(v, kb + ch * 8, p.c1, rt);
+          const float csum = p_chunk(v, kb + ch * 8, p.c1, rt);
+          mass += csum;
+          if (H16) {  // P as f16 pairs over the first half of this group's S columns
+            big = big || !(csum < 65504.0f);
+            uint32_t h[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const __half2 x = __floats2half2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+              h[i] = *reinterpret_cast<const uint32_t*>(&x);
+            }
+            tmem_st16(tmem + lane_base + static_cast<uint32_t>(buf * BN + grp * CPG * KC + ch * 16), h);
+          }
           if (VEC) {  // the value column on the CUDA cores; S is not written back
             const float4* vv = reinterpret_cast<const float4*>(&val_sm[bs][(grp * CPG + ch) * KC]);
             float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
@@ -734,13 +870,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
             for (int i = 0; i < 32; ++i)
               v[i] = __float_as_uint(__uint_as_float(v[i]) * __uint_as_float(sp[i]));
           }
-          if (!VEC) tmem_st32(taddr + static_cast<uint32_t>(ch * KC), v);
+          if (!VEC && !H16) tmem_st32(taddr + static_cast<uint32_t>(ch * KC), v);
           if (ch + 1 < CPG) {
             tmem_wait32(w);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = w[i];
           }
         }
+        if (H16 && __any_sync(0xffffffffu, big) && lane == 0) atomicOr(p.guard, 1u);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -766,6 +903,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
             uint32_t o[32];
             tmem_ld32(tmem + lane_base + O_COL + static_cast<uint32_t>(c * KC), o);
             tmem_wait32(o);
+            if (H16) {  // undo the scales of p (a_i 2^-15) and of V (1 / s_V)
+              const float sc = rsc * p.vscale[1];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * sc);
+            }
             if (whole) {
               if (r < p.nq) {
                 float* orow = p.out + r * p.d;
@@ -787,6 +929,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
           if (lane == 0) mbar_arrive(&o_empty);
         }
         // row masses (and VECTOR's o_i): the key groups of a row
+        if (H16) mass *= rsc;
         if (grp > 0) {
           mass_sh[grp - 1][row] = mass;
           if (VEC) vec_sh[grp - 1][row] = ov;
@@ -836,8 +979,10 @@ namespace {
 struct TrLayout {
   int64_t n_pad, m_pad, n_rb, ctas;
   int32_t d_pad, v_pad;
-  // byte offsets (yt: the values, transposed; po, pm: partial O and masses)
-  size_t x, y, yt, xn, yn, kb, rt, wq, wn, po, pm, total;
+  // byte offsets (yt: the values, transposed; po, pm: partial O and masses;
+  // yh, rt16, rsc, misc: the f16 values, scaled row terms, row scales and
+  // {max |V|, guard, s_V, 1 / s_V} of the HALF mode)
+  size_t x, y, yt, xn, yn, kb, rt, wq, wn, po, pm, yh, rt16, rsc, misc, total;
 };
 
 // moment: also room for the packed query directions (wq) and their norms
@@ -871,6 +1016,10 @@ TrLayout tr_layout(int64_t n, int64_t m, int32_t d, int32_t dv, bool moment = fa
   }
   L.po = take(static_cast<size_t>(L.ctas) * 2 * BM * dvs * 4);
   L.pm = take(static_cast<size_t>(L.ctas) * 2 * BM * 4);
+  L.yh = take(static_cast<size_t>(L.m_pad) * L.v_pad * 2);
+  L.rt16 = take(static_cast<size_t>(L.n_pad) * 4);
+  L.rsc = take(static_cast<size_t>(L.n_pad) * 4);
+  L.misc = take(64);
   L.total = o;
   return L;
 }
@@ -896,11 +1045,11 @@ cudaError_t launch_shape(tr::Params& p, const TrLayout& L, const float* yp, int 
   if (p.dv > C::MAX_DV || !encode_rows128(&p.kmap, yp, L.m_pad, L.d_pad, BN))
     return cudaErrorInvalidValue;
   // value chunks per ring slot: the largest divisor of the chunks per tile
-  // that fits
-  const int vbytes = p.dv * KC * 4;
+  // that fits (a chunk is one 128-byte row per value coordinate)
+  const int vbytes = p.dv * 128;
   p.vg = 1;
-  for (int g = C::CPT; g >= 1; --g)
-    if (C::CPT % g == 0 && g * vbytes <= C::SLOT) {
+  for (int g = C::VPT; g >= 1; --g)
+    if (C::VPT % g == 0 && g * vbytes <= C::SLOT) {
       p.vg = g;
       break;
     }
@@ -926,39 +1075,53 @@ cudaError_t launch_shape(tr::Params& p, const TrLayout& L, const float* yp, int 
 // S' beside S in 128-key tiles.  A single value column goes to the CUDA
 // cores (VECTOR, 256-key tiles, two S buffers): as a tensor product it
 // would cost as many MMA instructions per tile as 64 columns.
+// Tensor map of the value operand: rows v0 .. v0 + dv - 1 of the transposed
+// values [v_pad, m_pad] (fp32, or f16 for the HALF mode), boxes of one
+// 128-byte row of keys per value coordinate.
+bool encode_values(CUtensorMap* map, const void* base, const TrLayout& L, int32_t dv, bool half) {
+  b4::EncodeTiledFn fn = b4::encode_fn();
+  if (fn == nullptr) return false;
+  const int esize = half ? 2 : 4;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.m_pad), static_cast<cuuint64_t>(L.v_pad)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.m_pad) * esize};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(dv)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, half ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const float* yp,
-                             const float* yt, int32_t v0, int32_t dv, float* mass, bool moment,
-                             cudaStream_t stream) {
+                             const float* yt, const void* yh, int32_t v0, int32_t dv, float* mass,
+                             bool moment, cudaStream_t stream) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   const int nsm = b4::sm_count(dev);
   if (nsm <= 0) return cudaErrorInvalidDevice;
   tr::Params p = base;
-  // value operand: rows v0 .. v0 + dv - 1 of the transposed key points
-  {
-    b4::EncodeTiledFn fn = b4::encode_fn();
-    if (fn == nullptr) return cudaErrorInvalidValue;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.m_pad), static_cast<cuuint64_t>(L.v_pad)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.m_pad) * 4};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(KC), static_cast<cuuint32_t>(dv)};
-    const cuuint32_t estr[2] = {1, 1};
-    if (fn(&p.vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(yt), dims, strides, box,
-           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (!encode_values(&p.vmap, yt, L, dv, false)) return cudaErrorInvalidValue;
   p.v0 = v0;
   p.dv = dv;
   p.mass = mass;
+  p.guard_mode = 0;
   if (moment) return launch_shape<128, tr::MOMENT>(p, L, yp, dev, nsm, stream);
   if (base.d == 1) {
     p.dv = 1;
     p.kval = yt;  // row 0 of the transposed values: v_j, zero past m
     return launch_shape<256, tr::VECTOR>(p, L, yp, dev, nsm, stream);
   }
-  if (dv <= 128) return launch_shape<192, tr::VALUES>(p, L, yp, dev, nsm, stream);
-  return launch_shape<256, tr::VALUES>(p, L, yp, dev, nsm, stream);
+  // f16 operands for P V, then the TF32 redo that runs only if they overflowed
+  tr::Params h = p;
+  if (!encode_values(&h.vmap, yh, L, dv, true)) return cudaErrorInvalidValue;
+  p.guard_mode = 1;
+  if (dv <= 128) {
+    err = launch_shape<192, tr::HALF>(h, L, yp, dev, nsm, stream);
+    return err != cudaSuccess ? err : launch_shape<192, tr::VALUES>(p, L, yp, dev, nsm, stream);
+  }
+  err = launch_shape<256, tr::HALF>(h, L, yp, dev, nsm, stream);
+  return err != cudaSuccess ? err : launch_shape<256, tr::VALUES>(p, L, yp, dev, nsm, stream);
 }
 
 // The plan of (f, g) applied to the values V [m, dv]: out = pi V, mass =
@@ -1006,6 +1169,27 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
         f, log_a, xn, n, L.n_pad, static_cast<float>(1.4426950408889634 / eps), rt);
     e = cudaGetLastError();
   }
+  // HALF operands (several value columns, not the moment form): scaled row
+  // terms, the V scale and the f16 values; the guard starts clear
+  const bool half = !moment && dv > 1;
+  unsigned int* misc = reinterpret_cast<unsigned int*>(w + L.misc);  // vmax, guard, s_V, 1/s_V
+  float* vscale = reinterpret_cast<float*>(misc + 2);
+  if (e == cudaSuccess && half) {
+    e = cudaMemsetAsync(misc, 0, 2 * sizeof(unsigned int), s);
+    if (e == cudaSuccess) {
+      tr::rowterm16_kernel<<<static_cast<unsigned>((L.n_pad + 255) / 256), 256, 0, s>>>(
+          f, log_a, xn, n, L.n_pad, static_cast<float>(1.4426950408889634 / eps),
+          reinterpret_cast<float*>(w + L.rt16), reinterpret_cast<float*>(w + L.rsc));
+      const int64_t total = m * static_cast<int64_t>(dv);
+      const unsigned vb = static_cast<unsigned>(std::min<int64_t>((total + 255) / 256, 1024));
+      tr::vmax_kernel<<<vb, 256, 0, s>>>(V, total, misc);
+      tr::vscale_kernel<<<1, 1, 0, s>>>(misc, vscale, misc + 1);
+      const dim3 grid(static_cast<unsigned>(L.m_pad / 32), static_cast<unsigned>(L.v_pad / 32));
+      tr::pack_transposed_f16_kernel<<<grid, dim3(32, 8), 0, s>>>(
+          V, m, dv, L.m_pad, L.v_pad, vscale, reinterpret_cast<__half*>(w + L.yh));
+      e = cudaGetLastError();
+    }
+  }
   if (e != cudaSuccess) return b4::record_cuda_error(e);
   tr::Params p;
   if (!encode_rows128(&p.qmap, xp, L.n_pad, L.d_pad, BM) ||
@@ -1015,6 +1199,11 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   p.kbias = kb;
   p.rowterm = rt;
   p.kval = nullptr;
+  p.rowterm16 = reinterpret_cast<float*>(w + L.rt16);
+  p.rowscale = reinterpret_cast<float*>(w + L.rsc);
+  p.vscale = vscale;
+  p.guard = misc + 1;
+  p.guard_mode = 0;
   p.out = out;
   p.mass = nullptr;
   p.part_o = reinterpret_cast<float*>(w + L.po);
@@ -1028,7 +1217,7 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   // writes the row masses
   for (int32_t v0 = 0; v0 < L.v_pad && e == cudaSuccess; v0 += tr::DV) {
     const int32_t w_slice = std::min<int32_t>(tr::DV, L.v_pad - v0);
-    e = launch_transport(p, L, yp, vt, v0, w_slice, v0 == 0 ? mass : nullptr, moment, s);
+    e = launch_transport(p, L, yp, vt, w + L.yh, v0, w_slice, v0 == 0 ? mass : nullptr, moment, s);
   }
   return b4::record_cuda_error(e);
 }

@@ -255,6 +255,41 @@ def test_apply_plan_parity(n, m, d, dv):
         assert out.shape == (n, 1)
 
 
+def _apply_bound(X, Y, f, g, log_a, log_b, V, eps):
+    """Element bound of pi V from one TF32 score pass and 2^-10 + 2^-11
+    operand rounding in the second product (what the f16 form also
+    satisfies: 2^-11 for P and for the scaled V), fp32 accumulation."""
+    args = (np64(X), np64(Y), np64(f), np64(g), np64(log_a), np64(log_b), eps)
+    fr = np.abs(np64(f)) + eps * np.abs(np64(log_a))
+    t = row_bound(np64(X), np64(Y), np64(g), np64(log_b), fr, eps, eot.TF32) / 2.0
+    rel = np.expm1(t / eps + 2.0 ** -20)
+    P = oeot.plan64(*args)
+    m_pad = -(-Y.shape[0] // 256) * 256
+    return 2.0 * (rel + 2.0 ** -10 + 2.0 ** -11 + m_pad * 2.0 ** -23)[:, None] * (P @ np.abs(np64(V)))
+
+
+@pytest.mark.parametrize("vmag", [1e6, 1e-6])
+def test_apply_plan_f16_overflow_redo_and_value_scale(vmag):
+    """The f16 second product scales P by 2^15 / a_i and V by a power of
+    two.  Potentials shifted by 4 eps make every row of pi sum to e^4 a_i,
+    past that range: the TF32 redo must take over, within the same bound.
+    Values of magnitude 1e6 and 1e-6 exercise the V scale both ways."""
+    n, m, d, dv, eps = 400, 500, 8, 40, 0.1
+    X, Y, log_a, log_b = workloads.eot_clouds(n, m, d, seed=31, device=DEV, random_weights=True)
+    f64, g64 = oeot.sinkhorn64(np64(X), np64(Y), np64(log_a), np64(log_b), eps, 30)
+    V = torch.randn(m, dv, generator=torch.Generator().manual_seed(7)).to(DEV) * vmag
+    for shift in (0.0, 4.0 * eps):
+        f = torch.tensor(f64 + shift, dtype=torch.float32, device=DEV)
+        g = torch.tensor(g64, dtype=torch.float32, device=DEV)
+        out, mass = eot.apply_plan(X, Y, f, g, log_a, log_b, V, eps)
+        ref, mr = oeot.apply_plan64(np64(X), np64(Y), np64(f), np64(g), np64(log_a), np64(log_b),
+                                    eps, np64(V))
+        assert np.all(np.isfinite(np64(out)))
+        assert np.all(np.abs(np64(out) - ref) <= _apply_bound(X, Y, f, g, log_a, log_b, V, eps))
+        if shift > 0:
+            assert mr.sum() > 50 * np.exp(np64(log_a)).sum()  # rows of pi well past a_i
+
+
 def test_sinkhorn_iterations_capture_into_a_cuda_graph():
     """After one warm-up call (per-device set-up), eot_sinkhorn enqueues only
     kernels: a CUDA graph of 3 iterations, replayed twice, gives exactly
