@@ -259,28 +259,37 @@ __global__ void grad_kernel(const float* __restrict__ X, const float* __restrict
 
 // Row blocks whose key tiles were split between CTAs: the sum of the
 // partial O (and row masses) those CTAs left in their slots, in CTA order
-// (deterministic).  One CTA per row block; blocks that one CTA covered
-// whole were written by the transport kernel and are skipped.
+// (deterministic).  Grid: x = row block of the runs, y = 1024-element part
+// of its 128 x dv partial O (y = 0 also sums the masses); blocks that one
+// CTA covered whole were written by the transport kernel and are skipped.
+constexpr int kFixupElems = 1024;
 __global__ void fixup_kernel(const __grid_constant__ Params p) {
   if (p.guard_mode != 0 && *reinterpret_cast<volatile unsigned int*>(p.guard) == 0u) return;
+  __shared__ int64_t base[MAX_CTAS];          // first partial row of each contributing CTA
   const int64_t rb = p.full_rb + blockIdx.x;  // a row block of the runs
   const int64_t tr = blockIdx.x;                // its index among them
   const int64_t b_lo = run_owner(p, tr * p.n_kt), b_hi = run_owner(p, tr * p.n_kt + p.n_kt - 1);
   if (b_lo == b_hi) return;
+  const int nb = static_cast<int>(b_hi - b_lo + 1);  // at most the CTA count
   // slot 0 holds the first row block of a CTA's run, slot 1 its last
-  auto slot = [&](int64_t b) { return b * 2 + (run_start(p, b) / p.n_kt == tr ? 0 : 1); };
+  for (int k = threadIdx.x; k < nb; k += blockDim.x) {
+    const int64_t b = b_lo + k;
+    base[k] = (b * 2 + (run_start(p, b) / p.n_kt == tr ? 0 : 1)) * BM;
+  }
+  __syncthreads();
   const int dv = p.dv;
-  for (int e = threadIdx.x; e < BM * dv; e += blockDim.x) {
+  const int e1 = min(BM * dv, static_cast<int>(blockIdx.y + 1) * kFixupElems);
+  for (int e = blockIdx.y * kFixupElems + threadIdx.x; e < e1; e += blockDim.x) {
     const int row = e / dv, c = e - row * dv;
     float acc = 0.0f;
-    for (int64_t b = b_lo; b <= b_hi; ++b) acc += p.part_o[(slot(b) * BM + row) * dv + c];
+    for (int k = 0; k < nb; ++k) acc += p.part_o[(base[k] + row) * dv + c];
     const int64_t r = rb * BM + row;
     if (r < p.nq && p.v0 + c < p.d) p.out[r * p.d + p.v0 + c] = acc;
   }
-  if (p.mass != nullptr) {
+  if (p.mass != nullptr && blockIdx.y == 0) {
     for (int row = threadIdx.x; row < BM; row += blockDim.x) {
       float acc = 0.0f;
-      for (int64_t b = b_lo; b <= b_hi; ++b) acc += p.part_mass[slot(b) * BM + row];
+      for (int k = 0; k < nb; ++k) acc += p.part_mass[base[k] + row];
       const int64_t r = rb * BM + row;
       if (r < p.nq) p.mass[r] = acc;
     }
@@ -1065,7 +1074,9 @@ cudaError_t launch_shape(tr::Params& p, const TrLayout& L, const float* yp, int 
   tr::transport_kernel<BN, MODE><<<static_cast<unsigned>(ctas), tr::NTHREADS, C::SMEM, stream>>>(p);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || L.n_rb == p.full_rb) return err;
-  tr::fixup_kernel<<<static_cast<unsigned>(L.n_rb - p.full_rb), 256, 0, stream>>>(p);
+  const dim3 fgrid(static_cast<unsigned>(L.n_rb - p.full_rb),
+                   static_cast<unsigned>((BM * p.dv + tr::kFixupElems - 1) / tr::kFixupElems));
+  tr::fixup_kernel<<<fgrid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
