@@ -1089,11 +1089,12 @@ cudaError_t launch_shape(tr::Params& p, const TrLayout& L, const float* yp, int 
 // Tensor map of the value operand: rows v0 .. v0 + dv - 1 of the transposed
 // values [v_pad, m_pad] (fp32, or f16 for the HALF mode), boxes of one
 // 128-byte row of keys per value coordinate.
-bool encode_values(CUtensorMap* map, const void* base, const TrLayout& L, int32_t dv, bool half) {
+bool encode_values(CUtensorMap* map, const void* base, const TrLayout& L, int32_t v_pad,
+                   int32_t dv, bool half) {
   b4::EncodeTiledFn fn = b4::encode_fn();
   if (fn == nullptr) return false;
   const int esize = half ? 2 : 4;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.m_pad), static_cast<cuuint64_t>(L.v_pad)};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.m_pad), static_cast<cuuint64_t>(v_pad)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.m_pad) * esize};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(dv)};
   const cuuint32_t estr[2] = {1, 1};
@@ -1103,16 +1104,16 @@ bool encode_values(CUtensorMap* map, const void* base, const TrLayout& L, int32_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const float* yp,
-                             const float* yt, const void* yh, int32_t v0, int32_t dv, float* mass,
-                             bool moment, cudaStream_t stream) {
+cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, int32_t v_pad,
+                             const float* yp, const float* yt, const void* yh, int32_t v0,
+                             int32_t dv, float* mass, bool moment, cudaStream_t stream) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   const int nsm = b4::sm_count(dev);
   if (nsm <= 0) return cudaErrorInvalidDevice;
   tr::Params p = base;
-  if (!encode_values(&p.vmap, yt, L, dv, false)) return cudaErrorInvalidValue;
+  if (!encode_values(&p.vmap, yt, L, v_pad, dv, false)) return cudaErrorInvalidValue;
   p.v0 = v0;
   p.dv = dv;
   p.mass = mass;
@@ -1125,7 +1126,7 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const fl
   }
   // f16 operands for P V, then the TF32 redo that runs only if they overflowed
   tr::Params h = p;
-  if (!encode_values(&h.vmap, yh, L, dv, true)) return cudaErrorInvalidValue;
+  if (!encode_values(&h.vmap, yh, L, v_pad, dv, true)) return cudaErrorInvalidValue;
   p.guard_mode = 1;
   if (dv <= 128) {
     err = launch_shape<192, tr::HALF>(h, L, yp, dev, nsm, stream);
@@ -1133,6 +1134,119 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, const fl
   }
   err = launch_shape<256, tr::HALF>(h, L, yp, dev, nsm, stream);
   return err != cudaSuccess ? err : launch_shape<256, tr::VALUES>(p, L, yp, dev, nsm, stream);
+}
+
+// The plan of given potentials between queries Q and keys K, prepared once
+// (packed points, key biases, row terms, the query tensor map) and then
+// applied to any values V [nk, dv <= dv_max] by plan_apply.
+struct Plan {
+  TrLayout L;
+  tr::Params p;        // all but the value slice and the output
+  const float* yp;     // the packed keys
+  unsigned char* w;    // the plan's workspace region (tr_layout(...).total bytes)
+  int64_t nk;
+  bool moment;
+};
+
+// Arguments are checked by the callers.  Wd != NULL: the moment form, with
+// directions Wd [nq, d].
+cudaError_t plan_prepare(const float* Xq, const float* Xk, const float* fq, const float* gk,
+                         const float* log_q, const float* log_k, int64_t nq, int64_t nk, int32_t d,
+                         int32_t dv_max, float eps, const float* Wd, unsigned char* w,
+                         unsigned int* fault, cudaStream_t s, Plan* P) {
+  const bool moment = Wd != nullptr;
+  const TrLayout L = tr_layout(nq, nk, d, dv_max, moment);
+  P->L = L;
+  P->w = w;
+  P->nk = nk;
+  P->moment = moment;
+  float* xp = reinterpret_cast<float*>(w + L.x);
+  float* yp = reinterpret_cast<float*>(w + L.y);
+  float* xn = reinterpret_cast<float*>(w + L.xn);
+  float* yn = reinterpret_cast<float*>(w + L.yn);
+  float* kb = reinterpret_cast<float*>(w + L.kb);
+  float* rt = reinterpret_cast<float*>(w + L.rt);
+  P->yp = yp;
+  const float scale = static_cast<float>(1.4426950408889634 / eps);
+  const unsigned rgrid = static_cast<unsigned>((L.n_pad + 255) / 256);
+  cudaError_t e = pack(Xq, nq, d, L.n_pad, L.d_pad, xp, nullptr, xn, s);
+  if (e == cudaSuccess) e = pack(Xk, nk, d, L.m_pad, L.d_pad, yp, nullptr, yn, s);
+  float* wq = moment ? reinterpret_cast<float*>(w + L.wq) : nullptr;
+  if (e == cudaSuccess && moment)
+    e = pack(Wd, nq, d, L.n_pad, L.d_pad, wq, nullptr, reinterpret_cast<float*>(w + L.wn), s);
+  if (e == cudaSuccess) e = bias(gk, log_k, yn, nk, L.m_pad, eps, kb, s);
+  if (e == cudaSuccess) {
+    tr::rowterm_kernel<<<rgrid, 256, 0, s>>>(fq, log_q, xn, nq, L.n_pad, scale, rt);
+    if (!moment && dv_max > 1)
+      tr::rowterm16_kernel<<<rgrid, 256, 0, s>>>(fq, log_q, xn, nq, L.n_pad, scale,
+                                                 reinterpret_cast<float*>(w + L.rt16),
+                                                 reinterpret_cast<float*>(w + L.rsc));
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return e;
+  tr::Params& p = P->p;
+  if (!encode_rows128(&p.qmap, xp, L.n_pad, L.d_pad, BM) ||
+      (moment && !encode_rows128(&p.wmap, wq, L.n_pad, L.d_pad, BM)))
+    return cudaErrorInvalidValue;
+  if (!moment) p.wmap = p.qmap;
+  unsigned int* misc = reinterpret_cast<unsigned int*>(w + L.misc);  // vmax, guard, s_V, 1/s_V
+  p.kbias = kb;
+  p.rowterm = rt;
+  p.kval = nullptr;
+  p.rowterm16 = reinterpret_cast<float*>(w + L.rt16);
+  p.rowscale = reinterpret_cast<float*>(w + L.rsc);
+  p.vscale = reinterpret_cast<float*>(misc + 2);
+  p.guard = misc + 1;
+  p.guard_mode = 0;
+  p.out = nullptr;
+  p.mass = nullptr;
+  p.part_o = reinterpret_cast<float*>(w + L.po);
+  p.part_mass = reinterpret_cast<float*>(w + L.pm);
+  p.nq = nq;
+  p.d = 0;
+  p.n_kc = L.d_pad / KC;
+  p.c1 = static_cast<float>(2.0 * 1.4426950408889634 / eps);
+  p.fault = fault;
+  return cudaSuccess;
+}
+
+// out [nq, dv] = pi V (weights pi_ij (w_i . y_j) for the moment form) and,
+// if mass != NULL, mass = pi 1; V [nk, dv], 1 <= dv <= the plan's dv_max.
+cudaError_t plan_apply(const Plan& P, const float* V, int32_t dv, float* out, float* mass,
+                       cudaStream_t s) {
+  const TrLayout& L = P.L;
+  unsigned char* w = P.w;
+  const int32_t v_pad = static_cast<int32_t>(round_up(dv, KC));
+  float* vt = reinterpret_cast<float*>(w + L.yt);
+  const dim3 grid(static_cast<unsigned>(L.m_pad / 32), static_cast<unsigned>(v_pad / 32));
+  tr::pack_transposed_kernel<<<grid, dim3(32, 8), 0, s>>>(V, P.nk, dv, L.m_pad, v_pad, vt);
+  cudaError_t e = cudaGetLastError();
+  // HALF operands (several value columns, not the moment form): the V scale
+  // and the f16 values; the guard starts clear
+  if (e == cudaSuccess && !P.moment && dv > 1) {
+    unsigned int* misc = reinterpret_cast<unsigned int*>(w + L.misc);
+    e = cudaMemsetAsync(misc, 0, 2 * sizeof(unsigned int), s);
+    if (e == cudaSuccess) {
+      const int64_t total = P.nk * static_cast<int64_t>(dv);
+      const unsigned vb = static_cast<unsigned>(std::min<int64_t>((total + 255) / 256, 1024));
+      tr::vmax_kernel<<<vb, 256, 0, s>>>(V, total, misc);
+      tr::vscale_kernel<<<1, 1, 0, s>>>(misc, reinterpret_cast<float*>(misc + 2), misc + 1);
+      tr::pack_transposed_f16_kernel<<<grid, dim3(32, 8), 0, s>>>(
+          V, P.nk, dv, L.m_pad, v_pad, P.p.vscale, reinterpret_cast<__half*>(w + L.yh));
+      e = cudaGetLastError();
+    }
+  }
+  tr::Params p = P.p;
+  p.out = out;
+  p.d = dv;
+  // one launch per slice of up to 256 value coordinates; the first also
+  // writes the row masses
+  for (int32_t v0 = 0; v0 < v_pad && e == cudaSuccess; v0 += tr::DV) {
+    const int32_t w_slice = std::min<int32_t>(tr::DV, v_pad - v0);
+    e = launch_transport(p, L, v_pad, P.yp, vt, w + L.yh, v0, w_slice, v0 == 0 ? mass : nullptr,
+                         P.moment, s);
+  }
+  return e;
 }
 
 // The plan of (f, g) applied to the values V [m, dv]: out = pi V, mass =
@@ -1156,93 +1270,25 @@ int apply_impl(const float* X, const float* Y, const float* f, const float* g, c
   cudaError_t e = cudaSuccess;
   unsigned int* fault = b4::device_fault_latch(&e);
   if (e != cudaSuccess) return b4::record_cuda_error(e);
-  unsigned char* w = static_cast<unsigned char*>(workspace);
-  float* xp = reinterpret_cast<float*>(w + L.x);
-  float* yp = reinterpret_cast<float*>(w + L.y);
-  float* vt = reinterpret_cast<float*>(w + L.yt);
-  float* xn = reinterpret_cast<float*>(w + L.xn);
-  float* yn = reinterpret_cast<float*>(w + L.yn);
-  float* kb = reinterpret_cast<float*>(w + L.kb);
-  float* rt = reinterpret_cast<float*>(w + L.rt);
-  e = pack(X, n, d, L.n_pad, L.d_pad, xp, nullptr, xn, s);
-  if (e == cudaSuccess) e = pack(Y, m, d, L.m_pad, L.d_pad, yp, nullptr, yn, s);
-  float* wq = moment ? reinterpret_cast<float*>(w + L.wq) : nullptr;
-  if (e == cudaSuccess && moment)
-    e = pack(Wd, n, d, L.n_pad, L.d_pad, wq, nullptr, reinterpret_cast<float*>(w + L.wn), s);
-  if (e == cudaSuccess) {
-    const dim3 grid(static_cast<unsigned>(L.m_pad / 32), static_cast<unsigned>(L.v_pad / 32));
-    tr::pack_transposed_kernel<<<grid, dim3(32, 8), 0, s>>>(V, m, dv, L.m_pad, L.v_pad, vt);
-    e = cudaGetLastError();
-  }
-  if (e == cudaSuccess) e = bias(g, log_b, yn, m, L.m_pad, eps, kb, s);
-  if (e == cudaSuccess) {
-    tr::rowterm_kernel<<<static_cast<unsigned>((L.n_pad + 255) / 256), 256, 0, s>>>(
-        f, log_a, xn, n, L.n_pad, static_cast<float>(1.4426950408889634 / eps), rt);
-    e = cudaGetLastError();
-  }
-  // HALF operands (several value columns, not the moment form): scaled row
-  // terms, the V scale and the f16 values; the guard starts clear
-  const bool half = !moment && dv > 1;
-  unsigned int* misc = reinterpret_cast<unsigned int*>(w + L.misc);  // vmax, guard, s_V, 1/s_V
-  float* vscale = reinterpret_cast<float*>(misc + 2);
-  if (e == cudaSuccess && half) {
-    e = cudaMemsetAsync(misc, 0, 2 * sizeof(unsigned int), s);
-    if (e == cudaSuccess) {
-      tr::rowterm16_kernel<<<static_cast<unsigned>((L.n_pad + 255) / 256), 256, 0, s>>>(
-          f, log_a, xn, n, L.n_pad, static_cast<float>(1.4426950408889634 / eps),
-          reinterpret_cast<float*>(w + L.rt16), reinterpret_cast<float*>(w + L.rsc));
-      const int64_t total = m * static_cast<int64_t>(dv);
-      const unsigned vb = static_cast<unsigned>(std::min<int64_t>((total + 255) / 256, 1024));
-      tr::vmax_kernel<<<vb, 256, 0, s>>>(V, total, misc);
-      tr::vscale_kernel<<<1, 1, 0, s>>>(misc, vscale, misc + 1);
-      const dim3 grid(static_cast<unsigned>(L.m_pad / 32), static_cast<unsigned>(L.v_pad / 32));
-      tr::pack_transposed_f16_kernel<<<grid, dim3(32, 8), 0, s>>>(
-          V, m, dv, L.m_pad, L.v_pad, vscale, reinterpret_cast<__half*>(w + L.yh));
-      e = cudaGetLastError();
-    }
-  }
-  if (e != cudaSuccess) return b4::record_cuda_error(e);
-  tr::Params p;
-  if (!encode_rows128(&p.qmap, xp, L.n_pad, L.d_pad, BM) ||
-      (moment && !encode_rows128(&p.wmap, wq, L.n_pad, L.d_pad, BM)))
-    return b4::record_cuda_error(cudaErrorInvalidValue);
-  if (!moment) p.wmap = p.qmap;
-  p.kbias = kb;
-  p.rowterm = rt;
-  p.kval = nullptr;
-  p.rowterm16 = reinterpret_cast<float*>(w + L.rt16);
-  p.rowscale = reinterpret_cast<float*>(w + L.rsc);
-  p.vscale = vscale;
-  p.guard = misc + 1;
-  p.guard_mode = 0;
-  p.out = out;
-  p.mass = nullptr;
-  p.part_o = reinterpret_cast<float*>(w + L.po);
-  p.part_mass = reinterpret_cast<float*>(w + L.pm);
-  p.nq = n;
-  p.d = dv;
-  p.n_kc = L.d_pad / KC;
-  p.c1 = static_cast<float>(2.0 * 1.4426950408889634 / eps);
-  p.fault = fault;
-  // one launch per slice of up to 256 value coordinates; the first also
-  // writes the row masses
-  for (int32_t v0 = 0; v0 < L.v_pad && e == cudaSuccess; v0 += tr::DV) {
-    const int32_t w_slice = std::min<int32_t>(tr::DV, L.v_pad - v0);
-    e = launch_transport(p, L, yp, vt, w + L.yh, v0, w_slice, v0 == 0 ? mass : nullptr, moment, s);
-  }
+  Plan P;
+  e = plan_prepare(X, Y, f, g, log_a, log_b, n, m, d, dv, eps, Wd,
+                   static_cast<unsigned char*>(workspace), fault, s, &P);
+  if (e == cudaSuccess) e = plan_apply(P, V, dv, out, mass, s);
   return b4::record_cuda_error(e);
 }
 
-// Workspace of the Hessian-vector product: one region for the plan
-// applications (run one after another), then the vectors.
+// Workspace of the Hessian-vector product: the plan of (f, g) with X as
+// queries (fwd) and with Y as queries (rev; after CG, the moment form's
+// plan), then the vectors.
 struct HvpLayout {
-  size_t apply, py, xv, rhs, w, mr, z, zb, res, sv, pv, ap, pp, diag, mass, u, g2, mv, part, scal, total;
+  size_t fwd, rev, py, xv, rhs, w, mr, z, zb, res, sv, pv, ap, pp, diag, mass, u, g2, mv, part, scal,
+      total;
 };
 
 HvpLayout hvp_layout(int64_t n, int64_t m, int32_t d) {
   HvpLayout H;
-  const size_t ap = std::max({tr_layout(n, m, d, d + 1).total, tr_layout(m, n, d, d + 1).total,
-                              tr_layout(n, m, d, d, true).total});
+  const size_t fwd = tr_layout(n, m, d, d + 1).total;
+  const size_t rev = std::max(tr_layout(m, n, d, d + 1).total, tr_layout(n, m, d, d, true).total);
   const size_t N = static_cast<size_t>(n + m);
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -1250,7 +1296,8 @@ HvpLayout hvp_layout(int64_t n, int64_t m, int32_t d) {
     o += align_bytes(bytes);
     return at;
   };
-  H.apply = take(ap);
+  H.fwd = take(fwd);
+  H.rev = take(rev);
   H.py = take(static_cast<size_t>(n) * d * 4);
   H.xv = take(static_cast<size_t>(n) * 4);
   H.rhs = take(N * 4);
@@ -1292,9 +1339,10 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
     return B4_EINVAL;
   unsigned char* w = static_cast<unsigned char*>(workspace);
   auto F = [&](size_t off) { return reinterpret_cast<float*>(w + off); };
-  void* aw = w + H.apply;
-  const size_t ab = H.py - H.apply;
   const int64_t N = n + m;
+  cudaError_t e = cudaSuccess;
+  unsigned int* fault = b4::device_fault_latch(&e);
+  if (e != cudaSuccess) return b4::record_cuda_error(e);
   float *PY = F(H.py), *xv = F(H.xv), *rhs = F(H.rhs), *W = F(H.w), *Mr = F(H.mr), *z = F(H.z);
   float *zb = F(H.zb), *res = F(H.res), *sv = F(H.sv), *pv = F(H.pv), *Ap = F(H.ap), *Pp = F(H.pp);
   float *diag = F(H.diag), *mass = F(H.mass), *U = F(H.u), *G2 = F(H.g2), *MV = F(H.mv);
@@ -1308,30 +1356,30 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
     tr::dot_final_kernel<<<1, tr::kDotBlocks, 0, s>>>(part, outp);
     return cudaGetLastError();
   };
-  int st;
+  // the plan in both directions, prepared once for every application below
+  Plan fwd, rev;
+  e = plan_prepare(X, Y, f, g, log_a, log_b, n, m, d, d + 1, eps, nullptr, w + H.fwd, fault, s, &fwd);
+  if (e == cudaSuccess)
+    e = plan_prepare(Y, X, g, f, log_b, log_a, m, n, d, d + 1, eps, nullptr, w + H.rev, fault, s, &rev);
   // pi Y, then r and the values [x.v, V]
-  if ((st = apply_impl(X, Y, f, g, log_a, log_b, Y, d, PY, mass, n, m, d, eps, aw, ab, s)) != B4_OK)
-    return st;
+  if (e == cudaSuccess) e = plan_apply(fwd, Y, d, PY, mass, s);
+  if (e != cudaSuccess) return b4::record_cuda_error(e);
   tr::hvp_prep_kernel<<<bq, 256, 0, s>>>(X, V, PY, log_a, n, d, xv, rhs, W);
   // pi^T [x.v, V], then c
-  if ((st = apply_impl(Y, X, g, f, log_b, log_a, W, d + 1, Mr, mass, m, n, d, eps, aw, ab, s)) != B4_OK)
-    return st;
+  if ((e = plan_apply(rev, W, d + 1, Mr, mass, s)) != cudaSuccess) return b4::record_cuda_error(e);
   tr::hvp_col_kernel<<<bk, 256, 0, s>>>(Y, Mr, m, d, rhs + n);
   // conjugate gradients for (df, dg)
   tr::cg_init_kernel<<<bn, 256, 0, s>>>(rhs, log_a, log_b, n, N, diag, z, zb, res, sv, pv);
-  cudaError_t e = dot(res, sv, scal + 0);
+  e = dot(res, sv, scal + 0);
   if (e != cudaSuccess) return b4::record_cuda_error(e);
   tr::copy_scalar_kernel<<<1, 1, 0, s>>>(scal + 0, scal + 3);
   tr::copy_scalar_kernel<<<1, 1, 0, s>>>(scal + 0, scal + 5);
   for (int32_t k = 0; k < cg_iters; ++k) {
     double* rs = scal + (k & 1);
     double* rs_next = scal + ((k + 1) & 1);
-    if ((st = apply_impl(X, Y, f, g, log_a, log_b, pv + n, 1, Pp, mass, n, m, d, eps, aw, ab, s)) !=
-        B4_OK)
-      return st;
-    if ((st = apply_impl(Y, X, g, f, log_b, log_a, pv, 1, Pp + n, mass, m, n, d, eps, aw, ab, s)) !=
-        B4_OK)
-      return st;
+    if ((e = plan_apply(fwd, pv + n, 1, Pp, nullptr, s)) != cudaSuccess ||
+        (e = plan_apply(rev, pv, 1, Pp + n, nullptr, s)) != cudaSuccess)
+      return b4::record_cuda_error(e);
     tr::cg_matvec_kernel<<<bn, 256, 0, s>>>(diag, pv, Pp, N, Ap);
     if ((e = dot(pv, Ap, scal + 2)) != cudaSuccess) return b4::record_cuda_error(e);
     tr::cg_step_kernel<<<bn, 256, 0, s>>>(rs, scal + 2, scal + 3, scal + 5, pv, Ap, diag, N, z,
@@ -1347,11 +1395,12 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
   tr::null_remove_kernel<<<bn, 256, 0, s>>>(scal + 4, n, N, zb);
   // pi [dg, dg y], the second moment, and the combination
   tr::hvp_values_kernel<<<bk, 256, 0, s>>>(Y, zb + n, m, d, U);
-  if ((st = apply_impl(X, Y, f, g, log_a, log_b, U, d + 1, G2, mass, n, m, d, eps, aw, ab, s)) != B4_OK)
-    return st;
-  if ((st = apply_impl(X, Y, f, g, log_a, log_b, Y, d, MV, mass, n, m, d, eps, aw, ab, s, V)) !=
-      B4_OK)
-    return st;
+  if ((e = plan_apply(fwd, U, d + 1, G2, nullptr, s)) != cudaSuccess) return b4::record_cuda_error(e);
+  // the second moment: the moment form's plan in the region of rev (done)
+  Plan mom;
+  e = plan_prepare(X, Y, f, g, log_a, log_b, n, m, d, d, eps, V, w + H.rev, fault, s, &mom);
+  if (e == cudaSuccess) e = plan_apply(mom, Y, d, MV, nullptr, s);
+  if (e != cudaSuccess) return b4::record_cuda_error(e);
   const int64_t tot = n * static_cast<int64_t>(d);
   const int64_t blocks = std::min<int64_t>((tot + 255) / 256, 1 << 20);
   tr::hvp_final_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
