@@ -268,13 +268,14 @@ def _apply_bound(X, Y, f, g, log_a, log_b, V, eps):
     return 2.0 * (rel + 2.0 ** -10 + 2.0 ** -11 + m_pad * 2.0 ** -23)[:, None] * (P @ np.abs(np64(V)))
 
 
-@pytest.mark.parametrize("vmag", [1e6, 1e-6])
-def test_apply_plan_f16_overflow_redo_and_value_scale(vmag):
+@pytest.mark.parametrize("vmag,dv", [(1e6, 40), (1e-6, 40), (1.0, 200)])
+def test_apply_plan_f16_overflow_redo_and_value_scale(vmag, dv):
     """The f16 second product scales P by 2^15 / a_i and V by a power of
     two.  Potentials shifted by 4 eps make every row of pi sum to e^4 a_i,
-    past that range: the TF32 redo must take over, within the same bound.
-    Values of magnitude 1e6 and 1e-6 exercise the V scale both ways."""
-    n, m, d, dv, eps = 400, 500, 8, 40, 0.1
+    past that range: the TF32 redo must take over, within the same bound
+    (192-key tiles for 40 value columns, 256-key tiles for 200).  Values
+    of magnitude 1e6 and 1e-6 exercise the V scale both ways."""
+    n, m, d, eps = 400, 500, 8, 0.1
     X, Y, log_a, log_b = workloads.eot_clouds(n, m, d, seed=31, device=DEV, random_weights=True)
     f64, g64 = oeot.sinkhorn64(np64(X), np64(Y), np64(log_a), np64(log_b), eps, 30)
     V = torch.randn(m, dv, generator=torch.Generator().manual_seed(7)).to(DEV) * vmag
