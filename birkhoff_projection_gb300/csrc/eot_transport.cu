@@ -99,7 +99,8 @@ struct Params {
   const float* rowscale;   // HALF: a_i 2^-15, which takes a scaled p back to p
   const float* vscale;   // HALF: {s_V, 1 / s_V}, the power of two V was scaled by
   unsigned int* guard;   // HALF sets it when a scaled p leaves the f16 range
-  int32_t guard_mode;    // 1: run only if *guard is set (the VALUES redo)
+  int32_t guard_mode;    // 1: run only if *guard is set (the VALUES redo); 2: only if clear
+
   float* out;            // [nq, d]: columns v0 .. v0 + dv - 1 (those below d) written
   float* mass;           // [nq] row masses, or NULL
   float* part_o;         // [ctas][2][128][dv]: O of row blocks this CTA covers in part
@@ -118,6 +119,13 @@ struct Params {
   float c1;              // 2 log2(e) / eps
   unsigned int* fault;
 };
+
+// Whether a launch with this guard is to do nothing (uniform over the grid).
+__device__ __forceinline__ bool guard_skips(const Params& p) {
+  if (p.guard_mode == 0) return false;
+  const unsigned int g = *reinterpret_cast<volatile unsigned int*>(p.guard);
+  return p.guard_mode == 1 ? g == 0u : g != 0u;
+}
 
 // First tile and tile count of CTA b's run of the last row blocks.
 __host__ __device__ __forceinline__ int64_t run_start(const Params& p, int64_t b) {
@@ -264,7 +272,7 @@ __global__ void grad_kernel(const float* __restrict__ X, const float* __restrict
 // CTA covered whole were written by the transport kernel and are skipped.
 constexpr int kFixupElems = 1024;
 __global__ void fixup_kernel(const __grid_constant__ Params p) {
-  if (p.guard_mode != 0 && *reinterpret_cast<volatile unsigned int*>(p.guard) == 0u) return;
+  if (guard_skips(p)) return;
   __shared__ int64_t base[MAX_CTAS];          // first partial row of each contributing CTA
   const int64_t rb = p.full_rb + blockIdx.x;  // a row block of the runs
   const int64_t tr = blockIdx.x;                // its index among them
@@ -435,6 +443,12 @@ __global__ void cg_best_kernel(const double* __restrict__ rs, double* __restrict
   *keep = b ? 1.0 : 0.0;
   if (b) *best = *rs;
 }
+// stop = 1 once the iteration has stopped (the next step's alpha is 0), so
+// that the next step's plan products need not be computed.
+__global__ void cg_stop_kernel(const double* __restrict__ rs, const double* __restrict__ rs0,
+                               const double* __restrict__ best, unsigned int* __restrict__ stop) {
+  *stop = cg_live(rs, rs0, best) ? 0u : 1u;
+}
 // zb = z where the iterate just made is the best so far.
 __global__ void cg_keep_kernel(const double* __restrict__ keep, const float* __restrict__ z,
                                int64_t N, float* __restrict__ zb) {
@@ -551,8 +565,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   constexpr bool H16 = MODE == HALF;
   constexpr int VK = C::VK;
   constexpr int VPT = C::VPT;
-  // the VALUES redo of a HALF launch runs only if that launch overflowed
-  if (p.guard_mode != 0 && *reinterpret_cast<volatile unsigned int*>(p.guard) == 0u) return;
+  // the VALUES redo of a HALF launch runs only if that launch overflowed;
+  // guard_mode 2 skips a launch whose flag is set (a finished CG)
+  if (guard_skips(p)) return;
   constexpr int BN = C::BN;
   constexpr int NBUF = C::NBUF;
   constexpr int SLOT = C::SLOT;
@@ -1106,7 +1121,8 @@ bool encode_values(CUtensorMap* map, const void* base, const TrLayout& L, int32_
 
 cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, int32_t v_pad,
                              const float* yp, const float* yt, const void* yh, int32_t v0,
-                             int32_t dv, float* mass, bool moment, cudaStream_t stream) {
+                             int32_t dv, float* mass, bool moment, cudaStream_t stream,
+                             unsigned int* skip = nullptr) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -1122,6 +1138,10 @@ cudaError_t launch_transport(const tr::Params& base, const TrLayout& L, int32_t 
   if (base.d == 1) {
     p.dv = 1;
     p.kval = yt;  // row 0 of the transposed values: v_j, zero past m
+    if (skip != nullptr) {  // nothing to do once *skip is set
+      p.guard = skip;
+      p.guard_mode = 2;
+    }
     return launch_shape<256, tr::VECTOR>(p, L, yp, dev, nsm, stream);
   }
   // f16 operands for P V, then the TF32 redo that runs only if they overflowed
@@ -1212,8 +1232,10 @@ cudaError_t plan_prepare(const float* Xq, const float* Xk, const float* fq, cons
 
 // out [nq, dv] = pi V (weights pi_ij (w_i . y_j) for the moment form) and,
 // if mass != NULL, mass = pi 1; V [nk, dv], 1 <= dv <= the plan's dv_max.
+// skip (one value column only): a device flag; once it is set, the
+// products are not computed and out keeps what it held.
 cudaError_t plan_apply(const Plan& P, const float* V, int32_t dv, float* out, float* mass,
-                       cudaStream_t s) {
+                       cudaStream_t s, unsigned int* skip = nullptr) {
   const TrLayout& L = P.L;
   unsigned char* w = P.w;
   const int32_t v_pad = static_cast<int32_t>(round_up(dv, KC));
@@ -1244,7 +1266,7 @@ cudaError_t plan_apply(const Plan& P, const float* V, int32_t dv, float* out, fl
   for (int32_t v0 = 0; v0 < v_pad && e == cudaSuccess; v0 += tr::DV) {
     const int32_t w_slice = std::min<int32_t>(tr::DV, v_pad - v0);
     e = launch_transport(p, L, v_pad, P.yp, vt, w + L.yh, v0, w_slice, v0 == 0 ? mass : nullptr,
-                         P.moment, s);
+                         P.moment, s, dv == 1 ? skip : nullptr);
   }
   return e;
 }
@@ -1347,7 +1369,9 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
   float *zb = F(H.zb), *res = F(H.res), *sv = F(H.sv), *pv = F(H.pv), *Ap = F(H.ap), *Pp = F(H.pp);
   float *diag = F(H.diag), *mass = F(H.mass), *U = F(H.u), *G2 = F(H.g2), *MV = F(H.mv);
   double* part = reinterpret_cast<double*>(w + H.part);
-  double* scal = reinterpret_cast<double*>(w + H.scal);  // rs[2], pAp, rs0, z . n0, best, keep
+  // rs[2], pAp, rs0, z . n0, best, keep, and (as an unsigned int) the stop flag
+  double* scal = reinterpret_cast<double*>(w + H.scal);
+  unsigned int* stop = reinterpret_cast<unsigned int*>(scal + 7);
   const unsigned bn = static_cast<unsigned>((N + 255) / 256);
   const unsigned bq = static_cast<unsigned>((n + 255) / 256);
   const unsigned bk = static_cast<unsigned>((m + 255) / 256);
@@ -1374,11 +1398,14 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
   if (e != cudaSuccess) return b4::record_cuda_error(e);
   tr::copy_scalar_kernel<<<1, 1, 0, s>>>(scal + 0, scal + 3);
   tr::copy_scalar_kernel<<<1, 1, 0, s>>>(scal + 0, scal + 5);
+  if ((e = cudaMemsetAsync(stop, 0, sizeof(double), s)) != cudaSuccess)
+    return b4::record_cuda_error(e);
   for (int32_t k = 0; k < cg_iters; ++k) {
     double* rs = scal + (k & 1);
     double* rs_next = scal + ((k + 1) & 1);
-    if ((e = plan_apply(fwd, pv + n, 1, Pp, nullptr, s)) != cudaSuccess ||
-        (e = plan_apply(rev, pv, 1, Pp + n, nullptr, s)) != cudaSuccess)
+    // once the iteration has stopped, the products are skipped on the device
+    if ((e = plan_apply(fwd, pv + n, 1, Pp, nullptr, s, stop)) != cudaSuccess ||
+        (e = plan_apply(rev, pv, 1, Pp + n, nullptr, s, stop)) != cudaSuccess)
       return b4::record_cuda_error(e);
     tr::cg_matvec_kernel<<<bn, 256, 0, s>>>(diag, pv, Pp, N, Ap);
     if ((e = dot(pv, Ap, scal + 2)) != cudaSuccess) return b4::record_cuda_error(e);
@@ -1386,6 +1413,7 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
                                           res, sv);
     if ((e = dot(res, sv, rs_next)) != cudaSuccess) return b4::record_cuda_error(e);
     tr::cg_best_kernel<<<1, 1, 0, s>>>(rs_next, scal + 5, scal + 6);
+    tr::cg_stop_kernel<<<1, 1, 0, s>>>(rs_next, scal + 3, scal + 5, stop);
     tr::cg_keep_kernel<<<bn, 256, 0, s>>>(scal + 6, z, N, zb);
     tr::cg_dir_kernel<<<bn, 256, 0, s>>>(rs, rs_next, scal + 3, scal + 5, sv, N, pv);
   }

@@ -129,7 +129,9 @@ int eot_transport(const float *X, const float *Y, const float *f, const float *g
  * residual levels off: the iteration stops, on the device, once
  * r^T diag^-1 r is 1e-8 of its first value or has risen 1e4-fold above its
  * smallest value, and the iterate with the smallest value is used.  Its
- * component along (1, -1), which leaves H V unchanged, is removed.  Each step applies pi and pi^T once
+ * component along (1, -1), which leaves H V unchanged, is removed.
+ * cg_iters is a maximum: the plan products of the steps after the stop are
+ * skipped on the device.  Each step applies pi and pi^T once
  * to one column (two streaming passes over the n x m scores); the
  * remaining terms are plan applications (pi Y, pi^T [x.v, V],
  * pi [dg, dg y]) and one second-moment pass sum_j pi_ij (v_i . y_j) y_j.
