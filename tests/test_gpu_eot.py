@@ -209,23 +209,34 @@ def test_transport_row_masses_at_consistent_potentials():
     assert np.abs(mr / a - 1).max() <= 1e-3
 
 
-def test_transport_full_size_sampled_rows():
-    """65536 x 65536 points, d = 512 (four value slices): sampled rows
-    against the oracle's plan rows."""
+@pytest.mark.parametrize("d", [64, 512])
+def test_transport_full_size_sampled_rows(d):
+    """65536 x 65536 points at the bench sizes (d = 64: one value slice of
+    192-key f16 tiles; d = 512: two slices of 256-key tiles): sampled rows
+    against the oracle's plan rows.  With 512 row blocks on 152 SMs the
+    first 456 row blocks go whole to CTAs and the rest in stream-K runs;
+    rows on both sides of that line are sampled.  At d = 64 a one-column
+    plan product (CUDA cores) is checked on the same rows."""
     n = m = 65536
-    d = 512
     eps = workloads.EOT_EPS
     X, Y, log_a, log_b = workloads.eot_clouds(n, m, d, seed=0, device=DEV)
     g = torch.zeros(m, device=DEV)
     f = eot.update(X, Y, g, log_b, eps)
     PY, mass = eot.transport(X, Y, f, g, log_a, log_b, eps)
-    rows = np.r_[0, 127, 128, 30000, n - 1, np.random.default_rng(1).integers(0, n, 5)]
+    rows = np.r_[0, 127, 128, 30000, 58367, 58368, 60000, n - 1,
+                 np.random.default_rng(1).integers(0, n, 5)]
     idx = torch.as_tensor(rows, device=DEV)
     args = (np64(X[idx]), np64(Y), np64(f[idx]), np64(g), np64(log_a[idx]), np64(log_b), eps)
     PYr, mr = oeot.transport64(*args)
     b_py, b_mass = transport_bounds(*args)
     assert np.all(np.abs(np64(PY)[rows] - PYr) <= b_py)
     assert np.all(np.abs(np64(mass)[rows] - mr) <= b_mass)
+    if d == 64:
+        V = torch.randn(m, 1, generator=torch.Generator().manual_seed(9)).to(DEV)
+        out, _ = eot.apply_plan(X, Y, f, g, log_a, log_b, V, eps)
+        ref, _ = oeot.apply_plan64(*args, np64(V))
+        bound = _apply_bound(X[idx], Y, f[idx], g, log_a[idx], log_b, V, eps)
+        assert np.all(np.abs(np64(out)[rows] - ref) <= bound)
 
 
 @pytest.mark.parametrize("n,m,d,dv", [(700, 900, 16, 5), (300, 500, 64, 1), (257, 300, 8, 300)])
