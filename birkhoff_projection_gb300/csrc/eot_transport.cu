@@ -1,16 +1,22 @@
 // eot_transport.cu -- the transport application of streaming entropic OT
-// ("FlashSinkhorn: IO-Aware Entropic OT on GPU", Methodik s3): with the plan
-// of given potentials, pi_ij = a_i b_j exp((f_i + g_j - ||x_i - y_j||^2)/eps),
-// the kernel computes (pi Y)_i = sum_j pi_ij y_j and the row masses
-// r_i = sum_j pi_ij without storing pi, as two chained tensor-core products
-// per key tile (attention form): S = Q K^T into TMEM, P = 2^(S c1 + bias_j +
-// rowterm_i) written by the epilogue warps back over S in TMEM, then
-// O += P V^T into TMEM with P read from TMEM and V^T (the transposed key
-// points) from shared memory.  Because the
-// potential f fixes each row's normaliser, no running maximum is needed and
-// O is never rescaled.  From O and r follow the gradient of the entropic OT
-// cost with respect to X, 2 (r_i x_i - O_i), and the barycentric map O_i / r_i.
-// The extern "C" entries are declared and documented in eot_stream.h.
+// and the Hessian-vector product built on it ("FlashSinkhorn: IO-Aware
+// Entropic OT on GPU", Methodik s3).  With the plan of given potentials,
+// pi_ij = a_i b_j exp((f_i + g_j - ||x_i - y_j||^2)/eps), the kernel
+// computes O = pi V for values V [m, dv] (V = Y gives pi Y) and the row
+// masses r_i = sum_j pi_ij without storing pi, as two chained tensor-core
+// products per key tile (attention form): S = Q K^T (TF32) into TMEM,
+// P = 2^(S c1 + bias_j + rowterm_i) written by the epilogue warps back over
+// S in TMEM, then O += P V^T into TMEM with P read from TMEM (f16, scaled)
+// and V^T from shared memory.  Because the potential f fixes each row's
+// normaliser, no running maximum is needed and O is never rescaled.  From
+// O and r follow the gradient of the entropic OT cost with respect to X,
+// 2 (r_i x_i - O_i), and the barycentric map O_i / r_i.
+//
+// Layout of this file: the kernel shapes and parameters; small packing,
+// row-term, fix-up and CG kernels; transport_kernel (producer, MMA and
+// epilogue roles, four modes); the host side (workspace layout, launches,
+// plan_prepare / plan_apply, the HVP's conjugate gradients).  The extern
+// "C" entries are declared and documented in eot_stream.h.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
