@@ -44,6 +44,7 @@ SIGNATURES = {
     "eot_apply_plan_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, ctypes.c_int32, ctypes.c_int32]),
     "eot_apply_plan": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32, _vp, _vp, _i64,
                               _i64, ctypes.c_int32, ctypes.c_float, _vp, ctypes.c_size_t, _vp]),
+    "eot_transport_schedule": (_int, [_i64, ctypes.c_int32, ctypes.c_int32, _vp]),
     "eot_hvp_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, ctypes.c_int32]),
     "eot_hvp": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int32,
                        ctypes.c_float, ctypes.c_int32, _vp, ctypes.c_size_t, _vp]),

@@ -25,6 +25,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <vector>
 
 #include "b4_device.cuh"
 #include "b4_launch.cuh"
@@ -145,6 +146,39 @@ __host__ __device__ __forceinline__ int64_t run_owner(const Params& p, int64_t T
   const int64_t cut = p.t_rem * (p.t_base + 1);
   return T < cut ? T / (p.t_base + 1) : p.t_rem + (T - cut) / p.t_base;
 }
+// The partial slot of CTA b that holds row block full_rb + tr (tr-th of
+// the run's row blocks): 2b for the first row block of its run, 2b + 1 for
+// its last.
+__host__ __device__ __forceinline__ int64_t fixup_slot(const Params& p, int64_t b, int64_t tr) {
+  return b * 2 + (run_start(p, b) / p.n_kt == tr ? 0 : 1);
+}
+
+// The tiles of CTA b in the order it processes them: its whole row blocks
+// b, b + ctas, ... (n_full of them), then its run of the last row blocks.
+// Each role of the kernel walks them with one of these; there is a
+// division only where the run begins, not per tile.
+struct TileWalk {
+  int64_t u, rb, kt;  // local tile index, row block, key tile
+  int64_t n_kt, u_run, t0, full_rb, ctas;
+  __host__ __device__ TileWalk(const Params& p, int64_t b, int64_t ctas_)
+      : u(0), rb(b), kt(0), n_kt(p.n_kt), u_run(p.n_full * p.n_kt), t0(run_start(p, b)),
+        full_rb(p.full_rb), ctas(ctas_) {
+    if (u_run == 0) run_begin();
+  }
+  __host__ __device__ void run_begin() {
+    rb = full_rb + t0 / n_kt;
+    kt = t0 % n_kt;
+  }
+  __host__ __device__ void advance() {
+    ++u;
+    if (u == u_run) {
+      run_begin();
+    } else if (++kt == n_kt) {
+      kt = 0;
+      rb += u < u_run ? ctas : 1;
+    }
+  }
+};
 
 // MMA instruction descriptor (kind::tf32, fp32 accumulation, both operands
 // K-major) for M = 128 and a run-time N.
@@ -288,7 +322,7 @@ __global__ void fixup_kernel(const __grid_constant__ Params p) {
   // slot 0 holds the first row block of a CTA's run, slot 1 its last
   for (int k = threadIdx.x; k < nb; k += blockDim.x) {
     const int64_t b = b_lo + k;
-    base[k] = (b * 2 + (run_start(p, b) / p.n_kt == tr ? 0 : 1)) * BM;
+    base[k] = fixup_slot(p, b, tr) * BM;
   }
   __syncthreads();
   const int dv = p.dv;
@@ -602,31 +636,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t n_kt = p.n_kt;
   const int64_t u_run = p.n_full * n_kt;  // local index of this CTA's first run tile
-  const int64_t t0 = run_start(p, blockIdx.x);
   const int64_t cnt = u_run + run_count(p, blockIdx.x);
-  // Row block and key tile of this CTA's tiles, in order: each role walks
-  // them with a cursor (a division only where the run begins, not per tile).
-  struct Cursor {
-    int64_t u, rb, kt;
-  };
-  auto run_begin = [&](Cursor& c) {
-    c.rb = p.full_rb + t0 / n_kt;
-    c.kt = t0 % n_kt;
-  };
-  auto cursor0 = [&]() {
-    Cursor c{0, static_cast<int64_t>(blockIdx.x), 0};
-    if (u_run == 0) run_begin(c);
-    return c;
-  };
-  auto advance = [&](Cursor& c) {
-    ++c.u;
-    if (c.u == u_run) {
-      run_begin(c);
-    } else if (++c.kt == n_kt) {
-      c.kt = 0;
-      c.rb += c.u < u_run ? static_cast<int64_t>(gridDim.x) : 1;
-    }
-  };
+  const TileWalk walk0(p, blockIdx.x, gridDim.x);  // this CTA's first tile
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSLOT; ++s) {
@@ -669,11 +680,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     // ---------------- producer ----------------
     if (lane == 0) {
       uint32_t it = 0, nb = 0;  // ring slots and bias slots filled
-      Cursor cs = cursor0(), cv = cursor0();  // the tiles of S loads and of value loads
+      TileWalk cs = walk0, cv = walk0;  // the tiles of S loads and of value loads
       // the K chunks of S(u), after the biases of tile u
       auto load_s = [&](int64_t u) -> bool {
         const int64_t rb = cs.rb, kt = cs.kt;
-        advance(cs);
+        cs.advance();
         const int bs = static_cast<int>(u % NBIAS);
         if (!wait_bar(&bias_empty[bs], (static_cast<uint32_t>(u / NBIAS) & 1u) ^ 1u, abort_flag,
                       p.fault))
@@ -698,7 +709,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
       // the value chunks of P V(u), vg per slot (u in order)
       auto load_v = [&](int64_t) -> bool {
         const int64_t kt = cv.kt;
-        advance(cv);
+        cv.advance();
         for (int c = 0; c < VPT; c += vg, ++it) {
           const int s = static_cast<int>(it % NSLOT);
           if (!wait_bar(&slot_empty[s], ((it / NSLOT) & 1u) ^ 1u, abort_flag, p.fault)) return false;
@@ -763,10 +774,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
         return true;
       };
       // O += P(u) V(u)^T with P(u) read from its TMEM buffer (u in order)
-      Cursor cp = cursor0();
+      TileWalk cp = walk0;
       auto issue_pv = [&](int64_t u) -> bool {
         const int64_t kt = cp.kt;
-        advance(cp);
+        cp.advance();
         const bool first = kt == 0 || u == 0 || u == u_run, last = kt == n_kt - 1 || u == cnt - 1;
         if (first && !wait_bar(&o_empty, (seg & 1u) ^ 1u, abort_flag, p.fault)) return false;
         const int buf = static_cast<int>(u % NBUF);
@@ -837,8 +848,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) transport_kernel(const __grid_con
     float rt = 0.0f, mass = 0.0f, ov = 0.0f;  // ov: VECTOR's sum_j p_ij v_j
     float rsc = 1.0f;                         // HALF: a_i 2^-15 (scaled p -> p)
     bool ok = true;
-    Cursor ce = cursor0();
-    for (int64_t u = 0; u < cnt; ++u, advance(ce)) {
+    TileWalk ce = walk0;
+    for (int64_t u = 0; u < cnt; ++u, ce.advance()) {
       const int64_t rb = ce.rb, kt = ce.kt;
       if (u == 0 || kt == 0 || u == u_run) {  // a segment begins
         r = rb * BM + row;
@@ -1059,6 +1070,17 @@ bool tr_sizes_ok(int64_t n, int64_t m, int32_t d, int32_t dv) {
          dv >= 1 && dv <= 16384;
 }
 
+// The work split of n_rb row blocks of n_kt key tiles over `ctas` CTAs:
+// whole waves of row blocks first (one per CTA), the rest in equal runs.
+void make_schedule(tr::Params& p, int64_t n_rb, int64_t n_kt, int64_t ctas) {
+  p.n_kt = static_cast<int32_t>(n_kt);
+  p.n_full = n_rb / ctas;
+  p.full_rb = p.n_full * ctas;
+  const int64_t run_tiles = (n_rb - p.full_rb) * n_kt;
+  p.t_base = run_tiles / ctas;
+  p.t_rem = run_tiles % ctas;
+}
+
 // One launch of transport_kernel<BN, MODE> for the value slice in p
 // (v0, dv), then the fix-up of the row blocks that were split between CTAs.
 template <int BN, int MODE>
@@ -1083,15 +1105,9 @@ cudaError_t launch_shape(tr::Params& p, const TrLayout& L, const float* yp, int 
       p.vg = g;
       break;
     }
-  p.n_kt = static_cast<int32_t>(L.m_pad / BN);
-  const int64_t tiles = L.n_rb * p.n_kt;
-  const int64_t ctas = std::min<int64_t>(std::min<int64_t>(nsm, tiles), L.ctas);
-  // whole waves of row blocks, one per CTA; the rest in equal runs
-  p.n_full = L.n_rb / ctas;
-  p.full_rb = p.n_full * ctas;
-  const int64_t run_tiles = (L.n_rb - p.full_rb) * p.n_kt;
-  p.t_base = run_tiles / ctas;
-  p.t_rem = run_tiles % ctas;
+  const int64_t n_kt = L.m_pad / BN;
+  const int64_t ctas = std::min<int64_t>(std::min<int64_t>(nsm, L.n_rb * n_kt), L.ctas);
+  make_schedule(p, L.n_rb, n_kt, ctas);
   tr::transport_kernel<BN, MODE><<<static_cast<unsigned>(ctas), tr::NTHREADS, C::SMEM, stream>>>(p);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || L.n_rb == p.full_rb) return err;
@@ -1444,6 +1460,70 @@ int hvp_impl(const float* X, const float* Y, const float* f, const float* g, con
 
 }  // namespace
 }  // namespace eot
+
+extern "C" int eot_transport_schedule(int64_t n_rb, int32_t n_kt, int32_t ctas, int64_t* owner) {
+  if (n_rb < 1 || n_kt < 1 || ctas < 1 || ctas > eot::tr::MAX_CTAS || n_rb > (int64_t(1) << 24) ||
+      n_rb * n_kt < ctas || n_rb * n_kt > (int64_t(1) << 28))
+    return B4_EINVAL;
+  using eot::tr::Params;
+  Params p{};
+  eot::make_schedule(p, n_rb, n_kt, ctas);
+  const int64_t W = n_rb * n_kt;
+  std::vector<int64_t> own(static_cast<size_t>(W), -1), slot(static_cast<size_t>(W), -1);
+  std::vector<int64_t> holder(static_cast<size_t>(2 * ctas), -1);  // row block in each slot
+  int bad = 0;
+  for (int64_t b = 0; b < ctas; ++b) {
+    // the walk, segments and partial slots of transport_kernel's epilogue
+    eot::tr::TileWalk w(p, b, ctas);
+    const int64_t cnt = w.u_run + eot::tr::run_count(p, b);
+    std::vector<int64_t> seg;
+    int64_t kt0 = 0, sg = 0;
+    for (int64_t u = 0; u < cnt; ++u, w.advance()) {
+      if (u == 0 || w.kt == 0 || u == w.u_run) {
+        seg.clear();
+        kt0 = w.kt;
+      }
+      const int64_t T = w.rb * n_kt + w.kt;
+      if (w.rb < 0 || w.rb >= n_rb || own[static_cast<size_t>(T)] != -1) {
+        ++bad;  // outside the grid, or visited twice
+        continue;
+      }
+      own[static_cast<size_t>(T)] = b;
+      seg.push_back(T);
+      if (w.kt == n_kt - 1 || u == cnt - 1) {
+        const bool whole = kt0 == 0 && w.kt == n_kt - 1;
+        const int64_t s = whole ? -1 : b * 2 + (sg == p.n_full ? 0 : 1);
+        if (s >= 0) {
+          if (holder[static_cast<size_t>(s)] != -1) ++bad;  // a slot holding two row blocks
+          holder[static_cast<size_t>(s)] = w.rb;
+        }
+        for (const int64_t t : seg) slot[static_cast<size_t>(t)] = s;
+        ++sg;
+      }
+    }
+  }
+  for (int64_t T = 0; T < W; ++T)
+    if (own[static_cast<size_t>(T)] == -1) ++bad;  // never visited
+  // what fixup_kernel reads for every row block of the runs
+  for (int64_t rb = 0; rb < n_rb; ++rb) {
+    const int64_t lo = own[static_cast<size_t>(rb * n_kt)], hi = own[static_cast<size_t>(rb * n_kt + n_kt - 1)];
+    if (rb < p.full_rb) {
+      if (slot[static_cast<size_t>(rb * n_kt)] != -1) ++bad;  // whole-wave blocks are written whole
+      continue;
+    }
+    const int64_t tr = rb - p.full_rb;
+    const int64_t b_lo = eot::tr::run_owner(p, tr * n_kt), b_hi = eot::tr::run_owner(p, tr * n_kt + n_kt - 1);
+    if (b_lo != lo || b_hi != hi) ++bad;
+    for (int64_t kt = 0; kt < n_kt; ++kt) {
+      const size_t T = static_cast<size_t>(rb * n_kt + kt);
+      const int64_t want = b_lo == b_hi ? -1 : eot::tr::fixup_slot(p, own[T], tr);
+      if (slot[T] != want) ++bad;
+    }
+  }
+  if (owner != nullptr)
+    for (int64_t T = 0; T < W; ++T) owner[T] = own[static_cast<size_t>(T)];
+  return bad == 0 ? B4_OK : -bad;
+}
 
 extern "C" size_t eot_transport_workspace_bytes(int64_t n, int64_t m, int32_t d) {
   if (!eot::tr_sizes_ok(n, m, d, d)) return 0;

@@ -139,6 +139,22 @@ int eot_transport(const float *X, const float *Y, const float *f, const float *g
  * products, with no host synchronisation.
  * Workspace: eot_hvp_workspace_bytes(n, m, d), 256-byte aligned.  Errors as
  * for eot_update, and B4_EINVAL for cg_iters outside 0..100000. */
+/* Diagnostic (host only, no GPU needed): the transport kernel's work split
+ * of n_rb row blocks of n_kt key tiles over `ctas` CTAs, as used by
+ * eot_transport, eot_apply_plan and eot_hvp.  CTA b first takes whole row
+ * blocks b, b + ctas, ..., then an equal contiguous run of the remaining
+ * tiles.  The split is played on the host with the kernel's own tile walk
+ * and partial-slot rule and checked against the fix-up's slot rule:
+ *   - every tile is visited once;
+ *   - each row block is either one CTA's whole segment, or is split among
+ *     CTAs whose partial slots are the ones the fix-up sums;
+ *   - no slot holds two row blocks.
+ * owner [n_rb * n_kt] (row block major), or NULL, receives the CTA of each
+ * tile.  Returns B4_OK; B4_EINVAL unless n_rb >= 1, n_kt >= 1,
+ * 1 <= ctas <= min(256, n_rb n_kt) and n_rb n_kt <= 2^28; or minus the
+ * number of inconsistencies found. */
+int eot_transport_schedule(int64_t n_rb, int32_t n_kt, int32_t ctas, int64_t *owner);
+
 size_t eot_hvp_workspace_bytes(int64_t n, int64_t m, int32_t d);
 int eot_hvp(const float *X, const float *Y, const float *f, const float *g, const float *log_a,
             const float *log_b, const float *V, float *out, int64_t n, int64_t m, int32_t d,
