@@ -571,11 +571,13 @@ __device__ __forceinline__ float p_chunk(uint32_t (&v)[32], const float4* kb, fl
   return t.x + t.y;
 }
 
-// One CTA per SM.  The tiles T = row block * n_kt + key tile are cut into
-// one contiguous run per CTA (equal counts, so the last wave is full); a
-// run's tiles of one row block form a segment, and a segment that is not
-// the whole row block leaves its O and row masses in the CTA's partial
-// slots for fixup_kernel.  Warp roles:
+// One CTA per SM.  CTA b first takes whole row blocks b, b + G, ... (all
+// CTAs sweep the same key tiles together and share them in L2), then an
+// equal contiguous run of the remaining tiles T = row block * n_kt + key
+// tile, so that the last wave is full (TileWalk).  A CTA's tiles of one row
+// block form a segment; a segment that is not the whole row block leaves
+// its O and row masses in the CTA's partial slots for fixup_kernel.  Warp
+// roles:
 //   0      producer (lane 0): per tile the key biases (bulk copy, a ring of
 //          their own), and the operand ring in the order the MMA thread
 //          reads it: the K chunks of S(T) (query and key coordinates) and
@@ -587,8 +589,11 @@ __device__ __forceinline__ float p_chunk(uint32_t (&v)[32], const float4* kb, fl
 //          products of its neighbours; with one, P V(T - 1) goes first;
 //   2..9   epilogue: thread t of warp w owns query row 32 (w % 4) + t and key
 //          group (w - 2) / 4 (BN / 2 keys of each tile): p = 2^(S c1 + bias +
-//          rowterm) stored over its S columns in TMEM, the row mass, and at
-//          the end of a segment its chunks of O.
+//          rowterm) stored over its S columns in TMEM (as f16 pairs over
+//          their first half in the HALF mode), the row mass, and at the end
+//          of a segment its chunks of O.
+// HALF: VALUES with the f16 second product (scales and overflow flag: see
+// Mode).
 // MOMENT: the second-moment form used by the Hessian-vector product: with a
 // direction w_i per query, the weights become pi_ij (w_i . y_j), so O_i =
 // sum_j pi_ij (w_i . y_j) y_j.  A second MMA per K chunk (the packed
