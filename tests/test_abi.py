@@ -159,6 +159,31 @@ def test_eot_transport_arguments_are_checked(L):
               ws, need, None) == _lib.B4_EINVAL
 
 
+def test_eot_hvp_arguments_are_checked(L):
+    """Every check runs on the host before any CUDA call."""
+    f32 = ctypes.c_float
+    need = L.eot_hvp_workspace_bytes(100, 200, 16)
+    assert need > 0 and L.eot_hvp_workspace_bytes(100, 200, 0) == 0
+    ws = ctypes.c_void_p(0x100000)
+
+    def hvp(n=100, m=200, d=16, eps=0.1, it=10, w=ws, wb=need, v=FAKE, out=FAKE):
+        return L.eot_hvp(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, v, out, n, m, d, f32(eps), it, w, wb,
+                         None)
+
+    E = _lib.B4_EINVAL
+    assert hvp(eps=0.0) == E
+    assert hvp(eps=float("inf")) == E
+    assert hvp(it=-1) == E
+    assert hvp(it=100001) == E
+    assert hvp(d=0) == E
+    assert hvp(m=0) == E
+    assert hvp(v=None) == E
+    assert hvp(out=None) == E
+    assert hvp(w=ctypes.c_void_p(0x100040)) == E   # not 256-byte aligned
+    assert hvp(wb=need - 1) == E
+    assert hvp(n=0, w=None, out=None) == _lib.B4_OK  # nothing to do
+
+
 def test_bad_options_are_einval(L):
     def opts(**kw):
         o = _lib.Opts(in_dtype=0, out_dtype=0, max_evals=0, tol=0.0)
