@@ -281,6 +281,30 @@ def test_hvp_along_a_common_translation_sums_to_2t():
     assert np.abs(Hv.sum(0) - 2 * t).max() <= 1e-9
 
 
+def test_planted_hvp_cost_sign_mistake_fails():
+    """dC_ij built from (x_i + y_j).v_i instead of (x_i - y_j).v_i, carried
+    through the whole implicit solve, breaks the finite-difference pin."""
+    X, Y = clouds(5, 6, 2, seed=37)
+    la, lb = uniform(5), uniform(6)
+    eps, iters, h = 0.5, 4000, 1e-5
+    V = R(38).standard_normal(X.shape)
+    f, g = eot.sinkhorn64(X, Y, la, lb, eps, iters)
+    a, b = np.exp(la), np.exp(lb)
+    P = eot.plan64(X, Y, f, g, la, lb, eps)
+    dC = 2.0 * ((X * V).sum(1)[:, None] + V @ Y.T)  # the planted sign
+    A = np.block([[np.diag(a), P], [P.T, np.diag(b)]])
+    sol = np.linalg.lstsq(A, np.r_[(P * dC).sum(1), (P * dC).sum(0)], rcond=None)[0]
+    dP = P * (sol[:5][:, None] + sol[5:][None, :] - dC) / eps
+    bad = 2.0 * a[:, None] * V - 2.0 * dP @ Y
+
+    def grad(Xs):
+        fs, gs = eot.sinkhorn64(Xs, Y, la, lb, eps, iters)
+        return eot.grad_x64(Xs, Y, fs, gs, la, lb, eps)
+
+    fd = (grad(X + h * V) - grad(X - h * V)) / (2 * h)
+    assert np.abs(bad - fd).max() > 1e-2
+
+
 def test_planted_hvp_mistake_fails():
     """Dropping the implicit (df, dg) term breaks the finite-difference pin."""
     X, Y = clouds(5, 6, 2, seed=35)
