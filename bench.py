@@ -74,6 +74,52 @@ def recorded_traffic():
     return out
 
 
+ISSUE_FILE = os.path.join(ROOT, "profiles", "issue_counts.txt")
+
+
+def recorded_issue_counts():
+    """Warp instructions per 32 tokens of each kernel, from the committed ncu
+    summary, if it was taken on the current kernel sources (else {})."""
+    try:
+        lines = open(ISSUE_FILE).read().splitlines()
+    except OSError:
+        return {}
+    out, src = {}, None
+    for ln in lines:
+        parts = ln.split()
+        if len(parts) >= 2 and parts[0] == "kernel_source_hash":
+            src = parts[1]
+        if len(parts) >= 3 and parts[0] == "warp_inst_per_32_tokens":
+            out[parts[1]] = float(parts[2])
+    return out if src == kernel_source_hash() else {}
+
+
+def issue_ceiling(inst_per_32: float, nsm: int, sm_mhz: float) -> float:
+    """Tokens/s at which instruction issue alone would bind: every SM issues
+    one warp instruction per clock on each of its 4 schedulers."""
+    return nsm * 4 * sm_mhz * 1e6 * 32.0 / inst_per_32
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu or /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu model")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
 class ClockSampler:
     """nvidia-smi samples (200 ms) while the timed region runs."""
 
@@ -156,25 +202,126 @@ def whole_job_tokens_per_s(tokens_per_rank: int, world: int, steps: int, max_tot
     return world * tokens_per_rank * steps / (max_total_ms * 1e-3)
 
 
-def cpu_baseline(X_host, G_host, target_s: float = 12.0):
+def cpu_baseline(X_host, G_host, target_s: float = 12.0, single_s: float = 3.0):
     """The float64 oracle (Newton forward + implicit backward) on the host
-    cores, on a bounded prefix of the same tokens."""
+    cores, on a bounded prefix of the same tokens; then on one core."""
     import oracle
 
     oracle.build()
+
+    def timed(n):
+        t0 = time.perf_counter()
+        P = oracle.project64(X_host[:n])
+        oracle.backward64(P, G_host[:n])
+        return time.perf_counter() - t0
+
     n = 1 << 16
-    t0 = time.perf_counter()
-    P = oracle.project64(X_host[:n])
-    oracle.backward64(P, G_host[:n])
-    dt = time.perf_counter() - t0
+    dt = timed(n)
     n = int(min(X_host.shape[0], max(n, n * target_s / max(dt, 1e-3))))
-    t0 = time.perf_counter()
-    P = oracle.project64(X_host[:n])
-    oracle.backward64(P, G_host[:n])
-    dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+    dt = timed(n)
+    cores = oracle.num_threads()
+    prev = oracle.set_num_threads(1)
+    try:
+        n1 = 1 << 12
+        dt1 = timed(n1)
+        n1 = int(min(X_host.shape[0], max(n1, n1 * single_s / max(dt1, 1e-4))))
+        dt1 = timed(n1)
+    finally:
+        oracle.set_num_threads(prev)
+    return {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "single_core": {"value": n1 / dt1, "unit": "tokens/s", "cores": 1,
+                            "sample": "first %d tokens, %.1f s" % (n1, dt1)},
             "sample": "first %d tokens of the workload, float64 Newton forward + implicit "
                       "backward, %.1f s" % (n, dt)}
+
+
+def evals_stats(b4, X):
+    """Mean evaluations per token and the mean over consecutive 32-token
+    groups of their maximum (what one warp of one-token-per-thread lanes
+    waits for), from the kernel's own per-token counts."""
+    _, ev, nonconv = b4.forward(X, return_stats=True)
+    T = ev.numel() // 32 * 32
+    wmax = ev.reshape(-1)[:T].reshape(-1, 32).amax(1).float().mean()
+    return {"mean_evals": float(ev.float().mean()), "warp32_max_evals": float(wmax),
+            "nonconverged": int(nonconv.item())}
+
+
+def hard_configs(b4, workloads, dev, X, G, P, dX, peak, reps=10):
+    """Device times of the other workloads beside the headline (inputs
+    resident; each larger than L2 or rotated over copies that are):
+    the fused fp32 pass and 20-iteration Sinkhorn-Knopp on the headline
+    tokens; forward and forward + backward at T = 2^26, sigma = 10; the
+    large-magnitude workload (2^20 tokens); the bf16 mHC batch (2^24)."""
+    import torch
+
+    T = X.shape[0]
+    out = {}
+    tf = time_device(lambda i: b4._fused_pass(X, G, P, dX), reps, dev)
+    out["fused_f32_sigma1"] = {"tokens": T, "ms": tf, "tokens_per_s": T / (tf * 1e-3),
+                               "gbs": 256 * T / (tf * 1e-3) / 1e9,
+                               "hbm_frac": 256 * T / (tf * 1e-3) / 1e9 / peak,
+                               "bytes_per_token": 256}
+    ts = time_device(lambda i: b4.sinkhorn(X, 20, out=P), reps, dev)
+    tfw = time_device(lambda i: b4.forward(X, out=P), reps, dev)
+    out["sinkhorn20_f32_sigma1"] = {"tokens": T, "ms": ts, "tokens_per_s": T / (ts * 1e-3),
+                                    "newton_forward_ms": tfw,
+                                    "gbs": 128 * T / (ts * 1e-3) / 1e9}
+    # sigma = 10 at the same size
+    X10, G10 = workloads.sweep(T.bit_length() - 1, 10.0, device=dev)
+    f10 = time_device(lambda i: b4.forward(X10, out=P), reps, dev)
+
+    def fb10(i):
+        b4.forward(X10, out=P)
+        b4.backward(G10, P=P, out=dX)
+
+    fb = time_device(fb10, reps, dev)
+    st = evals_stats(b4, X10)
+    bound_f = 128 * T / (peak * 1e9) * 1e3
+    bound_fb = 320 * T / (peak * 1e9) * 1e3
+    out["sigma10"] = dict(st, tokens=T, fwd_ms=f10, fwd_bwd_ms=fb,
+                          fwd_tokens_per_s=T / (f10 * 1e-3), fwd_bwd_tokens_per_s=T / (fb * 1e-3),
+                          fwd_hbm_frac=bound_f / f10, fwd_bwd_hbm_frac=bound_fb / fb)
+    del X10, G10
+    # large magnitude, 2^20 tokens (67 MB per tensor): four copies rotate
+    X3, G3 = workloads.large_magnitude(device=dev)
+    sets = [(X3.clone(), G3.clone(), torch.empty_like(X3), torch.empty_like(X3)) for _ in range(4)]
+    T3 = X3.shape[0]
+    f3 = time_device(lambda i: b4.forward(sets[i % 4][0], out=sets[i % 4][2]), 4 * reps, dev)
+
+    def fb3(i):
+        x, g, p, d = sets[i % 4]
+        b4.forward(x, out=p)
+        b4.backward(g, P=p, out=d)
+
+    fb3t = time_device(fb3, 4 * reps, dev)
+    out["large_magnitude"] = dict(evals_stats(b4, X3), tokens=T3, fwd_ms=f3, fwd_bwd_ms=fb3t,
+                                  fwd_tokens_per_s=T3 / (f3 * 1e-3),
+                                  fwd_bwd_tokens_per_s=T3 / (fb3t * 1e-3),
+                                  fwd_hbm_frac=128 * T3 / (f3 * 1e-3) / 1e9 / peak,
+                                  fwd_bwd_hbm_frac=320 * T3 / (fb3t * 1e-3) / 1e9 / peak,
+                                  input_sets=4)
+    del sets, X3, G3
+    # bf16 mHC batch, 2^24 tokens (537 MB per tensor)
+    Xb, Gb = workloads.mhc_batch(device=dev)
+    Tb = Xb.numel() // 16
+    Pb, dXb = torch.empty_like(Xb), torch.empty_like(Xb)
+    tfu = time_device(lambda i: b4._fused_pass(Xb, Gb, Pb, dXb), reps, dev)
+
+    def sepb(i):
+        b4.forward(Xb, out=Pb)
+        b4.backward(Gb, P=Pb, out=dXb)
+
+    tsep = time_device(sepb, reps, dev)
+    tfb = time_device(lambda i: b4.forward(Xb, out=Pb), reps, dev)
+    out["mhc_bf16"] = dict(evals_stats(b4, Xb.reshape(Tb, 4, 4)), tokens=Tb, fused_ms=tfu,
+                           fused_tokens_per_s=Tb / (tfu * 1e-3),
+                           fused_hbm_frac=128 * Tb / (tfu * 1e-3) / 1e9 / peak,
+                           separate_ms=tsep, separate_hbm_frac=160 * Tb / (tsep * 1e-3) / 1e9 / peak,
+                           fwd_ms=tfb, fwd_hbm_frac=64 * Tb / (tfb * 1e-3) / 1e9 / peak)
+    del Xb, Gb, Pb, dXb
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_reference(args):
@@ -222,8 +369,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--log2-tokens", type=int, default=LOG2_T)
+    ap.add_argument("--sigma", type=float, default=SIGMA,
+                    help="logit scale of the timed workload (the headline is sigma = 1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-hard", action="store_true",
+                    help="skip the other workloads' device times (sigma 10, large magnitude, bf16 mHC, "
+                         "fused fp32, Sinkhorn-20)")
     ap.add_argument("--sweep", action="store_true",
                     help="throughput sweep T = 2^12..2^26, sigma 1 and 10 (one JSON line each)")
     ap.add_argument("--mhc", action="store_true",
@@ -263,7 +415,7 @@ def main():
     torch.cuda.set_device(dev)
     warmup = max(args.warmup, 3)
 
-    X, G = workloads.sweep(args.log2_tokens, SIGMA, device=dev, shard=rank)
+    X, G = workloads.sweep(args.log2_tokens, args.sigma, device=dev, shard=rank)
     T = X.shape[0]
     P = torch.empty_like(X)
     dX = torch.empty_like(X)
@@ -333,8 +485,9 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "sweep T=2^%d sigma=1 fp32, forward + backward" % args.log2_tokens,
-                   "tokens_per_gpu": T, "sigma": SIGMA,
+        "config": {"workload": "sweep T=2^%d sigma=%g fp32, forward + backward"
+                               % (args.log2_tokens, args.sigma),
+                   "tokens_per_gpu": T, "sigma": args.sigma,
                    "l2": "inputs larger than L2 (%.1f GB per tensor, L2 129 MB)" % (T * 64 / 1e9)},
         "fwd": {"tokens_per_s": world * T / (fwd_avg * 1e-3), "ms": fwd_avg, "gbs": fwd_gbs,
                 "hbm_frac": fwd_gbs / peak, "mean_evals": mean_evals,
@@ -365,6 +518,17 @@ def main():
         best["link_ceiling"] = ceiling
         best["link_frac"] = best["host_link_gbs"] / ceiling["both_gbs"]
         line["e2e"] = best
+    if not args.no_hard:
+        line["hard_configs"] = hard_configs(b4, workloads, dev, X, G, P, dX, peak)
+    counts = recorded_issue_counts()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_mhz") or 2070.0
+    line["issue_ceiling"] = {
+        k: {"warp_inst_per_32_tokens": v, "ceiling_tokens_per_s": issue_ceiling(v, nsm, mhz)}
+        for k, v in counts.items()} or None
+    if counts.get("forward_f32_sigma1"):
+        ic = line["issue_ceiling"]["forward_f32_sigma1"]
+        ic["achieved_frac"] = (T / (fwd_avg * 1e-3)) / ic["ceiling_tokens_per_s"]
     if not args.no_cpu_baseline:
         idx = slice(0, 1 << 22)
         line["cpu_baseline"] = cpu_baseline(X[idx].double().cpu().numpy(),

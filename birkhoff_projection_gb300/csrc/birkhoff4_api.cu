@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "b4_context.cuh"
 #include "b4_device.cuh"
 #include "b4_types.h"
 #include "birkhoff4.h"
@@ -28,18 +29,12 @@ int cuda_status(cudaError_t e) {
   return B4_ECUDA;
 }
 
-// Device address of g_fault_latch for the current device (cached).
+// Device address of g_fault_latch on the current device (cached per device
+// and context).
 unsigned int* fault_latch(cudaError_t* err) {
-  static std::atomic<unsigned int*> cache[64];
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  unsigned int* p = cache[dev].load(std::memory_order_acquire);
-  if (p != nullptr) return p;
-  *err = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_fault_latch);
-  if (*err != cudaSuccess) return nullptr;
-  cache[dev].store(p, std::memory_order_release);
-  return p;
+  static SymbolCache cache;
+  return static_cast<unsigned int*>(cached_symbol_address(
+      cache, [](void** q) { return cudaGetSymbolAddress(q, g_fault_latch); }, err));
 }
 
 bool dtype_ok(int32_t d) { return d == B4_F32 || d == B4_BF16; }

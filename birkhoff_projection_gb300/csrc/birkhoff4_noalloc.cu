@@ -6,13 +6,15 @@
 // cudaMalloc because it synchronises the device (latency-critical loops), code
 // whose device memory belongs to another framework's allocator or pool, and
 // plugins or sandboxed hosts where creating device allocations is not
-// allowed.  The array is reserved once per GPU when the library's module
-// loads on it and stays reserved until the process exits.
+// allowed.  The array belongs to this library's module.  With CUDA's lazy
+// module loading the module is loaded on a device by the first call there,
+// which reserves the array (and may synchronise); it then stays reserved
+// until the process exits.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstdint>
 
+#include "b4_context.cuh"
 #include "birkhoff4.h"
 
 namespace b4 {
@@ -26,26 +28,13 @@ static __device__ __align__(256) unsigned char g_static_scratch[B4_STATIC_SCRATC
 
 namespace {
 
-// Device address of g_static_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+// Device address of g_static_scratch on the current device, looked up with
+// that device current and cached per device and context (a reset or another
+// context makes it look the address up again).
 unsigned char* static_scratch_address(cudaError_t* err) {
-  static std::atomic<unsigned char*> cache[64];
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= 64) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
-  unsigned char* p = cache[dev].load(std::memory_order_acquire);
-  if (p != nullptr) return p;
-  void* q = nullptr;
-  *err = cudaGetSymbolAddress(&q, g_static_scratch);
-  if (*err == cudaSuccess && q == nullptr) *err = cudaErrorInvalidSymbol;
-  if (*err != cudaSuccess) return nullptr;
-  p = static_cast<unsigned char*>(q);
-  cache[dev].store(p, std::memory_order_release);
-  return p;
+  static SymbolCache cache;
+  return static_cast<unsigned char*>(cached_symbol_address(
+      cache, [](void** q) { return cudaGetSymbolAddress(q, g_static_scratch); }, err));
 }
 
 }  // namespace
@@ -65,7 +54,17 @@ extern "C" int birkhoff4_forward_backward_host_static(const void* X_h, const voi
   if (chunk < 1 || chunk > fit) return B4_ESCRATCH;
   if (T == 0) return B4_OK;
   if (X_h == nullptr || dP_h == nullptr || dX_h == nullptr || streams == nullptr) return B4_EINVAL;
-  cudaError_t err = cudaSuccess;
+  // Every stream must belong to the current device, whose array is used:
+  // checked before anything is enqueued.
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return b4::record_cuda_error(err);
+  for (int32_t k = 0; k < nstreams; ++k) {
+    int sdev = -1;
+    err = cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(streams[k]), &sdev);
+    if (err != cudaSuccess) return b4::record_cuda_error(err);
+    if (sdev != dev) return B4_EINVAL;
+  }
   unsigned char* scratch = b4::static_scratch_address(&err);
   if (scratch == nullptr) return b4::record_cuda_error(err);
   // The staging slots are written in full by the copies in before anything

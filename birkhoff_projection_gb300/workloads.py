@@ -68,6 +68,18 @@ def large_magnitude(T: int = 1 << 20, device="cpu"):
     return x, dp
 
 
+def large_magnitude_n(n: int, T: int, seed: int, device="cpu"):
+    """(X, dP) for n x n tokens with the large-magnitude recipe:
+    X_ij = 20 Z_ij + r_i + c_j, r, c ~ U[-50, 50] per token; dP iid N(0,1)."""
+    g = _gen(seed, device)
+    z = torch.randn(T, n, n, generator=g, device=device, dtype=torch.float32)
+    r = torch.rand(T, n, 1, generator=g, device=device, dtype=torch.float32) * 100.0 - 50.0
+    c = torch.rand(T, 1, n, generator=g, device=device, dtype=torch.float32) * 100.0 - 50.0
+    x = 20.0 * z + r + c
+    dp = torch.randn(T, n, n, generator=g, device=device, dtype=torch.float32)
+    return x, dp
+
+
 MHC_SHAPE = (64, 32, 8192)
 
 

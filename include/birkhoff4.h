@@ -196,21 +196,27 @@ int birkhoff4_forward_backward_host(const void *X_h, const void *dP_h, void *P_h
 /*                                                                        */
 /* Arguments and results as birkhoff4_forward_backward_host, except that   */
 /* the staging area is a static device array of B4_STATIC_SCRATCH_BYTES    */
-/* (32 MiB) inside the library, reserved on every GPU the library is       */
-/* loaded on until the process exits.  chunk_tokens: tokens per chunk; 0   */
-/* takes the largest chunk that fits (32 MiB / (nstreams * 4 * row bytes), */
-/* e.g. 65536 fp32 tokens with 2 streams).  A chunk that does not fit      */
-/* returns B4_ESCRATCH; T itself is not limited (the call loops over       */
-/* chunks).  The first call on a device looks up the array's device        */
-/* address (cudaGetSymbolAddress, with that device current): make it       */
-/* before any stream capture.  Apart from that one-time lookup the call    */
-/* only enqueues copies and kernels; it never calls cudaMalloc, cudaFree   */
-/* or any other allocating routine.  Every call uses the same array:       */
-/* calls whose work overlaps on the GPU (concurrent streams, or a second   */
-/* call before the first call's streams have finished) race on it, so      */
-/* order them (for example by reusing the same streams).  Nothing in the   */
-/* array needs to start at zero: every staging slot is filled by a copy    */
-/* before it is read.                                                      */
+/* (32 MiB) inside the library.  chunk_tokens: tokens per chunk; 0 takes  */
+/* the largest chunk that fits (32 MiB / (nstreams * 4 * row bytes), e.g.  */
+/* 65536 fp32 tokens with 2 streams).  A chunk that does not fit returns   */
+/* B4_ESCRATCH; T itself is not limited (the call loops over chunks).      */
+/* Every stream must belong to the current device (else B4_EINVAL, before  */
+/* anything is enqueued).                                                  */
+/* First call on a device: it looks up the array's device address          */
+/* (cudaGetSymbolAddress, with that device current).  With CUDA's lazy     */
+/* module loading (the default) that lookup loads the library's module on  */
+/* the device, which reserves the 32 MiB there and may synchronise the     */
+/* device; the array then stays reserved until the process exits.  Make   */
+/* one warm-up call before latency-critical work and before any stream     */
+/* capture.  The address is cached per device and CUDA context and looked  */
+/* up again after a context change (cudaDeviceReset included).  Apart from */
+/* that lookup the call only enqueues copies and kernels; it never calls   */
+/* cudaMalloc, cudaFree or any other allocating routine.  Every call uses  */
+/* the same array: calls whose work overlaps on the GPU (concurrent        */
+/* streams, or a second call before the first call's streams have         */
+/* finished) race on it, so order them (for example by reusing the same    */
+/* streams).  Nothing in the array needs to start at zero: every staging   */
+/* slot is filled by a copy before it is read.                             */
 /* ---------------------------------------------------------------------- */
 #define B4_STATIC_SCRATCH_BYTES (32ull << 20)
 int birkhoff4_forward_backward_host_static(const void *X_h, const void *dP_h, void *P_h,

@@ -84,6 +84,8 @@ def _load():
         lib.oracle_backward64_n.argtypes = [dp, dp, dp, i32, i64]
         lib.oracle_backward64_n.restype = None
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = None
         lib.oracle_version.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -108,6 +110,14 @@ def _tokens(X) -> np.ndarray:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Use n threads in later calls; returns the previous count."""
+    lib = _load()
+    prev = int(lib.oracle_num_threads())
+    lib.oracle_set_num_threads(int(n))
+    return prev
 
 
 def sinkhorn64(X, tol: float = 1e-13, max_iters: int = 20000):

@@ -61,6 +61,16 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads used by later calls (the CPU baseline times one core and all). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* log(sum_k exp(v[k])) for four values, shifted by the maximum. */
 static double lse4(double v0, double v1, double v2, double v3)
 {

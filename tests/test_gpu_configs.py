@@ -129,3 +129,28 @@ def test_sweep(log2_T, sigma):
     Pst, dXst = oracle_forward_backward(Xs, Gs)
     assert max_abs_err(np64(Ps), Pst) <= tol_p
     assert rel_fro(np64(dXs), dXst) <= TOL_DX_REL
+
+
+def test_sk20_accuracy_table():
+    """The accuracy comparison of 20-iteration Sinkhorn-Knopp and Newton
+    (tests/sk20_accuracy_table.py): the Newton forward is within the parity
+    tolerances on every workload, and the fixed-iteration scheme's median
+    error grows with the logits' magnitude, as the pages state (fine at
+    N(0,1), at least 100x the Newton median at N(0,10^2) and on the
+    large-magnitude workload)."""
+    from sk20_accuracy_table import accuracy_table
+
+    rows = accuracy_table(DEV)
+    by = {(r["workload"], r["method"].split(",")[0].split(" (")[0]): r for r in rows}
+    for (wl, method), r in by.items():
+        if method == "GPU Newton":
+            large = "N(0,10^2)" in wl or "large" in wl
+            assert r["err"][2] <= (TOL_P_LARGE if large else TOL_P_SMALL)
+            assert r["res"][2] <= (TOL_RES_LARGE if large else TOL_RES_SMALL)
+    for wl in {w for w, _ in by}:
+        newton = by[(wl, "GPU Newton")]["err"][0]
+        sk = by[(wl, "GPU Sinkhorn-Knopp")]["err"][0]
+        if "N(0,10^2)" in wl or "large" in wl:
+            assert sk >= 100 * max(newton, 1e-9)
+        else:
+            assert sk <= 1e-3

@@ -91,3 +91,49 @@ def test_autograd_and_in_place():
     b4.forward_nxn(Y, out=Y)
     assert torch.equal(Y, P.detach())
 
+
+
+def _oracle_rows(X, G, idx):
+    x = X[idx].double().cpu().numpy()
+    g = G[idx].double().cpu().numpy()
+    Pst = oracle.newton64_n(x)[0]
+    return Pst, oracle.backward64_n(Pst, g)
+
+
+@pytest.mark.parametrize("n", [3, 5, 8])
+def test_many_tiles_per_cta(n):
+    """2^20 + 77 tokens: the persistent grid is at most 152 SMs x 16 CTAs of
+    128 tokens (forward) or 152 x 32 CTAs of 64 tokens (backward), so every
+    CTA strides over at least three tiles and the last tile is ragged.
+    Device residual on every token; the oracle on a 2^17-token random
+    sample plus the last 4096 tokens."""
+    T = (1 << 20) + 77
+    X = tokens(n, T, 1.0, seed=300 + n)
+    G = tokens(n, T, 1.0, seed=400 + n)
+    P = b4.forward_nxn(X)
+    dX = b4.backward_nxn(G, P=P)
+    p = P.double()
+    res = torch.maximum((p.sum(2) - 1).abs().amax(1), (p.sum(1) - 1).abs().amax(1))
+    assert float(res.max()) <= 2e-6
+    gsel = torch.Generator(device="cpu").manual_seed(n)
+    idx = torch.cat([torch.randperm(T - 4096, generator=gsel)[: 1 << 17],
+                     torch.arange(T - 4096, T)]).to(DEV)
+    Pst, dXst = _oracle_rows(X, G, idx)
+    assert max_abs_err(P[idx].double().cpu().numpy(), Pst) <= 1e-5
+    assert rel_fro(dX[idx].double().cpu().numpy(), dXst) <= TOL_DX_REL
+
+
+@pytest.mark.parametrize("n", [3, 5, 8])
+def test_large_magnitude_nxn(n):
+    """X_ij = 20 Z_ij + r_i + c_j with offsets U[-50, 50] (|X| up to about
+    200): the large-magnitude tolerance class (1e-4 on P and on the
+    marginals), every token against the oracle."""
+    X, G = workloads.large_magnitude_n(n, 20000, seed=500 + n, device=DEV)
+    P = b4.forward_nxn(X)
+    dX = b4.backward_nxn(G, P=P)
+    Pst = oracle.newton64_n(X.double().cpu().numpy())[0]
+    dXst = oracle.backward64_n(Pst, G.double().cpu().numpy())
+    Pg = P.double().cpu().numpy()
+    assert max_abs_err(Pg, Pst) <= 1e-4
+    assert residual(Pg).max() <= 1e-4
+    assert rel_fro(dX.double().cpu().numpy(), dXst) <= TOL_DX_REL

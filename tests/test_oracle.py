@@ -357,3 +357,62 @@ def test_planted_mistakes_are_caught():
     z = X - b[:, None, :]
     e = np.exp(z - z.max(axis=2, keepdims=True))
     assert np.abs(e / e.sum(axis=2, keepdims=True) - Pn).max() > 1e-3
+
+
+# --------------------------------------------------------------------------
+# the Hessian solve exported by the oracle ("Accelerating the Birkhoff
+# Projection for Manifold-Constrained Hyper-Connections", s2.1: the 3x3 system
+# of the reduced dual), against an LU solve of the explicitly assembled matrix
+# --------------------------------------------------------------------------
+EDGES = [(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)]
+
+
+def grounded_laplacian(w):
+    """3x3 matrix of the Laplacian with edge weights w (node 3 grounded):
+    H_jj = sum of the weights of the edges at j, H_jk = -w_jk."""
+    H = np.zeros((len(w), 4, 4))
+    for e, (a, b) in enumerate(EDGES):
+        H[:, a, b] -= w[:, e]
+        H[:, b, a] -= w[:, e]
+        H[:, a, a] += w[:, e]
+        H[:, b, b] += w[:, e]
+    return H[:, :3, :3]
+
+
+def test_laplacian_solve_matches_lu_solve():
+    r = rng(19)
+    n = 4000
+    # weights over many decades (nearly disconnected graphs included)
+    w = 10.0 ** r.uniform(-6, 1, (n, 6))
+    rhs = r.standard_normal((n, 3))
+    x = oracle.laplacian_solve64(w, rhs)
+    H = grounded_laplacian(w)
+    want = np.linalg.solve(H, rhs[..., None])[..., 0]
+    cond = np.linalg.cond(H)
+    err = np.abs(x - want).max(1) / np.abs(want).max(1)
+    assert np.all(err <= 1e-13 * cond)
+    # the residual of the oracle's own solution, in the assembled matrix
+    res = np.abs(np.einsum("tjk,tk->tj", H, x) - rhs).max(1)
+    assert np.all(res <= 1e-12 * (np.abs(H).max((1, 2)) * np.abs(x).max(1) + np.abs(rhs).max(1)))
+    # the Hessian of a token: H = diag(colsum P) - P^T P on columns 0..2,
+    # whose edge weights are w_jk = sum_i p_ij p_ik (rows of P sum to one)
+    X = r.standard_normal((200, 4, 4))
+    P = oracle.newton64(X)[0]
+    wp = np.stack([(P[:, :, a] * P[:, :, b]).sum(1) for a, b in EDGES], 1)
+    Hp = (np.eye(4)[None] * P.sum(1)[:, None, :] - np.einsum("tij,tik->tjk", P, P))[:, :3, :3]
+    g = r.standard_normal((200, 3))
+    assert np.abs(oracle.laplacian_solve64(wp, g) - np.linalg.solve(Hp, g[..., None])[..., 0]).max() <= 1e-11
+    # a disconnected graph (all weights zero) has no solution: NaN, counted
+    z = oracle.laplacian_solve64(np.zeros((1, 6)), np.ones((1, 3)))
+    assert np.isnan(z).all()
+
+
+def test_laplacian_solve_planted_mistake():
+    """A transposed edge order (the (0,3) and (1,2) weights exchanged)
+    fails the LU pin."""
+    r = rng(20)
+    w = 10.0 ** r.uniform(-2, 1, (500, 6))
+    rhs = r.standard_normal((500, 3))
+    want = np.linalg.solve(grounded_laplacian(w), rhs[..., None])[..., 0]
+    bad = oracle.laplacian_solve64(w[:, [0, 1, 3, 2, 4, 5]], rhs)
+    assert np.abs(bad - want).max() > 1e-3
