@@ -34,8 +34,8 @@ BYTES_FWD_F32 = 128  # X read + P written per token
 BYTES_BWD_F32 = 192  # P, dP read + dX written per token
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["b4_device.cuh", "b4_math.cuh", "b4_kernels.cuh", "b4_launch.cuh", "b4_types.h",
-                  "k_forward.cu", "k_backward.cu"]
+KERNEL_SOURCES = ["b4_device.cuh", "b4_math.cuh", "b4_kernels.cuh", "b4_queue.cuh", "b4_launch.cuh",
+                  "b4_types.h", "k_forward.cu", "k_backward.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
@@ -369,6 +369,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--log2-tokens", type=int, default=LOG2_T)
+    ap.add_argument("--schedule", choices=["default", "queue", "lane"], default="default",
+                    help="token schedule of the Newton passes (birkhoff4_opts.schedule)")
     ap.add_argument("--sigma", type=float, default=SIGMA,
                     help="logit scale of the timed workload (the headline is sigma = 1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -424,7 +426,7 @@ def main():
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        b4.forward(X, out=P)
+        b4.forward(X, out=P, schedule=args.schedule)
         if ev is not None:
             ev[1].record(stream)
         b4.backward(G, P=P, out=dX)
@@ -432,7 +434,7 @@ def main():
             ev[2].record(stream)
 
     # evaluation counts of this input (outside the timed region)
-    _, evals, nonconv = b4.forward(X, return_stats=True)
+    _, evals, nonconv = b4.forward(X, return_stats=True, schedule=args.schedule)
     mean_evals = float(evals.float().mean())
     del evals
     torch.cuda.synchronize(dev)

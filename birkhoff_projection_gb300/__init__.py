@@ -69,13 +69,18 @@ class _on_device:
             self.ctx.__exit__(*exc)
 
 
+_SCHED = {"default": _lib.B4_SCHED_DEFAULT, "queue": _lib.B4_SCHED_QUEUE, "lane": _lib.B4_SCHED_LANE}
+
+
 def forward(X: torch.Tensor, *, out: torch.Tensor = None, out_dtype=None, return_dual: bool = False,
-            tol: float = 0.0, max_evals: int = 0, return_stats: bool = False):
+            tol: float = 0.0, max_evals: int = 0, return_stats: bool = False,
+            schedule: str = "default"):
     """Projection of every token of X ([..., 4, 4], fp32 or bf16).
 
     Returns P (dtype out_dtype, default X.dtype), plus b ([..., 4] fp32,
     natural-log column dual, b[..., 3] = 0) if return_dual, plus
-    (evals [...] int32, nonconverged count) if return_stats."""
+    (evals [...] int32, nonconverged count) if return_stats.  schedule:
+    "default", "queue" or "lane" (birkhoff4_schedule)."""
     T = _check_tokens(X, "X")
     odt = out_dtype or X.dtype
     if out is None:
@@ -85,7 +90,8 @@ def forward(X: torch.Tensor, *, out: torch.Tensor = None, out_dtype=None, return
         if out.shape != X.shape or out.dtype != odt or out.device != X.device:
             raise ValueError("out does not match X")
     b = torch.empty(X.shape[:-1], dtype=torch.float32, device=X.device) if return_dual else None
-    opts = Opts(in_dtype=_DT[X.dtype], out_dtype=_DT[odt], max_evals=int(max_evals), tol=float(tol))
+    opts = Opts(in_dtype=_DT[X.dtype], out_dtype=_DT[odt], max_evals=int(max_evals), tol=float(tol),
+                schedule=_SCHED[schedule])
     evals = nonconv = None
     if return_stats:
         evals = torch.empty(X.shape[:-2], dtype=torch.int32, device=X.device)
@@ -137,13 +143,14 @@ def forward_backward(X: torch.Tensor, dP: torch.Tensor, *, want_P: bool = True):
     return P, dX
 
 
-def _fused_pass(X, dP, P, dX):
+def _fused_pass(X, dP, P, dX, schedule: str = "default"):
     """The fused pass into preallocated outputs (P may be None)."""
     T = _check_tokens(X, "X")
-    fn = (lib().birkhoff4_forward_backward if X.dtype == torch.float32
-          else lib().birkhoff4_forward_backward_bf16)
+    opts = Opts(in_dtype=_DT[X.dtype], out_dtype=_DT[X.dtype], schedule=_SCHED[schedule])
     with _on_device(X):
-        check(fn(_ptr(X), _ptr(dP), _ptr(P), _ptr(dX), T, _stream(X)), "birkhoff4_forward_backward")
+        check(lib().birkhoff4_forward_backward_ex(_ptr(X), _ptr(dP), _ptr(P), _ptr(dX), T,
+                                                  ctypes.byref(opts), _stream(X)),
+              "birkhoff4_forward_backward_ex")
 
 
 def sinkhorn(X: torch.Tensor, iters: int = 20, *, out: torch.Tensor = None) -> torch.Tensor:

@@ -16,6 +16,7 @@ _lib = None
 
 B4_OK, B4_EINVAL, B4_ECUDA, B4_ENOTIMPL, B4_ESCRATCH = 0, 1, 2, 3, 4
 B4_F32, B4_BF16 = 0, 1
+B4_SCHED_DEFAULT, B4_SCHED_QUEUE, B4_SCHED_LANE = 0, 1, 2
 
 # Every function the header declares, with its ctypes signature.
 _vp = ctypes.c_void_p
@@ -29,6 +30,7 @@ SIGNATURES = {
     "birkhoff4_backward_bf16": (_int, [_vp, _vp, _vp, _vp, _i64, _vp]),
     "birkhoff4_forward_backward": (_int, [_vp, _vp, _vp, _vp, _i64, _vp]),
     "birkhoff4_forward_backward_bf16": (_int, [_vp, _vp, _vp, _vp, _i64, _vp]),
+    "birkhoff4_forward_backward_ex": (_int, [_vp, _vp, _vp, _vp, _i64, _vp, _vp]),
     "birkhoff4_forward_backward_host": (_int, [_vp, _vp, _vp, _vp, _i64, ctypes.c_int32, _vp,
                                                ctypes.c_size_t, _vp, ctypes.c_int32]),
     "birkhoff4_forward_backward_host_static": (_int, [_vp, _vp, _vp, _vp, _i64, ctypes.c_int32,
@@ -72,6 +74,7 @@ class Opts(ctypes.Structure):
         ("tol", ctypes.c_float),
         ("evals_out", ctypes.c_void_p),
         ("nonconv_count", ctypes.c_void_p),
+        ("schedule", ctypes.c_int32),
     ]
 
 

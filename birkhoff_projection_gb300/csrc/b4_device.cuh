@@ -136,6 +136,11 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Prefetch [addr, addr + bytes) of global memory into L2 (addr 16-byte
+// aligned, bytes a multiple of 16); nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* addr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
 // Make this thread's generic-proxy shared-memory writes visible to the TMA
 // (async proxy) before a bulk store reads them.
 __device__ __forceinline__ void fence_async_smem() {
@@ -183,6 +188,22 @@ struct TileIO<float> {
       *reinterpret_cast<float4*>(row + 16 * (k ^ sw)) =
           make_float4(v[2 * k].x, v[2 * k].y, v[2 * k + 1].x, v[2 * k + 1].y);
   }
+  // One row from / to global memory with 16-byte accesses (base 16-byte
+  // aligned; rows are 64 bytes).
+  __device__ __forceinline__ static void gload_vec(const void* base, int64_t t, float2 v[8]) {
+    const float4* p = static_cast<const float4*>(base) + 4 * t;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 c = __ldg(p + k);
+      v[2 * k] = make_float2(c.x, c.y);
+      v[2 * k + 1] = make_float2(c.z, c.w);
+    }
+  }
+  __device__ __forceinline__ static void gstore_vec(void* base, int64_t t, const float2 v[8]) {
+    float4* p = static_cast<float4*>(base) + 4 * t;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) p[k] = make_float4(v[2 * k].x, v[2 * k].y, v[2 * k + 1].x, v[2 * k + 1].y);
+  }
   // Unaligned global fallback: plain element loads/stores.
   __device__ __forceinline__ static void gload(const void* base, int64_t t, float2 v[8]) {
     const float* p = static_cast<const float*>(base) + 16 * t;
@@ -225,6 +246,26 @@ struct TileIO<bf16_t> {
       *reinterpret_cast<uint4*>(row + 16 * (k ^ sw)) =
           make_uint4(pack_bf16(v[4 * k].x, v[4 * k].y), pack_bf16(v[4 * k + 1].x, v[4 * k + 1].y),
                      pack_bf16(v[4 * k + 2].x, v[4 * k + 2].y), pack_bf16(v[4 * k + 3].x, v[4 * k + 3].y));
+  }
+  // One row from / to global memory with 16-byte accesses (base 16-byte
+  // aligned; rows are 32 bytes).
+  __device__ __forceinline__ static void gload_vec(const void* base, int64_t t, float2 v[8]) {
+    const uint4* p = static_cast<const uint4*>(base) + 2 * t;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint4 c = __ldg(p + k);
+      v[4 * k + 0] = make_float2(bf16lo(c.x), bf16hi(c.x));
+      v[4 * k + 1] = make_float2(bf16lo(c.y), bf16hi(c.y));
+      v[4 * k + 2] = make_float2(bf16lo(c.z), bf16hi(c.z));
+      v[4 * k + 3] = make_float2(bf16lo(c.w), bf16hi(c.w));
+    }
+  }
+  __device__ __forceinline__ static void gstore_vec(void* base, int64_t t, const float2 v[8]) {
+    uint4* p = static_cast<uint4*>(base) + 2 * t;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      p[k] = make_uint4(pack_bf16(v[4 * k].x, v[4 * k].y), pack_bf16(v[4 * k + 1].x, v[4 * k + 1].y),
+                        pack_bf16(v[4 * k + 2].x, v[4 * k + 2].y), pack_bf16(v[4 * k + 3].x, v[4 * k + 3].y));
   }
   __device__ __forceinline__ static void gload(const void* base, int64_t t, float2 v[8]) {
     const unsigned short* p = static_cast<const unsigned short*>(base) + 16 * t;

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "b4_kernels.cuh"
+#include "b4_queue.cuh"
 
 namespace b4 {
 
@@ -32,6 +33,9 @@ namespace b4 {
 #ifndef B4_FWD_MINB
 #define B4_FWD_MINB 1
 #endif
+#ifndef B4_FUSED_MINB
+#define B4_FUSED_MINB 6
+#endif
 #ifndef B4_BWD_TILE
 #define B4_BWD_TILE 256
 #endif
@@ -43,6 +47,30 @@ namespace b4 {
 #endif
 #ifndef B4_BWD_MINB
 #define B4_BWD_MINB 1
+#endif
+// Compacting schedule of the Newton passes (b4_queue.cuh): warps per CTA,
+// TMA stages, queue entries per warp, evaluations of a fresh round and of a
+// resume round, minimum resident CTAs per SM.
+#ifndef B4_Q_WARPS
+#define B4_Q_WARPS 4
+#endif
+#ifndef B4_Q_NSTAGE
+#define B4_Q_NSTAGE 2
+#endif
+#ifndef B4_Q_QC
+#define B4_Q_QC 64
+#endif
+#ifndef B4_Q_K1
+#define B4_Q_K1 6
+#endif
+#ifndef B4_Q_K2
+#define B4_Q_K2 2
+#endif
+#ifndef B4_Q_MINB_FWD
+#define B4_Q_MINB_FWD 8
+#endif
+#ifndef B4_Q_MINB_FUSED
+#define B4_Q_MINB_FUSED 5
 #endif
 #ifndef B4_FWD_PERWARP
 #define B4_FWD_PERWARP 0
@@ -57,7 +85,7 @@ struct TileCfg {
   static constexpr int TILE = STREAMING ? B4_BWD_TILE : B4_FWD_TILE;
   static constexpr int NSTAGE = STREAMING ? B4_BWD_NSTAGE : B4_FWD_NSTAGE;
   static constexpr int NOSTAGE = STREAMING ? B4_BWD_NOSTAGE : B4_FWD_NOSTAGE;
-  static constexpr int MINB = STREAMING ? B4_BWD_MINB : B4_FWD_MINB;
+  static constexpr int MINB = STREAMING ? B4_BWD_MINB : (M == Mode::Forward ? B4_FWD_MINB : B4_FUSED_MINB);
   // per-warp pipelines (TILE/32 independent warps per CTA) or CTA tiles
   static constexpr bool PERWARP = STREAMING ? (B4_BWD_PERWARP != 0) : (B4_FWD_PERWARP != 0);
 };
@@ -120,6 +148,50 @@ inline void* advance(void* p, int64_t tokens) {
   return p == nullptr ? nullptr : static_cast<void*>(static_cast<unsigned char*>(p) + tokens * TileIO<T>::ROW_BYTES);
 }
 
+// The Newton passes with compaction of slow tokens (queue_kernel): X by TMA
+// tiles of B4_Q_WARPS x 32 tokens, results stored directly.
+template <Mode M, class TIn, class TOut>
+cudaError_t launch_queue(const LaunchArgs& la, cudaStream_t stream, int dev, int nsm) {
+  using Q = QueueShape<M, TIn, TOut, B4_Q_WARPS, B4_Q_NSTAGE, B4_Q_QC>;
+  constexpr int MINB = M == Mode::Forward ? B4_Q_MINB_FWD : B4_Q_MINB_FUSED;
+  auto kern = queue_kernel<M, TIn, TOut, B4_Q_WARPS, B4_Q_NSTAGE, B4_Q_QC, B4_Q_K1, B4_Q_K2, MINB>;
+  static std::atomic<int> cap_cache[64];
+  int grid_cap = dev < 64 ? cap_cache[dev].load(std::memory_order_acquire) : 0;
+  cudaError_t err;
+  if (grid_cap == 0) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    int occ = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Q::TILE, Q::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    grid_cap = nsm * std::max(occ, 1);
+    if (dev < 64) cap_cache[dev].store(grid_cap, std::memory_order_release);
+  }
+  constexpr int NIN = ModeTraits<M>::NIN;
+  constexpr int NOUT = ModeTraits<M>::NOUT;
+  for (int64_t done = 0; done < la.T; done += kChunkTokens) {
+    const int64_t n = std::min(la.T - done, kChunkTokens);
+    KParams p;
+    memset(&p, 0, sizeof(p));
+    for (int k = 0; k < NIN; ++k) p.gin[k] = advance<TIn>(la.in[k], done);
+    for (int k = 0; k < NOUT; ++k) p.gout[k] = advance<TOut>(la.out[k], done);
+    p.b = la.b ? la.b + 4 * done : nullptr;
+    p.b_vec = aligned16(la.b) ? 1 : 0;
+    p.evals_out = la.evals_out ? la.evals_out + done : nullptr;
+    p.nonconv = la.nonconv;
+    p.fault = la.fault;
+    p.T = n;
+    p.cfg = la.cfg;
+    if (!encode_rows<TIn>(&p.in[0], p.gin[0], n, Q::TILE)) return cudaErrorInvalidValue;
+    p.ntiles = static_cast<int32_t>((n + Q::TILE - 1) / Q::TILE);
+    const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, grid_cap));
+    kern<<<grid, Q::TILE, Q::SMEM_BYTES, stream>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
 // Enqueue one pass over la.T tokens on `stream`.  Returns the CUDA error of
 // the preparation or launch (cudaSuccess if everything was enqueued).
 template <Mode M, class TIn, class TOut>
@@ -138,6 +210,12 @@ cudaError_t launch(const LaunchArgs& la, cudaStream_t stream) {
   bool aligned = true;
   for (int k = 0; k < NIN; ++k) aligned = aligned && aligned16(la.in[k]);
   for (int k = 0; k < NOUT; ++k) aligned = aligned && aligned16(la.out[k]);
+
+  // the compacting schedule for the Newton passes (16-byte aligned tokens)
+  constexpr bool NEWTON = (M == Mode::Forward || M == Mode::Fused || M == Mode::Recompute);
+  if constexpr (NEWTON) {
+    if (aligned && la.schedule != Schedule::Lane) return launch_queue<M, TIn, TOut>(la, stream, dev, nsm);
+  }
 
   using WS = WarpShape<M, TIn, TOut, C::TILE / 32, C::NSTAGE, C::NOSTAGE>;
   auto kern = C::PERWARP ? warp_stream_kernel<M, TIn, TOut, C::TILE / 32, C::NSTAGE, C::NOSTAGE, C::MINB>

@@ -139,21 +139,17 @@ __device__ __forceinline__ void laplacian_solve(const float w[6], const float g[
   x[0] = fmaf(w[0], x[1], fmaf(w[1], x[2], g[0])) * i0;
 }
 
-// Forward solve of one token [s2.1].  Returns true if the residual reached
-// tol (or its stagnation floor); p is the last evaluation, beta the dual.
-// reload(Tok&) fetches X again for the periodic log-domain refresh, so X does
-// not have to stay live in registers through the iteration (no N(0,1) token
-// ever gets that far).
-template <class Reload>
-__device__ __forceinline__ bool newton_forward(const Tok& x, Tok& p, float beta[3], int& evals,
-                                               const NewtonCfg& cfg, Reload&& reload) {
+// Start of the forward solve of one token [s2.1]: the column-mean dual and
+// the first (log-domain) evaluation.  Returns false for a token with NaN or
+// infinite logits (or sums beyond the fp32 range): p and beta are then NaN
+// and evals 0.
+__device__ __forceinline__ bool newton_start(const Tok& x, Tok& p, float beta[3], int& evals) {
   // Column-mean start: the exact dual when X_ij = u_i + v_j, and a first-order
   // estimate otherwise: b_j = -(mean_i X_ij - mean_i X_i3).
   const float2 cs01 = add2(add2(x.v[0], x.v[2]), add2(x.v[4], x.v[6]));
   const float2 cs23 = add2(add2(x.v[1], x.v[3]), add2(x.v[5], x.v[7]));
   const float all = (cs01.x + cs01.y) + (cs23.x + cs23.y);
   if (!isfinite(all)) {
-    // NaN or infinite logits (or sums beyond the fp32 range): no projection
     const float nan = __int_as_float(0x7fffffff);
 #pragma unroll
     for (int k = 0; k < 8; ++k) p.v[k] = splat(nan);
@@ -167,15 +163,34 @@ __device__ __forceinline__ bool newton_forward(const Tok& x, Tok& p, float beta[
   beta[2] = (cs23.y - cs23.x) * q;
   eval_log(x, beta, p);
   evals = 1;
-  float prev = 3.0e38f;
-  for (int k = 0;; ++k) {
+  return true;
+}
+
+// Outcome of newton_run.
+enum NewtonStatus : int { kPaused = 0, kConverged = 1, kCapped = 2 };
+
+// Newton iterations of one token from the state (p, beta, prev, evals) [s2.1],
+// until the residual reaches tol (or its stagnation floor): kConverged; or
+// until cfg.max_evals evaluations: kCapped; or, with the token unfinished,
+// until `until` evaluations: kPaused (the state is then complete: calling
+// again continues the same iteration, redoing only the residual test).
+// prev is the previous residual (3e38 before the first step).  With REFRESH,
+// every 8th step re-evaluates P in the log domain from X, which
+// reload(Tok&) fetches, so that X does not have to stay live in registers
+// through the iteration.
+template <bool REFRESH, class Reload>
+__device__ __forceinline__ int newton_run(Tok& p, float beta[3], float& prev, int& evals, int until,
+                                          const NewtonCfg& cfg, Reload&& reload) {
+  const int lim = until < cfg.max_evals ? until : cfg.max_evals;
+  for (;;) {
     float2 g01, g23;
     colsum_minus_one(p, g01, g23);
     const float res = fmaxf(max3(fabsf(g01.x), fabsf(g01.y), fabsf(g23.x)), fabsf(g23.y));
     const bool stop = (res <= cfg.tol) || (res <= kStagnation * cfg.tol && res > 0.5f * prev);
-    if (stop) return true;
-    if (evals >= cfg.max_evals) return false;
+    if (stop) return kConverged;
+    if (evals >= lim) return evals >= cfg.max_evals ? kCapped : kPaused;
     prev = res;
+    const int k = evals - 1;  // Newton steps taken so far
     // Newton step on b_0..b_2 (natural-log units)
     float w[6], d[3];
     const float g[3] = {g01.x, g01.y, g23.x};
@@ -185,8 +200,8 @@ __device__ __forceinline__ bool newton_forward(const Tok& x, Tok& p, float beta[
     // zero step unscaled).  From the kDampFrom-th step on it is also damped by
     // 1/(1 + lambda) when the Newton decrement lambda = sqrt(g^T H^-1 g)
     // exceeds 1: rare tokens (about one in 10^6 at N(0,10^2)) otherwise cycle.
-    // k is the same for every active lane of a warp, so warps whose tokens
-    // all converge earlier (every N(0,1) warp) never run this branch.
+    // Lanes that start together share k, so warps whose tokens all converge
+    // earlier (every N(0,1) warp) never run this branch.
     float lim = 1.0f;
     if (k >= kDampFrom) {
       const float lam2 = fmaf(g[0], d[0], fmaf(g[1], d[1], g[2] * d[2]));
@@ -199,7 +214,7 @@ __device__ __forceinline__ bool newton_forward(const Tok& x, Tok& p, float beta[
       d[j] *= scale;  // base-2 units
       beta[j] -= d[j];
     }
-    if ((k & (kRefreshEvery - 1)) == kRefreshEvery - 1) {
+    if (REFRESH && (k & (kRefreshEvery - 1)) == kRefreshEvery - 1) {
       Tok xr;
       reload(xr);
       eval_log(xr, beta, p);
@@ -208,6 +223,17 @@ __device__ __forceinline__ bool newton_forward(const Tok& x, Tok& p, float beta[
     }
     ++evals;
   }
+}
+
+// Forward solve of one token [s2.1] to the end.  Returns true if the
+// residual reached tol (or its stagnation floor); p is the last evaluation,
+// beta the dual.
+template <class Reload>
+__device__ __forceinline__ bool newton_forward(const Tok& x, Tok& p, float beta[3], int& evals,
+                                               const NewtonCfg& cfg, Reload&& reload) {
+  if (!newton_start(x, p, beta, evals)) return false;
+  float prev = 3.0e38f;
+  return newton_run<true>(p, beta, prev, evals, 0x7fffffff, cfg, reload) == kConverged;
 }
 
 // Backward of one token [s2.2]: dX = (dP/dX)^T G from P and G.

@@ -17,6 +17,13 @@ enum class Mode : int {
   Sinkhorn = 4,   // X -> P, fixed iterations
 };
 
+// How the Newton passes assign tokens to threads (birkhoff4_opts.schedule).
+enum class Schedule : int {
+  Default = 0,  // the measured fastest (Queue)
+  Queue = 1,    // one thread per token, slow tokens compacted into resume rounds
+  Lane = 2,     // one thread per token for its whole solve
+};
+
 // Stopping rule of the Newton forward.
 struct NewtonCfg {
   int max_evals;  // cap on evaluations of P (>= 1)
@@ -38,6 +45,7 @@ struct LaunchArgs {
   NewtonCfg cfg;
   int32_t iters;                // Sinkhorn iterations
   unsigned int* fault;          // device fault latch
+  Schedule schedule;            // Newton passes: token schedule
 };
 
 // Enqueue one pass (defined in b4_launch.cuh, instantiated per pass in the

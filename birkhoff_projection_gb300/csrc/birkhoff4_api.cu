@@ -65,24 +65,34 @@ LaunchArgs blank(int64_t T) {
   la.cfg = newton_cfg(nullptr);
   la.iters = 0;
   la.fault = nullptr;
+  la.schedule = Schedule::Default;
   return la;
+}
+
+// Options common to the Newton entry points: checks, then copied into la.
+int apply_opts(const birkhoff4_opts* o, LaunchArgs* la) {
+  if (o->max_evals < 0 || o->max_evals > 1024) return B4_EINVAL;
+  if (!(o->tol >= 0.0f) || std::isinf(o->tol)) return B4_EINVAL;
+  if (o->schedule < B4_SCHED_DEFAULT || o->schedule > B4_SCHED_LANE) return B4_EINVAL;
+  la->evals_out = o->evals_out;
+  la->nonconv = o->nonconv_count;
+  la->cfg = newton_cfg(o);
+  la->schedule = static_cast<Schedule>(o->schedule);
+  return B4_OK;
 }
 
 int forward_impl(const void* X, void* P, float* b, int64_t T, const birkhoff4_opts* o,
                  cudaStream_t s) {
   if (T < 0 || o == nullptr) return B4_EINVAL;
   if (!dtype_ok(o->in_dtype) || !dtype_ok(o->out_dtype)) return B4_EINVAL;
-  if (o->max_evals < 0 || o->max_evals > 1024) return B4_EINVAL;
-  if (!(o->tol >= 0.0f) || std::isinf(o->tol)) return B4_EINVAL;
+  LaunchArgs la = blank(T);
+  const int st = apply_opts(o, &la);
+  if (st != B4_OK) return st;
   if (T == 0) return B4_OK;
   if (X == nullptr || P == nullptr) return B4_EINVAL;
-  LaunchArgs la = blank(T);
   la.in[0] = X;
   la.out[0] = P;
   la.b = b;
-  la.evals_out = o->evals_out;
-  la.nonconv = o->nonconv_count;
-  la.cfg = newton_cfg(o);
   const bool fin = o->in_dtype == B4_F32, fout = o->out_dtype == B4_F32;
   if (fin && fout) return run<Mode::Forward, float, float>(la, s);
   if (!fin && !fout) return run<Mode::Forward, bf16_t, bf16_t>(la, s);
@@ -108,11 +118,16 @@ int backward_impl(const void* X, const void* P, const void* dP, void* dX, int64_
 }
 
 template <class T>
-int fused_impl(const void* X, const void* dP, void* P, void* dX, int64_t n, cudaStream_t s) {
+int fused_impl(const void* X, const void* dP, void* P, void* dX, int64_t n, cudaStream_t s,
+               const birkhoff4_opts* o = nullptr) {
   if (n < 0) return B4_EINVAL;
+  LaunchArgs la = blank(n);
+  if (o != nullptr) {
+    const int st = apply_opts(o, &la);
+    if (st != B4_OK) return st;
+  }
   if (n == 0) return B4_OK;
   if (X == nullptr || dP == nullptr || dX == nullptr) return B4_EINVAL;
-  LaunchArgs la = blank(n);
   la.in[0] = X;
   la.in[1] = dP;
   if (P == nullptr) {
@@ -289,6 +304,15 @@ int birkhoff4_forward_backward(const float* X, const float* dP, float* P, float*
 int birkhoff4_forward_backward_bf16(const uint16_t* X, const uint16_t* dP, uint16_t* P,
                                     uint16_t* dX, int64_t T, birkhoff4_stream_t stream) {
   return fused_impl<bf16_t>(X, dP, P, dX, T, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int birkhoff4_forward_backward_ex(const void* X, const void* dP, void* P, void* dX, int64_t T,
+                                  const birkhoff4_opts* opts, birkhoff4_stream_t stream) {
+  if (opts == nullptr || !dtype_ok(opts->in_dtype) || opts->out_dtype != opts->in_dtype)
+    return B4_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (opts->in_dtype == B4_F32) return fused_impl<float>(X, dP, P, dX, T, s, opts);
+  return fused_impl<bf16_t>(X, dP, P, dX, T, s, opts);
 }
 
 int birkhoff4_forward_backward_host(const void* X_h, const void* dP_h, void* P_h, void* dX_h,

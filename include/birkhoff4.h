@@ -61,7 +61,7 @@
 extern "C" {
 #endif
 
-#define BIRKHOFF4_VERSION 1
+#define BIRKHOFF4_VERSION 2
 
 /* Same type as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st *birkhoff4_stream_t;
@@ -79,15 +79,36 @@ enum birkhoff4_dtype {
     B4_BF16 = 1
 };
 
-/* Options of birkhoff4_forward_ex.  Zero-initialise, then set fields. */
+/* How the Newton passes assign tokens to threads [mHC s2.3: a batched     */
+/* per-token kernel; the mapping is the implementation's choice].  Every   */
+/* schedule computes the same iteration; they differ in speed, and in the  */
+/* last bits of slow tokens (see B4_SCHED_QUEUE).                          */
+enum birkhoff4_schedule {
+    B4_SCHED_DEFAULT = 0, /* the measured fastest: B4_SCHED_QUEUE          */
+    /* One thread per token; a warp solves its 32 tokens for at most 6     */
+    /* evaluations, parks the unsolved ones (dual, residual, index, count) */
+    /* in shared memory and solves them later in full warps of parked      */
+    /* tokens, 2 evaluations per round, re-evaluating P in the log domain  */
+    /* from X and the dual on each resume (which replaces the periodic     */
+    /* log-domain refresh).  Needs 16-byte aligned arrays (else as LANE).  */
+    B4_SCHED_QUEUE = 1,
+    /* One thread per token from start to finish: a warp runs as long as   */
+    /* its slowest token.                                                  */
+    B4_SCHED_LANE = 2
+};
+
+/* Options of birkhoff4_forward_ex and birkhoff4_forward_backward_ex.      */
+/* Zero-initialise, then set fields.                                       */
 typedef struct birkhoff4_opts {
     int32_t in_dtype;   /* B4_F32 or B4_BF16 (X) */
     int32_t out_dtype;  /* B4_F32 or B4_BF16 (P) */
     int32_t max_evals;  /* cap on evaluations of P per token, 1..1024; 0 = 48 */
     float tol;          /* stop at max_j |colsum_j(P) - 1| <= tol; 0 = 1e-6 */
-    int32_t *evals_out; /* NULL or device [T]: evaluations used per token */
+    int32_t *evals_out; /* NULL or device [T]: evaluations used per token (the
+                           log-domain re-evaluation on a resume is not one) */
     unsigned long long *nonconv_count; /* NULL or device counter: += tokens
                                           that stopped above tol */
+    int32_t schedule;   /* a birkhoff4_schedule; 0 = B4_SCHED_DEFAULT */
 } birkhoff4_opts;
 
 /* ---------------------------------------------------------------------- */
@@ -96,8 +117,9 @@ typedef struct birkhoff4_opts {
 /* Per token: b starts from the column-mean estimate                       */
 /* b_j = -(mean_i X_ij - mean_i X_i3); each evaluation forms the row       */
 /* softmax of X + b (first in the log domain with every row shifted by its */
-/* maximum, then by multiplicative updates of the previous P, refreshed in */
-/* the log domain every 8 evaluations); the gradient is colsum(P) - 1 and  */
+/* maximum, then by multiplicative updates of the previous P, evaluated    */
+/* again in the log domain when a parked token resumes (B4_SCHED_QUEUE) or */
+/* every 8 evaluations (B4_SCHED_LANE)); the gradient is colsum(P) - 1 and */
 /* the Hessian sum_i diag(p_i) - p_i p_i^T restricted to columns 0..2; the */
 /* 3x3 Newton system is solved by Laplacian elimination; the step is       */
 /* clamped to 3 (natural-log units) in the max norm and, from the fifth    */
@@ -148,6 +170,12 @@ int birkhoff4_forward_backward(const float *X, const float *dP, float *P, float 
                                birkhoff4_stream_t stream);
 int birkhoff4_forward_backward_bf16(const uint16_t *X, const uint16_t *dP, uint16_t *P,
                                     uint16_t *dX, int64_t T, birkhoff4_stream_t stream);
+/* The fused pass with options: opts->in_dtype == opts->out_dtype gives    */
+/* the dtype of X, dP, P and dX; tol, max_evals, the statistics and the    */
+/* schedule as in birkhoff4_forward_ex.  P == NULL: dX only (P recomputed  */
+/* in registers, nothing else written).                                    */
+int birkhoff4_forward_backward_ex(const void *X, const void *dP, void *P, void *dX, int64_t T,
+                                  const birkhoff4_opts *opts, birkhoff4_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
 /* General n x n tokens, 2 <= n <= 8 [mHC s2.1: the dual reduces to m-1    */

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_strerror(L):
-    assert L.birkhoff4_version() == 1
+    assert L.birkhoff4_version() == 2
     for code in (0, 1, 2, 3, 99):
         s = L.birkhoff4_strerror(code)
         assert isinstance(s, bytes) and len(s) > 0
@@ -200,6 +200,17 @@ def test_bad_options_are_einval(L):
     assert f(FAKE, FAKE, None, 4, opts(tol=-1.0), None) == _lib.B4_EINVAL
     assert f(FAKE, FAKE, None, 4, opts(tol=float("nan")), None) == _lib.B4_EINVAL
     assert f(FAKE, FAKE, None, 4, opts(tol=float("inf")), None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, None, 4, opts(schedule=3), None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, None, 4, opts(schedule=-1), None) == _lib.B4_EINVAL
+    # the fused pass with options: same checks, one dtype for everything
+    g = L.birkhoff4_forward_backward_ex
+    assert g(FAKE, FAKE, FAKE, FAKE, 4, None, None) == _lib.B4_EINVAL
+    assert g(FAKE, FAKE, FAKE, FAKE, 4, opts(out_dtype=1), None) == _lib.B4_EINVAL
+    assert g(FAKE, FAKE, FAKE, FAKE, 4, opts(schedule=7), None) == _lib.B4_EINVAL
+    assert g(FAKE, FAKE, FAKE, FAKE, 4, opts(max_evals=2000), None) == _lib.B4_EINVAL
+    assert g(FAKE, FAKE, FAKE, FAKE, -1, opts(), None) == _lib.B4_EINVAL
+    assert g(None, None, None, None, 0, opts(), None) == _lib.B4_OK
+    assert g(None, FAKE, FAKE, FAKE, 4, opts(), None) == _lib.B4_EINVAL
 
 
 def test_host_streaming_argument_checks(L):
