@@ -369,7 +369,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--log2-tokens", type=int, default=LOG2_T)
-    ap.add_argument("--schedule", choices=["default", "queue", "lane"], default="default",
+    ap.add_argument("--schedule", choices=["default", "queue", "lane", "lanes4"], default="default",
                     help="token schedule of the Newton passes (birkhoff4_opts.schedule)")
     ap.add_argument("--sigma", type=float, default=SIGMA,
                     help="logit scale of the timed workload (the headline is sigma = 1)")

@@ -69,7 +69,8 @@ class _on_device:
             self.ctx.__exit__(*exc)
 
 
-_SCHED = {"default": _lib.B4_SCHED_DEFAULT, "queue": _lib.B4_SCHED_QUEUE, "lane": _lib.B4_SCHED_LANE}
+_SCHED = {"default": _lib.B4_SCHED_DEFAULT, "queue": _lib.B4_SCHED_QUEUE, "lane": _lib.B4_SCHED_LANE,
+          "lanes4": _lib.B4_SCHED_LANES4}
 
 
 def forward(X: torch.Tensor, *, out: torch.Tensor = None, out_dtype=None, return_dual: bool = False,
@@ -80,7 +81,8 @@ def forward(X: torch.Tensor, *, out: torch.Tensor = None, out_dtype=None, return
     Returns P (dtype out_dtype, default X.dtype), plus b ([..., 4] fp32,
     natural-log column dual, b[..., 3] = 0) if return_dual, plus
     (evals [...] int32, nonconverged count) if return_stats.  schedule:
-    "default", "queue" or "lane" (birkhoff4_schedule)."""
+    "default", "queue", "lane" or "lanes4" (birkhoff4_schedule; "lanes4"
+    for fp32 only)."""
     T = _check_tokens(X, "X")
     odt = out_dtype or X.dtype
     if out is None:

@@ -16,7 +16,7 @@ _lib = None
 
 B4_OK, B4_EINVAL, B4_ECUDA, B4_ENOTIMPL, B4_ESCRATCH = 0, 1, 2, 3, 4
 B4_F32, B4_BF16 = 0, 1
-B4_SCHED_DEFAULT, B4_SCHED_QUEUE, B4_SCHED_LANE = 0, 1, 2
+B4_SCHED_DEFAULT, B4_SCHED_QUEUE, B4_SCHED_LANE, B4_SCHED_LANES4 = 0, 1, 2, 3
 
 # Every function the header declares, with its ctypes signature.
 _vp = ctypes.c_void_p

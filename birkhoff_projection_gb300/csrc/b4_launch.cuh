@@ -11,8 +11,10 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "b4_kernels.cuh"
+#include "b4_lanes4.cuh"
 #include "b4_queue.cuh"
 
 namespace b4 {
@@ -192,6 +194,41 @@ cudaError_t launch_queue(const LaunchArgs& la, cudaStream_t stream, int dev, int
   return cudaSuccess;
 }
 
+// The fp32 forward with four lanes per token (lanes4_kernel): 256-thread CTAs,
+// a persistent grid, tokens read and written as contiguous 16-byte rows.
+inline cudaError_t launch_lanes4(const LaunchArgs& la, cudaStream_t stream, int dev, int nsm) {
+  auto kern = lanes4_kernel<float, float>;
+  static std::atomic<int> cap_cache[64];
+  int grid_cap = dev < 64 ? cap_cache[dev].load(std::memory_order_acquire) : 0;
+  cudaError_t err;
+  if (grid_cap == 0) {
+    int occ = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 256, 0);
+    if (err != cudaSuccess) return err;
+    grid_cap = nsm * std::max(occ, 1);
+    if (dev < 64) cap_cache[dev].store(grid_cap, std::memory_order_release);
+  }
+  for (int64_t done = 0; done < la.T; done += kChunkTokens) {
+    const int64_t n = std::min(la.T - done, kChunkTokens);
+    KParams p;
+    memset(&p, 0, sizeof(p));
+    p.gin[0] = advance<float>(la.in[0], done);
+    p.gout[0] = advance<float>(la.out[0], done);
+    p.b = la.b ? la.b + 4 * done : nullptr;
+    p.b_vec = aligned16(la.b) ? 1 : 0;
+    p.evals_out = la.evals_out ? la.evals_out + done : nullptr;
+    p.nonconv = la.nonconv;
+    p.fault = la.fault;
+    p.T = n;
+    p.cfg = la.cfg;
+    const int grid = static_cast<int>(std::min<int64_t>((n + 63) / 64, grid_cap));
+    kern<<<grid, 256, 0, stream>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
 // Enqueue one pass over la.T tokens on `stream`.  Returns the CUDA error of
 // the preparation or launch (cudaSuccess if everything was enqueued).
 template <Mode M, class TIn, class TOut>
@@ -211,10 +248,15 @@ cudaError_t launch(const LaunchArgs& la, cudaStream_t stream) {
   for (int k = 0; k < NIN; ++k) aligned = aligned && aligned16(la.in[k]);
   for (int k = 0; k < NOUT; ++k) aligned = aligned && aligned16(la.out[k]);
 
+  // four lanes per token: the fp32 forward (16-byte aligned tokens)
+  if constexpr (M == Mode::Forward && std::is_same<TIn, float>::value && std::is_same<TOut, float>::value) {
+    if (aligned && la.schedule == Schedule::Lanes4) return launch_lanes4(la, stream, dev, nsm);
+  }
   // the compacting schedule for the Newton passes (16-byte aligned tokens)
   constexpr bool NEWTON = (M == Mode::Forward || M == Mode::Fused || M == Mode::Recompute);
   if constexpr (NEWTON) {
-    if (aligned && la.schedule != Schedule::Lane) return launch_queue<M, TIn, TOut>(la, stream, dev, nsm);
+    if (aligned && (la.schedule == Schedule::Default || la.schedule == Schedule::Queue))
+      return launch_queue<M, TIn, TOut>(la, stream, dev, nsm);
   }
 
   using WS = WarpShape<M, TIn, TOut, C::TILE / 32, C::NSTAGE, C::NOSTAGE>;

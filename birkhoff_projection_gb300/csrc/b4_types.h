@@ -22,6 +22,7 @@ enum class Schedule : int {
   Default = 0,  // the measured fastest (Queue)
   Queue = 1,    // one thread per token, slow tokens compacted into resume rounds
   Lane = 2,     // one thread per token for its whole solve
+  Lanes4 = 3,   // four lanes per token, one row each (fp32 forward only)
 };
 
 // Stopping rule of the Newton forward.

@@ -73,7 +73,7 @@ LaunchArgs blank(int64_t T) {
 int apply_opts(const birkhoff4_opts* o, LaunchArgs* la) {
   if (o->max_evals < 0 || o->max_evals > 1024) return B4_EINVAL;
   if (!(o->tol >= 0.0f) || std::isinf(o->tol)) return B4_EINVAL;
-  if (o->schedule < B4_SCHED_DEFAULT || o->schedule > B4_SCHED_LANE) return B4_EINVAL;
+  if (o->schedule < B4_SCHED_DEFAULT || o->schedule > B4_SCHED_LANES4) return B4_EINVAL;
   la->evals_out = o->evals_out;
   la->nonconv = o->nonconv_count;
   la->cfg = newton_cfg(o);
@@ -88,6 +88,8 @@ int forward_impl(const void* X, void* P, float* b, int64_t T, const birkhoff4_op
   LaunchArgs la = blank(T);
   const int st = apply_opts(o, &la);
   if (st != B4_OK) return st;
+  if (o->schedule == B4_SCHED_LANES4 && (o->in_dtype != B4_F32 || o->out_dtype != B4_F32))
+    return B4_ENOTIMPL;
   if (T == 0) return B4_OK;
   if (X == nullptr || P == nullptr) return B4_EINVAL;
   la.in[0] = X;
@@ -125,6 +127,7 @@ int fused_impl(const void* X, const void* dP, void* P, void* dX, int64_t n, cuda
   if (o != nullptr) {
     const int st = apply_opts(o, &la);
     if (st != B4_OK) return st;
+    if (o->schedule == B4_SCHED_LANES4) return B4_ENOTIMPL;  // forward only
   }
   if (n == 0) return B4_OK;
   if (X == nullptr || dP == nullptr || dX == nullptr) return B4_EINVAL;

@@ -82,7 +82,8 @@ enum birkhoff4_dtype {
 /* How the Newton passes assign tokens to threads [mHC s2.3: a batched     */
 /* per-token kernel; the mapping is the implementation's choice].  Every   */
 /* schedule computes the same iteration; they differ in speed, and in the  */
-/* last bits of slow tokens (see B4_SCHED_QUEUE).                          */
+/* last bits of slow tokens (see B4_SCHED_QUEUE) and, for LANES4, in the  */
+/* rounding of sums taken in another order.                                */
 enum birkhoff4_schedule {
     B4_SCHED_DEFAULT = 0, /* the measured fastest: B4_SCHED_QUEUE          */
     /* One thread per token; a warp solves its 32 tokens for at most 6     */
@@ -94,7 +95,14 @@ enum birkhoff4_schedule {
     B4_SCHED_QUEUE = 1,
     /* One thread per token from start to finish: a warp runs as long as   */
     /* its slowest token.                                                  */
-    B4_SCHED_LANE = 2
+    B4_SCHED_LANE = 2,
+    /* Four lanes per token, one row each [mHC s2.3: a matrix spread over  */
+    /* lanes, column sums by __shfl_xor_sync]: contiguous 16-byte loads    */
+    /* and stores, column sums and Hessian weights as butterfly sums over  */
+    /* the four lanes, the 3x3 solve repeated in each.  A warp waits for   */
+    /* its slowest of 8 tokens.  fp32 forward only (B4_ENOTIMPL for bf16   */
+    /* and for the fused pass); unaligned arrays run as LANE.              */
+    B4_SCHED_LANES4 = 3
 };
 
 /* Options of birkhoff4_forward_ex and birkhoff4_forward_backward_ex.      */

@@ -200,13 +200,16 @@ def test_bad_options_are_einval(L):
     assert f(FAKE, FAKE, None, 4, opts(tol=-1.0), None) == _lib.B4_EINVAL
     assert f(FAKE, FAKE, None, 4, opts(tol=float("nan")), None) == _lib.B4_EINVAL
     assert f(FAKE, FAKE, None, 4, opts(tol=float("inf")), None) == _lib.B4_EINVAL
-    assert f(FAKE, FAKE, None, 4, opts(schedule=3), None) == _lib.B4_EINVAL
+    assert f(FAKE, FAKE, None, 4, opts(schedule=4), None) == _lib.B4_EINVAL
+    # four lanes per token: the fp32 forward only
+    assert f(FAKE, FAKE, None, 4, opts(schedule=3, in_dtype=1, out_dtype=1), None) == _lib.B4_ENOTIMPL
     assert f(FAKE, FAKE, None, 4, opts(schedule=-1), None) == _lib.B4_EINVAL
     # the fused pass with options: same checks, one dtype for everything
     g = L.birkhoff4_forward_backward_ex
     assert g(FAKE, FAKE, FAKE, FAKE, 4, None, None) == _lib.B4_EINVAL
     assert g(FAKE, FAKE, FAKE, FAKE, 4, opts(out_dtype=1), None) == _lib.B4_EINVAL
     assert g(FAKE, FAKE, FAKE, FAKE, 4, opts(schedule=7), None) == _lib.B4_EINVAL
+    assert g(FAKE, FAKE, FAKE, FAKE, 4, opts(schedule=3), None) == _lib.B4_ENOTIMPL
     assert g(FAKE, FAKE, FAKE, FAKE, 4, opts(max_evals=2000), None) == _lib.B4_EINVAL
     assert g(FAKE, FAKE, FAKE, FAKE, -1, opts(), None) == _lib.B4_EINVAL
     assert g(None, None, None, None, 0, opts(), None) == _lib.B4_OK

@@ -1,4 +1,4 @@
-"""The two token schedules of the Newton passes (birkhoff4_opts.schedule),
+"""The token schedules of the Newton passes (birkhoff4_opts.schedule),
 through the C ABI.
 
 B4_SCHED_QUEUE (the default) solves each warp's tokens in a fresh round of
@@ -14,6 +14,8 @@ each resume.  B4_SCHED_LANE keeps one token per thread to the end.
     consistent with the forward.
   * Caps inside and beyond the fresh round; non-finite tokens among parked
     ones; ragged token counts.
+B4_SCHED_LANES4 (four lanes per token, fp32 forward) against the oracle on
+the three magnitude classes and ragged sizes.
 """
 import numpy as np
 import pytest
@@ -22,8 +24,8 @@ import torch
 import birkhoff_projection_gb300 as b4
 import oracle
 from birkhoff_projection_gb300 import workloads
-from _helpers import (TOL_DX_REL, TOL_P_LARGE, TOL_RES_LARGE, max_abs_err, np64, rel_fro,
-                      residual)
+from _helpers import (TOL_DX_REL, TOL_P_LARGE, TOL_P_SMALL, TOL_RES_LARGE, TOL_RES_SMALL,
+                      max_abs_err, np64, rel_fro, residual)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -145,3 +147,44 @@ def test_queue_ragged_small(T):
     Pst = oracle.project64(np64(X))
     assert max_abs_err(np64(P), Pst) <= TOL_P_LARGE
     assert residual(np64(P)).max() <= TOL_RES_LARGE
+
+
+@pytest.mark.parametrize("kind,T", [("normal", 40009), ("sigma10", 30011), ("large", 20001)])
+def test_lanes4_forward(kind, T):
+    """Four lanes per token (B4_SCHED_LANES4, fp32 forward): the same
+    iteration with sums taken across lanes.  Parity with the oracle in the
+    workload's tolerance class, b consistent with P, evaluation counts as in
+    the one-thread kernel up to rounding-order effects."""
+    if kind == "normal":
+        X = workloads.normal(T, 1.0, seed=47, device=DEV)
+    elif kind == "sigma10":
+        X = workloads.normal(T, 10.0, seed=48, device=DEV)
+    else:
+        X = workloads.large_magnitude(T, device=DEV)[0]
+    X[T // 2, 1, 1] = float("nan")
+    P, b, ev, nc = b4.forward(X, return_dual=True, return_stats=True, schedule="lanes4")
+    _, evl, _ = b4.forward(X, return_stats=True, schedule="lane")
+    ok = torch.ones(T, dtype=torch.bool)
+    ok[T // 2] = False
+    Pc = P.cpu()
+    assert torch.isnan(Pc[T // 2]).all() and int(ev[T // 2]) == 0
+    assert int(nc.item()) == 1
+    Pg = Pc[ok].double().numpy()
+    Pst = oracle.project64(np64(X)[ok.numpy()])
+    tol_p, tol_r = ((TOL_P_SMALL, TOL_RES_SMALL) if kind == "normal" else (TOL_P_LARGE, TOL_RES_LARGE))
+    assert max_abs_err(Pg, Pst) <= tol_p
+    assert residual(Pg).max() <= tol_r
+    bb = b.double().cpu().numpy()[ok.numpy()]
+    assert (bb[:, 3] == 0).all()
+    assert abs(float(ev[ok].float().mean()) - float(evl[ok].float().mean())) <= 0.05
+    if kind != "large":
+        z = np64(X)[ok.numpy()] + bb[:, None, :]
+        s = np.exp(z - z.max(axis=2, keepdims=True))
+        assert max_abs_err(s / s.sum(axis=2, keepdims=True), Pg) <= 10 * tol_p
+
+
+@pytest.mark.parametrize("T", [1, 7, 8, 9, 63, 65, 1001])
+def test_lanes4_ragged(T):
+    X = workloads.normal(T, 1.0, seed=49 + T, device=DEV)
+    P = b4.forward(X, schedule="lanes4")
+    assert max_abs_err(np64(P), oracle.project64(np64(X))) <= TOL_P_SMALL
