@@ -386,6 +386,8 @@ def main():
                     help="streaming entropic OT: n = m = 65536 points, d = 64 and 512, both precisions")
     ap.add_argument("--nxn", action="store_true",
                     help="n x n kernels, n = 2..8, 1 GiB of fp32 X per n (one JSON line each)")
+    ap.add_argument("--nxn-n", type=int, default=None, help="with --nxn: this n only")
+    ap.add_argument("--nxn-mib", type=int, default=1024, help="with --nxn: MiB of fp32 X per n")
     ap.add_argument("--eot-profile", choices=["update", "transport", "hvp"],
                     help="profiling target (not a measurement): three calls of one streaming "
                          "EOT op on seeded clouds, n = m = --eot-n points of dimension --eot-d")
@@ -635,8 +637,8 @@ def run_extra(args):
         run_eot(dev)
     if args.nxn:
         peak, peak_kind = hbm_peak()
-        for n in range(2, 9):
-            T = (1 << 28) // (n * n)  # 1 GiB of fp32 X
+        for n in (range(2, 9) if args.nxn_n is None else [args.nxn_n]):
+            T = (args.nxn_mib << 18) // (n * n)  # MiB of fp32 X
             g = torch.Generator(device=dev).manual_seed(11 + n)
             X = torch.randn(T, n, n, device=dev, generator=g)
             G = torch.randn(T, n, n, device=dev, generator=g)

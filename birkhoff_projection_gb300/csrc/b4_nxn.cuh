@@ -28,6 +28,11 @@ struct NxnShape {
 constexpr float kNxnRidge = 1e-7f;
 constexpr float kNxnClamp = 3.0f;
 constexpr int kNxnDampFrom = 4;
+// From this n on the forward keeps P in shared memory (nxn_newton_smem).
+#ifndef B4_NXN_SMEM_FROM
+#define B4_NXN_SMEM_FROM 7
+#endif
+constexpr int kNxnSmemFrom = B4_NXN_SMEM_FROM;
 
 // Row softmax of (x log2e + beta), rows shifted by their maximum; x is the
 // token's row in shared memory.
@@ -220,13 +225,205 @@ __device__ __forceinline__ bool nxn_newton(const float* xs, float p[N * N], floa
   }
 }
 
+// The same forward with P kept in the token's own row of shared memory
+// instead of registers (for large n, where P, the Hessian and the solve do
+// not fit the register budget of several resident CTAs).  `row` holds X on
+// entry and P on return; xg is the token's X in global memory, read again by
+// the periodic log-domain refresh.  Every evaluation streams the rows --
+// load, scale, normalise, store -- and accumulates the column sums and the
+// Hessian edge weights of the new P on the way, so only those, the dual and
+// one row are live.  The operations and their order are those of nxn_newton:
+// the results are the same bit for bit.
+template <int N>
+__device__ __forceinline__ void nxn_row_ld(const float* r, float v[N]) {
+#pragma unroll
+  for (int j = 0; j < N; ++j) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[j]) : "r"(smem_addr(r + j)));
+}
+template <int N>
+__device__ __forceinline__ void nxn_row_st(float* r, const float v[N]) {
+#pragma unroll
+  for (int j = 0; j < N; ++j) asm volatile("st.shared.f32 [%0], %1;" ::"r"(smem_addr(r + j)), "f"(v[j]) : "memory");
+}
+
+// Column sums and edge weights (+ base) accumulated over rows.
+template <int N>
+struct NxnAccum {
+  float c[N];
+  float w[N][N];
+  __device__ __forceinline__ void reset(float base) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      c[j] = 0.0f;
+#pragma unroll
+      for (int k = j + 1; k < N; ++k) w[j][k] = base;
+    }
+  }
+  __device__ __forceinline__ void add(const float p[N]) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      c[j] += p[j];
+#pragma unroll
+      for (int k = j + 1; k < N; ++k) w[j][k] = fmaf(p[j], p[k], w[j][k]);
+    }
+  }
+};
+
+template <int N>
+__device__ __forceinline__ bool nxn_newton_smem(float* row, const float* xg, float beta[N], int& evals,
+                                                const NewtonCfg& cfg) {
+  static_assert(N >= 3, "n >= 3");
+  float cs[N];
+  float all = 0.0f;
+#pragma unroll
+  for (int j = 0; j < N; ++j) cs[j] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float x[N];
+    nxn_row_ld<N>(row + N * i, x);
+#pragma unroll
+    for (int j = 0; j < N; ++j) cs[j] += x[j];
+  }
+#pragma unroll
+  for (int j = 0; j < N; ++j) all += cs[j];
+  if (!isfinite(all)) {
+    const float nan = __int_as_float(0x7fffffff);
+    float v[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) v[j] = nan;
+#pragma unroll
+    for (int i = 0; i < N; ++i) nxn_row_st<N>(row + N * i, v);
+#pragma unroll
+    for (int j = 0; j < N; ++j) beta[j] = nan;
+    evals = 0;
+    return false;
+  }
+#pragma unroll
+  for (int j = 0; j < N; ++j) beta[j] = (cs[N - 1] - cs[j]) * (LOG2E / N);
+  NxnAccum<N> acc;
+  // log-domain evaluation of row i from x (row-max shift), stored and accumulated
+  auto eval_log_row = [&](int i, const float x[N]) {
+    float z[N];
+    float m = -3.0e38f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      z[j] = fmaf(x[j], LOG2E, beta[j]);
+      m = fmaxf(m, z[j]);
+    }
+    float sum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      z[j] = ex2(z[j] - m);
+      sum += z[j];
+    }
+    const float r = rcp(sum);
+#pragma unroll
+    for (int j = 0; j < N; ++j) z[j] *= r;
+    nxn_row_st<N>(row + N * i, z);
+    acc.add(z);
+  };
+  acc.reset(kNxnRidge);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float x[N];
+    nxn_row_ld<N>(row + N * i, x);
+    eval_log_row(i, x);
+  }
+  evals = 1;
+  float prev = 3.0e38f;
+  for (int k = 0;; ++k) {
+    float g[N];
+    float res = 0.0f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      g[j] = acc.c[j] - 1.0f;
+      res = fmaxf(res, fabsf(g[j]));
+    }
+    const bool stop = (res <= cfg.tol) || (res <= 64.0f * cfg.tol && res > 0.5f * prev);
+    if (stop) return true;
+    if (evals >= cfg.max_evals) return false;
+    prev = res;
+    float d[N - 1];
+    nxn_solve<N>(acc.w, g, d);
+    float lim = 1.0f;
+    if (k >= kNxnDampFrom) {
+      float lam2 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < N - 1; ++j) lam2 = fmaf(g[j], d[j], lam2);
+      if (lam2 > 1.0f) lim = rcp(1.0f + lam2 * rsqrt(lam2));
+    }
+    float dmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < N - 1; ++j) dmax = fmaxf(dmax, fabsf(d[j]));
+    const float scale = LOG2E * fminf(lim, kNxnClamp * rcp(dmax));
+#pragma unroll
+    for (int j = 0; j < N - 1; ++j) {
+      d[j] *= scale;
+      beta[j] -= d[j];
+    }
+    acc.reset(kNxnRidge);
+    if ((k & 7) == 7) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        float x[N];
+#pragma unroll
+        for (int j = 0; j < N; ++j) x[j] = __ldg(xg + N * i + j);
+        eval_log_row(i, x);
+      }
+    } else {
+      float wv[N];
+#pragma unroll
+      for (int j = 0; j < N - 1; ++j) wv[j] = ex2(-d[j]);
+      wv[N - 1] = 1.0f;
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        float q[N];
+        nxn_row_ld<N>(row + N * i, q);
+        float sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+          q[j] *= wv[j];
+          sum += q[j];
+        }
+        const float r = rcp(sum);
+#pragma unroll
+        for (int j = 0; j < N; ++j) q[j] *= r;
+        nxn_row_st<N>(row + N * i, q);
+        acc.add(q);
+      }
+    }
+    ++evals;
+  }
+}
+
 // Backward of one n x n token [s2.2], the difference forms of the 4 x 4
 // kernel: D_kl = sum_j p_kj (G_kl - G_kj), v_l = sum_k p_kl D_kl,
 // H lambda = v (lambda_{N-1} = 0, ridge 1e-7 max w),
 // dX_kq = p_kq (D_kq - sum_l p_kl (lambda_q - lambda_l)).  G is the token's
-// row in shared memory; dx may alias nothing else.
+// row in shared memory; dX is written to `out` (the token's own row, which
+// may hold P: P is read into registers first).  Both passes over D go row by
+// row -- a row of G is loaded, its row of D formed and used -- so that only
+// p, the Hessian and one row are live (holding D or G whole spills at n = 8).
 template <int N>
-__device__ __forceinline__ void nxn_backward(const float pin[N * N], const float* Gs, float dx[N * N]) {
+__device__ __forceinline__ void nxn_load_row(const float* g, float G[N]) {
+  // ordered shared loads: each row is fetched where it is used
+#pragma unroll
+  for (int j = 0; j < N; ++j) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(G[j]) : "r"(smem_addr(g + j)));
+}
+
+template <int N>
+__device__ __forceinline__ void nxn_D_row(const float p[N * N], const float G[N], int k, float D[N]) {
+#pragma unroll
+  for (int l = 0; l < N; ++l) {
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+      if (j != l) s = fmaf(p[N * k + j], G[l] - G[j], s);
+    D[l] = s;
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void nxn_backward(const float pin[N * N], const float* Gs, float* out) {
   float p[N * N];
 #pragma unroll
   for (int k = 0; k < N; ++k) {
@@ -237,24 +434,16 @@ __device__ __forceinline__ void nxn_backward(const float pin[N * N], const float
 #pragma unroll
     for (int j = 0; j < N; ++j) p[N * k + j] = pin[N * k + j] * r;
   }
-  // D in dx
-#pragma unroll
-  for (int k = 0; k < N; ++k)
-#pragma unroll
-    for (int l = 0; l < N; ++l) {
-      float s = 0.0f;
-#pragma unroll
-      for (int j = 0; j < N; ++j)
-        if (j != l) s = fmaf(p[N * k + j], Gs[N * k + l] - Gs[N * k + j], s);
-      dx[N * k + l] = s;
-    }
   float v[N - 1];
 #pragma unroll
-  for (int l = 0; l < N - 1; ++l) {
-    float s = 0.0f;
+  for (int l = 0; l < N - 1; ++l) v[l] = 0.0f;
 #pragma unroll
-    for (int k = 0; k < N; ++k) s = fmaf(p[N * k + l], dx[N * k + l], s);
-    v[l] = s;
+  for (int k = 0; k < N; ++k) {
+    float G[N], D[N];
+    nxn_load_row<N>(Gs + N * k, G);
+    nxn_D_row<N>(p, G, k, D);
+#pragma unroll
+    for (int l = 0; l < N - 1; ++l) v[l] = fmaf(p[N * k + l], D[l], v[l]);
   }
   float w[N][N];
   nxn_weights<N>(p, w, 0.0f);
@@ -271,15 +460,19 @@ __device__ __forceinline__ void nxn_backward(const float pin[N * N], const float
   nxn_solve<N>(w, v, lam);
   lam[N - 1] = 0.0f;
 #pragma unroll
-  for (int k = 0; k < N; ++k)
+  for (int k = 0; k < N; ++k) {
+    float G[N], D[N];
+    nxn_load_row<N>(Gs + N * k, G);
+    nxn_D_row<N>(p, G, k, D);
 #pragma unroll
     for (int q = 0; q < N; ++q) {
       float c = 0.0f;
 #pragma unroll
       for (int l = 0; l < N; ++l)
         if (l != q) c = fmaf(p[N * k + l], lam[q] - lam[l], c);
-      dx[N * k + q] = p[N * k + q] * (dx[N * k + q] - c);
+      out[N * k + q] = p[N * k + q] * (D[q] - c);
     }
+  }
 }
 
 struct NxnParams {
@@ -294,16 +487,31 @@ struct NxnParams {
 // Persistent kernel over tiles of TILE tokens: coalesced copy into shared
 // memory, per-token compute, coalesced copy out.
 // Resident CTAs per SM the register allocation aims at (launch-bounds
-// minimum): for n >= 5 the per-token state would otherwise take 128-255
-// registers and leave 2-4 CTAs per SM.  Chosen by a sweep on GB300 (2^28
-// bytes of tokens per n): forward 128-thread CTAs 3 / 4 / 4 / 3 and backward
-// 64-thread CTAs 6 / 8 / 8 / 6 for n = 5 / 6 / 7 / 8 (n = 7: forward 1.63 ->
-// 1.00 ms, backward 2.35 -> 1.37 ms; a cap of 8 backward CTAs at n = 8
-// spills and is slower).
+// minimum), swept on GB300.  Forward (128-thread CTAs): 3 / 4 for n = 5 / 6,
+// where P, the Hessian and the solve live in registers (128-255 of them
+// uncapped; n = 7 went 1.63 -> 1.00 ms with a cap); 7 / 6 for n = 7 / 8,
+// where P lives in shared memory (nxn_newton_smem: 72 / 80 registers, no
+// spill; n = 8 went 0.72 -> 0.36 ms at 512 MiB).  Backward (64-thread CTAs,
+// P and dP tiles in shared memory): the most CTAs that both the shared
+// memory and a spill-free register allocation allow, 11 / 10 / 9 / 6 (the
+// backward forms D row by row, so it needs far fewer registers than it
+// once did).
+#ifndef B4_NXN_F5
+#define B4_NXN_F5 3
+#endif
+#ifndef B4_NXN_F6
+#define B4_NXN_F6 4
+#endif
+#ifndef B4_NXN_F7
+#define B4_NXN_F7 7
+#endif
+#ifndef B4_NXN_F8
+#define B4_NXN_F8 6
+#endif
 template <int N, bool FWD>
 constexpr int nxn_minb() {
-  return N == 5 ? (FWD ? 3 : 6) : N == 6 ? (FWD ? 4 : 8) : N == 7 ? (FWD ? 4 : 8)
-       : N == 8 ? (FWD ? 3 : 6) : 1;
+  return N == 5 ? (FWD ? B4_NXN_F5 : 11) : N == 6 ? (FWD ? B4_NXN_F6 : 10)
+       : N == 7 ? (FWD ? B4_NXN_F7 : 9) : N == 8 ? (FWD ? B4_NXN_F8 : 6) : 1;
 }
 
 template <int N, int TILE, bool FWD>
@@ -313,11 +521,24 @@ __global__ void __launch_bounds__(TILE, (nxn_minb<N, FWD>())) nxn_kernel(const N
   float* s0 = sm;                     // X or P tile, reused for the output
   float* s1 = sm + TILE * S::STRIDE;  // dP tile (backward)
   const int tid = threadIdx.x;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * TILE; base < a.T;
-       base += static_cast<int64_t>(gridDim.x) * TILE) {
+  const int64_t step = static_cast<int64_t>(gridDim.x) * TILE;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * TILE; base < a.T; base += step) {
     const int64_t left = a.T - base;
     const int ntok = left < TILE ? static_cast<int>(left) : TILE;
     const int nel = ntok * S::NN;
+    if (tid == 0 && base + step < a.T) {
+      // this CTA's next tile into L2 while the current one is computed (a
+      // whole tile is TILE * n^2 * 4 bytes from a 16-byte aligned start
+      // when the arrays are; the last one is rounded down to 16 bytes)
+      const int64_t nl = a.T - (base + step) < TILE ? a.T - (base + step) : TILE;
+      const uint32_t bytes = static_cast<uint32_t>(nl * S::NN * 4) & ~15u;
+      const float* n0 = a.in0 + (base + step) * S::NN;
+      if (bytes != 0u && (reinterpret_cast<uintptr_t>(n0) & 15u) == 0u) prefetch_l2_bulk(n0, bytes);
+      if constexpr (!FWD) {
+        const float* n1 = a.in1 + (base + step) * S::NN;
+        if (bytes != 0u && (reinterpret_cast<uintptr_t>(n1) & 15u) == 0u) prefetch_l2_bulk(n1, bytes);
+      }
+    }
     const float* g0 = a.in0 + base * S::NN;
     for (int i = tid; i < nel; i += TILE) s0[(i / S::NN) * S::STRIDE + i % S::NN] = __ldg(g0 + i);
     if constexpr (!FWD) {
@@ -325,13 +546,16 @@ __global__ void __launch_bounds__(TILE, (nxn_minb<N, FWD>())) nxn_kernel(const N
       for (int i = tid; i < nel; i += TILE) s1[(i / S::NN) * S::STRIDE + i % S::NN] = __ldg(g1 + i);
     }
     __syncthreads();
-    float out[S::NN];
+    float out[(FWD && N < kNxnSmemFrom) ? S::NN : 1];
     const bool valid = tid < ntok;
     if (valid) {
       if constexpr (FWD) {
         float beta[N];
         int evals = 0;
-        nxn_newton<N>(s0 + tid * S::STRIDE, out, beta, evals, a.cfg);
+        if constexpr (N >= kNxnSmemFrom)
+          nxn_newton_smem<N>(s0 + tid * S::STRIDE, a.in0 + (base + tid) * S::NN, beta, evals, a.cfg);
+        else
+          nxn_newton<N>(s0 + tid * S::STRIDE, out, beta, evals, a.cfg);
         if (a.b != nullptr) {
           float* bp = a.b + (base + tid) * N;
 #pragma unroll
@@ -339,16 +563,20 @@ __global__ void __launch_bounds__(TILE, (nxn_minb<N, FWD>())) nxn_kernel(const N
           bp[N - 1] = 0.0f;
         }
       } else {
+        // dX goes straight into the token's own row of s0 (each thread
+        // touches only its own rows)
         float pin[S::NN];
 #pragma unroll
         for (int e = 0; e < S::NN; ++e) pin[e] = s0[tid * S::STRIDE + e];
-        nxn_backward<N>(pin, s1 + tid * S::STRIDE, out);
+        nxn_backward<N>(pin, s1 + tid * S::STRIDE, s0 + tid * S::STRIDE);
       }
     }
-    __syncthreads();  // every token's inputs have been read
-    if (valid) {
+    if constexpr (FWD && N < kNxnSmemFrom) {
+      __syncthreads();  // every token's inputs have been read
+      if (valid) {
 #pragma unroll
-      for (int e = 0; e < S::NN; ++e) s0[tid * S::STRIDE + e] = out[e];
+        for (int e = 0; e < S::NN; ++e) s0[tid * S::STRIDE + e] = out[e];
+      }
     }
     __syncthreads();
     float* go = a.out + base * S::NN;
