@@ -399,8 +399,8 @@ __device__ __forceinline__ bool nxn_newton_smem(float* row, const float* xg, flo
 // kernel: D_kl = sum_j p_kj (G_kl - G_kj), v_l = sum_k p_kl D_kl,
 // H lambda = v (lambda_{N-1} = 0, ridge 1e-7 max w),
 // dX_kq = p_kq (D_kq - sum_l p_kl (lambda_q - lambda_l)).  G is the token's
-// row in shared memory; dX is written to `out` (the token's own row, which
-// may hold P: P is read into registers first).  Both passes over D go row by
+// row in shared memory; P is read from its row Ps into registers first, so
+// dX may be written to `out` == Ps.  Both passes over D go row by
 // row -- a row of G is loaded, its row of D formed and used -- so that only
 // p, the Hessian and one row are live (holding D or G whole spills at n = 8).
 template <int N>
@@ -423,16 +423,19 @@ __device__ __forceinline__ void nxn_D_row(const float p[N * N], const float G[N]
 }
 
 template <int N>
-__device__ __forceinline__ void nxn_backward(const float pin[N * N], const float* Gs, float* out) {
+__device__ __forceinline__ void nxn_backward(const float* Ps, const float* Gs, float* out) {
+  // P from its shared-memory row, rescaled to unit row sums
   float p[N * N];
 #pragma unroll
   for (int k = 0; k < N; ++k) {
+    float row[N];
+    nxn_load_row<N>(Ps + N * k, row);
     float s = 0.0f;
 #pragma unroll
-    for (int j = 0; j < N; ++j) s += pin[N * k + j];
+    for (int j = 0; j < N; ++j) s += row[j];
     const float r = rcp(s);
 #pragma unroll
-    for (int j = 0; j < N; ++j) p[N * k + j] = pin[N * k + j] * r;
+    for (int j = 0; j < N; ++j) p[N * k + j] = row[j] * r;
   }
   float v[N - 1];
 #pragma unroll
@@ -472,6 +475,78 @@ __device__ __forceinline__ void nxn_backward(const float pin[N * N], const float
         if (l != q) c = fmaf(p[N * k + l], lam[q] - lam[l], c);
       out[N * k + q] = p[N * k + q] * (D[q] - c);
     }
+  }
+}
+
+// The same backward with P kept in its shared-memory row (for large n, where
+// holding P and the Hessian in registers puts them in local memory):
+// pass 1 rescales each row of P to unit sum in place and accumulates the
+// edge weights, pass 2 forms v from rows of P and dP, pass 3 forms dX row by
+// row into the same row of shared memory.  `row` holds P on entry and dX on
+// return.
+template <int N>
+__device__ __forceinline__ void nxn_backward_smem(float* row, const float* Gs) {
+  NxnAccum<N> acc;
+  acc.reset(0.0f);
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    float q[N];
+    nxn_row_ld<N>(row + N * k, q);
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) s += q[j];
+    const float r = rcp(s);
+#pragma unroll
+    for (int j = 0; j < N; ++j) q[j] *= r;
+    nxn_row_st<N>(row + N * k, q);
+    acc.add(q);
+  }
+  float v[N - 1];
+#pragma unroll
+  for (int l = 0; l < N - 1; ++l) v[l] = 0.0f;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    float q[N], G[N];
+    nxn_row_ld<N>(row + N * k, q);
+    nxn_row_ld<N>(Gs + N * k, G);
+#pragma unroll
+    for (int l = 0; l < N - 1; ++l) {
+      float d = 0.0f;
+#pragma unroll
+      for (int j = 0; j < N; ++j)
+        if (j != l) d = fmaf(q[j], G[l] - G[j], d);
+      v[l] = fmaf(q[l], d, v[l]);
+    }
+  }
+  float wmax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+#pragma unroll
+    for (int k = j + 1; k < N; ++k) wmax = fmaxf(wmax, acc.w[j][k]);
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+#pragma unroll
+    for (int k = j + 1; k < N; ++k) acc.w[j][k] = fmaf(1e-7f, wmax, acc.w[j][k]);
+  float lam[N];
+  nxn_solve<N>(acc.w, v, lam);
+  lam[N - 1] = 0.0f;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    float q[N], G[N], o[N];
+    nxn_row_ld<N>(row + N * k, q);
+    nxn_row_ld<N>(Gs + N * k, G);
+#pragma unroll
+    for (int c = 0; c < N; ++c) {
+      float d = 0.0f, e = 0.0f;
+#pragma unroll
+      for (int j = 0; j < N; ++j)
+        if (j != c) {
+          d = fmaf(q[j], G[c] - G[j], d);
+          e = fmaf(q[j], lam[c] - lam[j], e);
+        }
+      o[c] = q[c] * (d - e);
+    }
+    nxn_row_st<N>(row + N * k, o);
   }
 }
 
@@ -563,12 +638,12 @@ __global__ void __launch_bounds__(TILE, (nxn_minb<N, FWD>())) nxn_kernel(const N
           bp[N - 1] = 0.0f;
         }
       } else {
-        // dX goes straight into the token's own row of s0 (each thread
-        // touches only its own rows)
-        float pin[S::NN];
-#pragma unroll
-        for (int e = 0; e < S::NN; ++e) pin[e] = s0[tid * S::STRIDE + e];
-        nxn_backward<N>(pin, s1 + tid * S::STRIDE, s0 + tid * S::STRIDE);
+        // P is read from the token's own row of s0 and dX written back
+        // there (each thread touches only its own rows)
+        if constexpr (N >= kNxnSmemFrom)
+          nxn_backward_smem<N>(s0 + tid * S::STRIDE, s1 + tid * S::STRIDE);
+        else
+          nxn_backward<N>(s0 + tid * S::STRIDE, s1 + tid * S::STRIDE, s0 + tid * S::STRIDE);
       }
     }
     if constexpr (FWD && N < kNxnSmemFrom) {
