@@ -91,8 +91,8 @@ __device__ __forceinline__ void token_compute(const KParams& a, int64_t tok, boo
       const unsigned miss = __ballot_sync(0xffffffffu, valid && !ok);
       if ((threadIdx.x & 31) == 0 && miss != 0u) atomicAdd(a.nonconv, (unsigned long long)__popc(miss));
     }
-    if constexpr (M == Mode::Recompute) implicit_backward(p, in1, out0);
-    if constexpr (M == Mode::Fused) implicit_backward(out0, in1, out1);
+    if constexpr (M == Mode::Recompute) implicit_backward<false>(p, in1, out0);
+    if constexpr (M == Mode::Fused) implicit_backward<false>(out0, in1, out1);
   }
 }
 

@@ -243,14 +243,21 @@ __device__ __forceinline__ bool newton_forward(const Tok& x, Tok& p, float beta[
 // The two sums are written in their difference forms (valid for unit row
 // sums, enforced first) so that nothing cancels when a row is nearly one-hot;
 // H is regularised by 1e-7 * max weight.
+// RENORM rescales the rows of P to unit sums first (a stored P, possibly
+// rounded to bf16); a P straight from an evaluation has them already.
+template <bool RENORM = true>
 __device__ __forceinline__ void implicit_backward(const Tok& pin, const Tok& G, Tok& dx) {
   Tok p;
+  if constexpr (RENORM) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 s = add2(pin.v[2 * k], pin.v[2 * k + 1]);
-    const float2 r = splat(rcp(s.x + s.y));
-    p.v[2 * k] = mul2(pin.v[2 * k], r);
-    p.v[2 * k + 1] = mul2(pin.v[2 * k + 1], r);
+    for (int k = 0; k < 4; ++k) {
+      const float2 s = add2(pin.v[2 * k], pin.v[2 * k + 1]);
+      const float2 r = splat(rcp(s.x + s.y));
+      p.v[2 * k] = mul2(pin.v[2 * k], r);
+      p.v[2 * k + 1] = mul2(pin.v[2 * k + 1], r);
+    }
+  } else {
+    p = pin;
   }
   Tok D;
 #pragma unroll

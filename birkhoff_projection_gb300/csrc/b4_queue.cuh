@@ -74,7 +74,7 @@ __device__ __forceinline__ void queue_finish(const KParams& a, int tok, const To
   } else {
     Tok G, dx;
     TileIO<TIn>::gload_vec(a.gin[1], tok, G.v);
-    implicit_backward(p, G, dx);
+    implicit_backward<false>(p, G, dx);  // p is an evaluation: unit row sums
     if constexpr (M == Mode::Fused) {
       TileIO<TOut>::gstore_vec(a.gout[0], tok, p.v);
       TileIO<TOut>::gstore_vec(a.gout[1], tok, dx.v);
