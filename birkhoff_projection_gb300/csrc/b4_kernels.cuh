@@ -203,119 +203,6 @@ __global__ void __launch_bounds__(TILE, MINB) stream_kernel(const __grid_constan
   }
 }
 
-// Per-warp variant: every warp runs its own pipeline over 32-token sub-tiles
-// (its own TMA ring, mbarriers and output buffers; lane 0 issues the copies),
-// so warps never wait for each other.  In the CTA-tile kernel above every
-// tile ends at a block barrier and all warps wait for the slowest one's
-// Newton iterations; here a fast warp simply moves on to its next sub-tile.
-template <Mode M, class TIn, class TOut, int WARPS, int NSTAGE, int NOSTAGE>
-struct WarpShape {
-  static constexpr int NIN = ModeTraits<M>::NIN;
-  static constexpr int NOUT = ModeTraits<M>::NOUT;
-  static constexpr int SUB_IN = 32 * TileIO<TIn>::ROW_BYTES;    // one input, one sub-tile
-  static constexpr int SUB_OUT = 32 * TileIO<TOut>::ROW_BYTES;  // one output, one sub-tile
-  static constexpr int STAGE_BYTES = NIN * SUB_IN;
-  static constexpr int OSTAGE_BYTES = NOUT * SUB_OUT;
-  static constexpr int WARP_BYTES = NSTAGE * STAGE_BYTES + NOSTAGE * OSTAGE_BYTES;
-  static constexpr int BAR_OFFSET = WARPS * WARP_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFFSET + 8 * WARPS * NSTAGE + 1024;
-  static_assert(SUB_IN % 1024 == 0 && SUB_OUT % 1024 == 0, "sub-tile buffers stay 1024-aligned");
-};
-
-template <Mode M, class TIn, class TOut, int WARPS, int NSTAGE, int NOSTAGE, int MINB>
-__global__ void __launch_bounds__(WARPS * 32, MINB) warp_stream_kernel(const __grid_constant__ KParams a) {
-  using W = WarpShape<M, TIn, TOut, WARPS, NSTAGE, NOSTAGE>;
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned char* in_stage = smem + warp * W::WARP_BYTES;
-  unsigned char* out_stage = in_stage + NSTAGE * W::STAGE_BYTES;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + W::BAR_OFFSET) + warp * NSTAGE;
-
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar[s], 1);
-    mbar_init_fence();
-    if (warp == 0) {
-#pragma unroll
-      for (int k = 0; k < W::NIN; ++k) prefetch_tmap(&a.in[k]);
-#pragma unroll
-      for (int k = 0; k < W::NOUT; ++k) prefetch_tmap(&a.out[k]);
-    }
-  }
-  __syncwarp();
-
-  const int nsub = a.ntiles;
-  const int gw = blockIdx.x * WARPS + warp;
-  const int nw = gridDim.x * WARPS;
-  // loads in flight, kept by lane 0 (as in stream_kernel)
-  uint32_t pending = 0, pph = 0;
-  auto issue = [&](int s, int j, int sub) {
-    mbar_arrive_expect_tx(&bar[s], W::STAGE_BYTES);
-#pragma unroll
-    for (int k = 0; k < W::NIN; ++k)
-      tma_load_2d(in_stage + s * W::STAGE_BYTES + k * W::SUB_IN, &a.in[k], &bar[s], 0, sub * 32);
-    pending |= 1u << s;
-    pph = (pph & ~(1u << s)) | ((static_cast<uint32_t>(j / NSTAGE) & 1u) << s);
-  };
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < NSTAGE; ++s) {
-      const int sub = gw + s * nw;
-      if (sub < nsub) issue(s, s, sub);
-    }
-  }
-
-  bool failed = false;
-  int it = 0;
-  for (int sub = gw; sub < nsub; sub += nw, ++it) {
-    const int s = it % NSTAGE;
-    const uint32_t ph = static_cast<uint32_t>(it / NSTAGE) & 1u;
-    const bool ok = mbar_wait(&bar[s], ph, kWaitLimitNs);
-    if (!__all_sync(0xffffffffu, ok)) {
-      failed = true;
-      break;
-    }
-    Tok in0, in1;
-    TileIO<TIn>::load(in_stage + s * W::STAGE_BYTES, lane, in0.v);
-    if constexpr (W::NIN == 2) TileIO<TIn>::load(in_stage + s * W::STAGE_BYTES + W::SUB_IN, lane, in1.v);
-    __syncwarp();  // stage s fully read: refill it
-    if (lane == 0) {
-      pending &= ~(1u << s);
-      const int next = sub + NSTAGE * nw;
-      if (next < nsub) issue(s, it + NSTAGE, next);
-    }
-
-    const int64_t tok = static_cast<int64_t>(sub) * 32 + lane;
-    const bool valid = tok < a.T;
-    Tok out0, out1;
-    token_compute<M, TIn>(a, tok, valid, in0, in1, out0, out1);
-
-    const int os = it % NOSTAGE;
-    if (lane == 0) bulk_wait_read<NOSTAGE - 1>();  // the store that used stage os is done
-    __syncwarp();
-    unsigned char* ob = out_stage + os * W::OSTAGE_BYTES;
-    TileIO<TOut>::store(ob, lane, out0.v);
-    if constexpr (W::NOUT == 2) TileIO<TOut>::store(ob + W::SUB_OUT, lane, out1.v);
-    fence_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-#pragma unroll
-      for (int k = 0; k < W::NOUT; ++k) tma_store_2d(&a.out[k], ob + k * W::SUB_OUT, 0, sub * 32);
-      bulk_commit();
-    }
-  }
-  if (lane == 0) {
-    bulk_wait_all();
-    if (failed) {
-      if (a.fault != nullptr) atomicOr(a.fault, 1u);
-      for (int s = 0; s < NSTAGE; ++s)
-        if (pending & (1u << s)) (void)mbar_wait(&bar[s], (pph >> s) & 1u, kWaitLimitNs);
-    }
-  }
-}
-
 // Plain-load variant for base addresses without 16-byte alignment.
 template <Mode M, class TIn, class TOut>
 __global__ void __launch_bounds__(256) plain_kernel(const __grid_constant__ KParams a) {

@@ -74,11 +74,11 @@ namespace b4 {
 #ifndef B4_Q_MINB_FUSED
 #define B4_Q_MINB_FUSED 5
 #endif
-#ifndef B4_FWD_PERWARP
-#define B4_FWD_PERWARP 0
+#ifndef B4_Q_MINB_RECOMPUTE
+#define B4_Q_MINB_RECOMPUTE 7
 #endif
-#ifndef B4_BWD_PERWARP
-#define B4_BWD_PERWARP 0
+#ifndef B4_Q_MINB_BF16
+#define B4_Q_MINB_BF16 8
 #endif
 
 template <Mode M, class TIn>
@@ -88,8 +88,6 @@ struct TileCfg {
   static constexpr int NSTAGE = STREAMING ? B4_BWD_NSTAGE : B4_FWD_NSTAGE;
   static constexpr int NOSTAGE = STREAMING ? B4_BWD_NOSTAGE : B4_FWD_NOSTAGE;
   static constexpr int MINB = STREAMING ? B4_BWD_MINB : (M == Mode::Forward ? B4_FWD_MINB : B4_FUSED_MINB);
-  // per-warp pipelines (TILE/32 independent warps per CTA) or CTA tiles
-  static constexpr bool PERWARP = STREAMING ? (B4_BWD_PERWARP != 0) : (B4_FWD_PERWARP != 0);
 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -155,7 +153,14 @@ inline void* advance(void* p, int64_t tokens) {
 template <Mode M, class TIn, class TOut>
 cudaError_t launch_queue(const LaunchArgs& la, cudaStream_t stream, int dev, int nsm) {
   using Q = QueueShape<M, TIn, TOut, B4_Q_WARPS, B4_Q_NSTAGE, B4_Q_QC>;
-  constexpr int MINB = M == Mode::Forward ? B4_Q_MINB_FWD : B4_Q_MINB_FUSED;
+  // Register caps, swept on GB300: the fp32 fused pass (256 B per token,
+  // close to HBM) is fastest with 5 CTAs per SM, the compute-heavier bf16
+  // passes and the recompute pass with more.
+  constexpr bool BF16 = std::is_same<TIn, bf16_t>::value;
+  constexpr int MINB = M == Mode::Forward ? B4_Q_MINB_FWD
+                       : BF16             ? B4_Q_MINB_BF16
+                       : M == Mode::Fused ? B4_Q_MINB_FUSED
+                                          : B4_Q_MINB_RECOMPUTE;
   auto kern = queue_kernel<M, TIn, TOut, B4_Q_WARPS, B4_Q_NSTAGE, B4_Q_QC, B4_Q_K1, B4_Q_K2, MINB>;
   static std::atomic<int> cap_cache[64];
   int grid_cap = dev < 64 ? cap_cache[dev].load(std::memory_order_acquire) : 0;
@@ -259,11 +264,9 @@ cudaError_t launch(const LaunchArgs& la, cudaStream_t stream) {
       return launch_queue<M, TIn, TOut>(la, stream, dev, nsm);
   }
 
-  using WS = WarpShape<M, TIn, TOut, C::TILE / 32, C::NSTAGE, C::NOSTAGE>;
-  auto kern = C::PERWARP ? warp_stream_kernel<M, TIn, TOut, C::TILE / 32, C::NSTAGE, C::NOSTAGE, C::MINB>
-                         : stream_kernel<M, TIn, TOut, C::TILE, C::NSTAGE, C::NOSTAGE, C::MINB>;
-  const int smem_bytes = C::PERWARP ? WS::SMEM_BYTES : S::SMEM_BYTES;
-  const int box_rows = C::PERWARP ? 32 : C::TILE;
+  auto kern = stream_kernel<M, TIn, TOut, C::TILE, C::NSTAGE, C::NOSTAGE, C::MINB>;
+  const int smem_bytes = S::SMEM_BYTES;
+  const int box_rows = C::TILE;
   // Persistent grid size (SMs x resident CTAs), worked out once per device
   // for this kernel: the shared-memory opt-in and the occupancy query are
   // host calls that would otherwise dominate small launches.
@@ -303,8 +306,7 @@ cudaError_t launch(const LaunchArgs& la, cudaStream_t stream) {
     }
     if (use_tma) {
       p.ntiles = static_cast<int32_t>((n + box_rows - 1) / box_rows);
-      const int64_t per_cta = C::TILE / box_rows;  // tiles a CTA works on at once
-      const int grid = static_cast<int>(std::min<int64_t>((p.ntiles + per_cta - 1) / per_cta, grid_cap));
+      const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, grid_cap));
       kern<<<grid, C::TILE, smem_bytes, stream>>>(p);
     } else {
       const int64_t blocks = (n + 255) / 256;
