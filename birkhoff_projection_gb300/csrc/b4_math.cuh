@@ -61,12 +61,12 @@ __device__ __forceinline__ void eval_log(const Tok& x, const float beta[3], Tok&
   }
 }
 
-// The same row softmax after beta_j -= d_j, from the previous (row-normalised)
-// p: p_ij <- p_ij 2^{-d_j} / sum_k p_ik 2^{-d_k}.  Mathematically identical to
+// The same row softmax after beta_j += e_j, from the previous (row-normalised)
+// p: p_ij <- p_ij 2^{e_j} / sum_k p_ik 2^{e_k}.  Mathematically identical to
 // eval_log at the new beta; its rounding does not grow with |X|.
-__device__ __forceinline__ void eval_mul(Tok& p, const float d[3]) {
-  const float2 w01 = make_float2(ex2(-d[0]), ex2(-d[1]));
-  const float2 w23 = make_float2(ex2(-d[2]), 1.0f);
+__device__ __forceinline__ void eval_mul(Tok& p, const float e[3]) {
+  const float2 w01 = make_float2(ex2(e[0]), ex2(e[1]));
+  const float2 w23 = make_float2(ex2(e[2]), 1.0f);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 q01 = mul2(p.v[2 * i], w01);
@@ -117,9 +117,13 @@ __device__ __forceinline__ void laplacian_weights(const Tok& p, float w[6], floa
 // w_aj w_ak / d_a to the remaining edge weights (a Schur complement of a
 // Laplacian is a Laplacian), so every pivot d is a sum of positive terms and
 // nothing cancels in the matrix however small the weights.
+// GUARD keeps every pivot >= 1e-30; without it the weights must include a
+// positive ridge (every pivot is then a sum of positive terms).
+template <bool GUARD = true>
 __device__ __forceinline__ void laplacian_solve(const float w[6], const float g[3], float x[3]) {
+  auto pivot = [](float v) { return GUARD ? fmaxf(v, 1e-30f) : v; };
   // eliminate column 0
-  const float d0 = fmaxf(w[0] + w[1] + w[2], 1e-30f);
+  const float d0 = pivot(w[0] + w[1] + w[2]);
   const float i0 = rcp(d0);
   const float t1 = w[0] * i0, t2 = w[1] * i0;
   const float w12 = fmaf(t1, w[1], w[3]);
@@ -128,10 +132,10 @@ __device__ __forceinline__ void laplacian_solve(const float w[6], const float g[
   const float g1 = fmaf(t1, g[0], g[1]);
   const float g2 = fmaf(t2, g[0], g[2]);
   // eliminate column 1
-  const float d1 = fmaxf(w12 + w13, 1e-30f);
+  const float d1 = pivot(w12 + w13);
   const float i1 = rcp(d1);
   const float u2 = w12 * i1;
-  const float d2 = fmaxf(fmaf(u2, w13, w23), 1e-30f);
+  const float d2 = pivot(fmaf(u2, w13, w23));
   const float h2 = fmaf(u2, g1, g2);
   // back substitution
   x[2] = h2 * rcp(d2);
@@ -195,7 +199,7 @@ __device__ __forceinline__ int newton_run(Tok& p, float beta[3], float& prev, in
     float w[6], d[3];
     const float g[3] = {g01.x, g01.y, g23.x};
     laplacian_weights(p, w, kRidge);
-    laplacian_solve(w, g, d);
+    laplacian_solve<false>(w, g, d);  // the ridge keeps every pivot positive
     // The step is clamped to kClamp in the max norm (rcp(0) = inf leaves a
     // zero step unscaled).  From the kDampFrom-th step on it is also damped by
     // 1/(1 + lambda) when the Newton decrement lambda = sqrt(g^T H^-1 g)
@@ -208,11 +212,13 @@ __device__ __forceinline__ int newton_run(Tok& p, float beta[3], float& prev, in
       if (lam2 > 1.0f) lim = rcp(1.0f + lam2 * rsqrt(lam2));
     }
     const float dmax = max3(fabsf(d[0]), fabsf(d[1]), fabsf(d[2]));
-    const float scale = LOG2E * fminf(lim, kClamp * rcp(dmax));
+    // the negated step in base-2 units, beta_j += e_j: -log2(e) min(lim,
+    // kClamp / dmax) (rcp(0) = inf leaves a zero step zero)
+    const float nscale = fmaxf(-LOG2E * lim, (-LOG2E * kClamp) * rcp(dmax));
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
-      d[j] *= scale;  // base-2 units
-      beta[j] -= d[j];
+      d[j] *= nscale;
+      beta[j] += d[j];
     }
     if (REFRESH && (k & (kRefreshEvery - 1)) == kRefreshEvery - 1) {
       Tok xr;
