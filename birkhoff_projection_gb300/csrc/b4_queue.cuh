@@ -61,7 +61,7 @@ __device__ __forceinline__ void queue_finish(const KParams& a, int tok, const To
     TileIO<TOut>::gstore_vec(a.gout[0], tok, p.v);
     if (a.b != nullptr) {
       const float b0 = beta[0] * LN2, b1 = beta[1] * LN2, b2 = beta[2] * LN2;
-      float* bp = a.b + 4 * tok;
+      float* bp = a.b + 4 * static_cast<int64_t>(tok);  // 4 tok can pass 2^31
       if (a.b_vec) {
         *reinterpret_cast<float4*>(bp) = make_float4(b0, b1, b2, 0.0f);
       } else {
