@@ -130,18 +130,17 @@ def backward(dP: torch.Tensor, *, P: torch.Tensor = None, X: torch.Tensor = None
     return out
 
 
-def forward_backward(X: torch.Tensor, dP: torch.Tensor, *, want_P: bool = True):
-    """One fused pass: (P, dX) (P is None if not wanted)."""
-    T = _check_tokens(X, "X")
+def forward_backward(X: torch.Tensor, dP: torch.Tensor, *, want_P: bool = True,
+                     schedule: str = "default"):
+    """One fused pass: (P, dX) (P is None if not wanted).  schedule:
+    "default", "queue" or "lane" (birkhoff4_schedule)."""
+    _check_tokens(X, "X")
     _check_tokens(dP, "dP")
     if X.shape != dP.shape or X.dtype != dP.dtype or X.device != dP.device:
         raise ValueError("X and dP must match in shape, dtype and device")
     P = torch.empty_like(X) if want_P else None
     dX = torch.empty_like(dP)
-    fn = (lib().birkhoff4_forward_backward if X.dtype == torch.float32
-          else lib().birkhoff4_forward_backward_bf16)
-    with _on_device(X):
-        check(fn(_ptr(X), _ptr(dP), _ptr(P), _ptr(dX), T, _stream(X)), "birkhoff4_forward_backward")
+    _fused_pass(X, dP, P, dX, schedule=schedule)
     return P, dX
 
 
