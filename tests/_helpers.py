@@ -58,6 +58,15 @@ def rne_bf16(x) -> np.ndarray:
     return np.ldexp(r, e - 8)
 
 
+def rna_tf32(x) -> np.ndarray:
+    """Round fp32 values to TF32 as cvt.rna.tf32.f32 does (nearest, ties
+    away from zero): add half of the 13 dropped mantissa bits to the
+    magnitude field, then clear them.  Returns float64."""
+    bits = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x1000) & ~np.uint64(0x1FFF)
+    return bits.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def bf16_ulp(x) -> np.ndarray:
     """Spacing of bf16 numbers at |x| (normal range)."""
     x = np.abs(np.asarray(x, dtype=np.float64))

@@ -23,6 +23,7 @@ import torch
 
 from birkhoff_projection_gb300 import eot, workloads
 from oracle import eot as oeot
+from _helpers import rna_tf32
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -334,37 +335,64 @@ def _hvp_case(n, m, d, eps, seed):
 
 
 def _hvp_bound(X, Y, f, g, log_a, log_b, V, eps):
-    """Element bound of H v, row by row.  Every term of
-        (H v)_i = 2 a_i v_i - (2/eps) sum_j pi_ij (df_i + dg_j - dC_ij) y_j
-    is a plan application, so each row carries the plan's per-row relative
-    error delta_i of the transport bound (score rounding through the
-    exponential, TF32 rounding of pi and of the values, 2^-9 together, and
-    fp32 accumulation over m_pad keys), applied to
-    sum_j pi_ij (|df_i + dg_j| + |dC_ij|) |y_j|.  The solve for (df, dg) is
-    taken to inherit the same relative error (its conditioning in the
-    combination df_i + dg_j that enters H v is taken as 1), and 2 a_i v_i is
-    rounded once (2^-21).  (df, dg) come from the oracle's dense solve."""
+    """Element bound of H v, entry by entry of the plan.  The kernel forms
+        (H v)_i = 2 a_i v_i - (2/eps) [(df_i - 2 xv_i) (pi Y)_i
+                                        + sum_j pi_ij dg_j y_j
+                                        + 2 sum_j pi_ij (v_i . y_j) y_j]
+    (xv_i = x_i . v_i), each sum a plan application.  Plan entry pi_ij
+    carries a relative error delta_ij:
+      * its score x_i . y_j: the operands are rounded to TF32 exactly as
+        the kernel rounds them (cvt.rna), so that part of the error is
+        computed here, not bounded; fp32 accumulation adds d_pad 2^-23 of
+        sum_k |x_ik y_jk| (rounded operands);
+      * norms, biases, ex2 and the exponent's combination as in row_bound,
+        but with this entry's own magnitudes;
+      * the second product: 2^-10 for pi (TF32 truncation; f16 rounds to
+        2^-11) plus 2^-11 for the values, and fp32 accumulation over m_pad
+        keys.
+    Each term's error is delta_ij times its own magnitude:
+    |df_i - 2 xv_i| + |dg_j| + 2 |v_i . y_j|, plus |df_i| + |dg_j| for the
+    solve, which is taken to inherit the same relative error (its
+    conditioning in the combination df_i + dg_j that enters H v is taken
+    as 1).  The moment weights v_i . y_j are a TF32 product of their own
+    (rounded the same way, computed here).  2 a_i v_i is rounded once
+    (2^-21).  (df, dg) come from the oracle's dense solve."""
     args = (np64(X), np64(Y), np64(f), np64(g), np64(log_a), np64(log_b), eps)
     Xn, Yn, Vn = np64(X), np64(Y), np64(V)
-    n, m = Xn.shape[0], Yn.shape[0]
-    a, b = np.exp(np64(log_a)), np.exp(np64(log_b))
-    P = oeot.plan64(*args)
-    fr = np.abs(np64(f)) + eps * np.abs(np64(log_a))
+    fn, gn, la, lb = np64(f), np64(g), np64(log_a), np64(log_b)
+    n, d = Xn.shape
+    m = Yn.shape[0]
+    d_pad = -(-d // 32) * 32
     m_pad = -(-m // 256) * 256
-    delta = (np.expm1(row_bound(Xn, Yn, np64(g), np64(log_b), fr, eps, eot.TF32) / 2.0 / eps + 2.0 ** -20)
-             + 2.0 ** -9 + m_pad * 2.0 ** -23)
-    dC = 2.0 * ((Xn * Vn).sum(1)[:, None] - Vn @ Yn.T)
+    a, b = np.exp(la), np.exp(lb)
+    P = oeot.plan64(*args)
+    Xt, Yt, Vt = rna_tf32(Xn), rna_tf32(Yn), rna_tf32(Vn)
+    xy = Xn @ Yn.T
+    score = np.abs(Xt @ Yt.T - xy) + d_pad * 2.0 ** -23 * (np.abs(Xt) @ np.abs(Yt).T)
+    N = (Xn * Xn).sum(1)[:, None]
+    B = (Yn * Yn).sum(1)[None, :]
+    fr = (np.abs(fn) + eps * np.abs(la))[:, None]
+    t = (2.0 * score + d * 2.0 ** -23 * (N + B)
+         + 2.0 ** -21 * (2.0 * np.abs(xy) + np.abs(gn)[None, :] + B + eps * np.abs(lb)[None, :] + fr + N)
+         + eps * 2.0 ** -18)
+    delta = np.expm1(t / eps + 2.0 ** -20) + 2.0 ** -10 + 2.0 ** -11 + m_pad * 2.0 ** -23
+    xv = (Xn * Vn).sum(1)
+    vy = Vn @ Yn.T
+    dC = 2.0 * (xv[:, None] - vy)
     A = np.block([[np.diag(a), P], [P.T, np.diag(b)]])
     z = np.linalg.lstsq(A, np.r_[(P * dC).sum(1), (P * dC).sum(0)], rcond=None)[0]
-    S = np.abs(z[:n, None] + z[None, n:]) + np.abs(dC)
-    return (2.0 / eps) * delta[:, None] * ((P * S) @ np.abs(Yn)) + 2.0 ** -21 * 2.0 * a[:, None] * np.abs(Vn)
+    df, dg = z[:n], z[n:]
+    S = (np.abs(df - 2.0 * xv) + np.abs(df))[:, None] + 2.0 * np.abs(dg)[None, :] + 2.0 * np.abs(vy)
+    moment = 2.0 * (np.abs(Vt @ Yt.T - vy) + d_pad * 2.0 ** -23 * (np.abs(Vt) @ np.abs(Yt).T))
+    return ((2.0 / eps) * ((P * (delta * S + moment)) @ np.abs(Yn))
+            + 2.0 ** -21 * 2.0 * a[:, None] * np.abs(Vn))
 
 
 @pytest.mark.parametrize("n,m,d,eps", [(300, 400, 8, 0.5), (500, 350, 32, 1.0), (200, 600, 3, 0.5)])
 def test_hvp_parity(n, m, d, eps):
     """eot_hvp against the dense oracle at the same potentials, every element
-    within twice the row-wise bound of _hvp_bound (CG runs long enough to
-    converge at these sizes)."""
+    within the bound of _hvp_bound itself (CG runs long enough to converge
+    at these sizes)."""
     X, Y, log_a, log_b, f, g = _hvp_case(n, m, d, eps, seed=n + m + d)
     V = torch.randn(n, d, generator=torch.Generator().manual_seed(d)).to(DEV)
     Hv = eot.hvp(X, Y, f, g, log_a, log_b, V, eps, cg_iters=150)
@@ -372,7 +400,7 @@ def test_hvp_parity(n, m, d, eps):
     bound = _hvp_bound(X, Y, f, g, log_a, log_b, V, eps)
     err = np.abs(np64(Hv) - ref)
     assert np.all(np.isfinite(np64(Hv)))
-    worst = (err / (2.0 * bound)).max()
+    worst = (err / bound).max()
     assert worst <= 1.0, (worst, np.unravel_index((err / bound).argmax(), err.shape))
 
 
