@@ -530,9 +530,17 @@ def main():
     line["issue_ceiling"] = {
         k: {"warp_inst_per_32_tokens": v, "ceiling_tokens_per_s": issue_ceiling(v, nsm, mhz)}
         for k, v in counts.items()} or None
-    if counts.get("forward_f32_sigma1"):
-        ic = line["issue_ceiling"]["forward_f32_sigma1"]
-        ic["achieved_frac"] = (T / (fwd_avg * 1e-3)) / ic["ceiling_tokens_per_s"]
+    # achieved tokens/s of each counted kernel against its issue ceiling
+    achieved = {"forward_f32_sigma1": T / (fwd_avg * 1e-3), "backward_f32_sigma1": T / (bwd_avg * 1e-3)}
+    hard = line.get("hard_configs") or {}
+    if "sigma10" in hard:
+        achieved["forward_f32_sigma10"] = hard["sigma10"]["fwd_tokens_per_s"]
+    if "mhc_bf16" in hard:
+        achieved["fused_bf16_mhc"] = hard["mhc_bf16"]["fused_tokens_per_s"]
+    for k, v in achieved.items():
+        if counts.get(k):
+            ic = line["issue_ceiling"][k]
+            ic["achieved_frac"] = v / ic["ceiling_tokens_per_s"]
     if not args.no_cpu_baseline:
         idx = slice(0, 1 << 22)
         line["cpu_baseline"] = cpu_baseline(X[idx].double().cpu().numpy(),
