@@ -2,7 +2,8 @@
 // host-streaming forward + backward with its device staging area in a
 // file-scope static device array instead of caller-allocated memory.
 //
-// For callers that cannot allocate device memory: code that must not call
+// The pages have no counterpart to this entry point; it is a deployment
+// variant.  For callers that cannot allocate device memory: code that must not call
 // cudaMalloc because it synchronises the device (latency-critical loops), code
 // whose device memory belongs to another framework's allocator or pool, and
 // plugins or sandboxed hosts where creating device allocations is not

@@ -243,8 +243,8 @@ int birkhoff4_forward_backward_host(const void *X_h, const void *dP_h, void *P_h
 /* module loading (the default) that lookup loads the library's module on  */
 /* the device, which reserves the 32 MiB there and may synchronise the     */
 /* device; the array then stays reserved until the process exits.  Make   */
-/* one warm-up call before latency-critical work and before any stream     */
-/* capture.  The address is cached per device and CUDA context and looked  */
+/* one warm-up call before latency-critical work.  The address is cached   */
+/* per device and CUDA context and looked                                  */
 /* up again after a context change (cudaDeviceReset included).  Apart from */
 /* that lookup the call only enqueues copies and kernels; it never calls   */
 /* cudaMalloc, cudaFree or any other allocating routine.  Every call uses  */
