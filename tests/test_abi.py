@@ -273,3 +273,14 @@ def test_python_binding_refuses_cpu_tensors():
         b4.backward(x, P=x)
     with pytest.raises(ValueError):
         b4.sinkhorn(x)
+
+
+def test_missing_library_raises(monkeypatch):
+    """With no built library the binding raises instead of computing
+    anything another way: there is no fallback path."""
+    from birkhoff_projection_gb300 import _build
+
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_build, "build", lambda *a, **k: "/nonexistent/libbirkhoff4.so")
+    with pytest.raises(_lib.Birkhoff4Error):
+        _lib.lib()
