@@ -33,6 +33,14 @@ constexpr int kNxnDampFrom = 4;
 #define B4_NXN_SMEM_FROM 7
 #endif
 constexpr int kNxnSmemFrom = B4_NXN_SMEM_FROM;
+// The backward keeps P in shared memory (nxn_backward_smem) for odd n and
+// from n = 7 on.  Measured on GB300 (1 GiB of X per n): n = 3 went 0.594 ->
+// 0.532 ms and n = 5 0.623 -> 0.588 ms that way, while n = 4 and 6 are
+// faster with P in registers (0.568 against 0.584 ms, 0.647 against 0.657).
+template <int N>
+struct NxnBwdSmem {
+  static constexpr bool value = (N % 2 == 1) || N >= 7;
+};
 
 // Row softmax of (x log2e + beta), rows shifted by their maximum; x is the
 // token's row in shared memory.
@@ -398,7 +406,8 @@ __device__ __forceinline__ bool nxn_newton_smem(float* row, const float* xg, flo
 // Backward of one n x n token [s2.2], the difference forms of the 4 x 4
 // kernel: D_kl = sum_j p_kj (G_kl - G_kj), v_l = sum_k p_kl D_kl,
 // H lambda = v (lambda_{N-1} = 0, ridge 1e-7 max w),
-// dX_kq = p_kq (D_kq - sum_l p_kl (lambda_q - lambda_l)).  G is the token's
+// dX_kq = p_kq (D_kq - sum_l p_kl (lambda_q - lambda_l)); the sums over the
+// other columns of a row are formed in O(n) by nxn_excl_diff.  G is the token's
 // row in shared memory; P is read from its row Ps into registers first, so
 // dX may be written to `out` == Ps.  Both passes over D go row by
 // row -- a row of G is loaded, its row of D formed and used -- so that only
@@ -410,16 +419,49 @@ __device__ __forceinline__ void nxn_load_row(const float* g, float G[N]) {
   for (int j = 0; j < N; ++j) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(G[j]) : "r"(smem_addr(g + j)));
 }
 
+// out_c = sum_{j != c} q_j (h_c - h_j) for every c of one row.  From n = 5
+// on in O(N) instead of O(N^2): with R_c and S_c the sums of q_j and of
+// q_j h_j over j != c, each a prefix sum (j < c) plus a suffix sum (j > c),
+// out_c = h_c R_c - S_c.  R_c is a sum of the other entries of the row,
+// never 1 - q_c, so nothing cancels when the row is nearly one-hot.
+// Measured on GB300 (1 GiB of X per n), the n = 7 and 8 backwards went
+// 0.796 -> 0.647 ms and 1.032 -> 0.780 ms; for n <= 4 the direct sums are
+// cheaper and stay.
+template <int N>
+__device__ __forceinline__ void nxn_excl_diff(const float* q, const float h[N], float out[N]) {
+  if constexpr (N <= 4) {
+#pragma unroll
+    for (int c = 0; c < N; ++c) {
+      float s = 0.0f;
+#pragma unroll
+      for (int j = 0; j < N; ++j)
+        if (j != c) s = fmaf(q[j], h[c] - h[j], s);
+      out[c] = s;
+    }
+  } else {
+    float pr[N], ps[N];
+    float a = 0.0f, b = 0.0f;
+#pragma unroll
+    for (int c = 0; c < N; ++c) {
+      pr[c] = a;
+      ps[c] = b;
+      a += q[c];
+      b = fmaf(q[c], h[c], b);
+    }
+    a = 0.0f;
+    b = 0.0f;
+#pragma unroll
+    for (int c = N - 1; c >= 0; --c) {
+      out[c] = fmaf(h[c], pr[c] + a, -(ps[c] + b));
+      a += q[c];
+      b = fmaf(q[c], h[c], b);
+    }
+  }
+}
+
 template <int N>
 __device__ __forceinline__ void nxn_D_row(const float p[N * N], const float G[N], int k, float D[N]) {
-#pragma unroll
-  for (int l = 0; l < N; ++l) {
-    float s = 0.0f;
-#pragma unroll
-    for (int j = 0; j < N; ++j)
-      if (j != l) s = fmaf(p[N * k + j], G[l] - G[j], s);
-    D[l] = s;
-  }
+  nxn_excl_diff<N>(p + N * k, G, D);
 }
 
 template <int N>
@@ -462,19 +504,16 @@ __device__ __forceinline__ void nxn_backward(const float* Ps, const float* Gs, f
   float lam[N];
   nxn_solve<N>(w, v, lam);
   lam[N - 1] = 0.0f;
+  // dX_kq = p_kq sum_{l != q} p_kl ((G_kq - lam_q) - (G_kl - lam_l))
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    float G[N], D[N];
-    nxn_load_row<N>(Gs + N * k, G);
-    nxn_D_row<N>(p, G, k, D);
+    float H[N], E[N];
+    nxn_load_row<N>(Gs + N * k, H);
 #pragma unroll
-    for (int q = 0; q < N; ++q) {
-      float c = 0.0f;
+    for (int q = 0; q < N; ++q) H[q] -= lam[q];
+    nxn_excl_diff<N>(p + N * k, H, E);
 #pragma unroll
-      for (int l = 0; l < N; ++l)
-        if (l != q) c = fmaf(p[N * k + l], lam[q] - lam[l], c);
-      out[N * k + q] = p[N * k + q] * (D[q] - c);
-    }
+    for (int q = 0; q < N; ++q) out[N * k + q] = p[N * k + q] * E[q];
   }
 }
 
@@ -506,17 +545,12 @@ __device__ __forceinline__ void nxn_backward_smem(float* row, const float* Gs) {
   for (int l = 0; l < N - 1; ++l) v[l] = 0.0f;
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    float q[N], G[N];
+    float q[N], G[N], D[N];
     nxn_row_ld<N>(row + N * k, q);
     nxn_row_ld<N>(Gs + N * k, G);
+    nxn_excl_diff<N>(q, G, D);
 #pragma unroll
-    for (int l = 0; l < N - 1; ++l) {
-      float d = 0.0f;
-#pragma unroll
-      for (int j = 0; j < N; ++j)
-        if (j != l) d = fmaf(q[j], G[l] - G[j], d);
-      v[l] = fmaf(q[l], d, v[l]);
-    }
+    for (int l = 0; l < N - 1; ++l) v[l] = fmaf(q[l], D[l], v[l]);
   }
   float wmax = 0.0f;
 #pragma unroll
@@ -532,22 +566,81 @@ __device__ __forceinline__ void nxn_backward_smem(float* row, const float* Gs) {
   lam[N - 1] = 0.0f;
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    float q[N], G[N], o[N];
+    float q[N], H[N], o[N];
     nxn_row_ld<N>(row + N * k, q);
-    nxn_row_ld<N>(Gs + N * k, G);
+    nxn_row_ld<N>(Gs + N * k, H);
 #pragma unroll
-    for (int c = 0; c < N; ++c) {
-      float d = 0.0f, e = 0.0f;
+    for (int c = 0; c < N; ++c) H[c] -= lam[c];
+    nxn_excl_diff<N>(q, H, o);
 #pragma unroll
-      for (int j = 0; j < N; ++j)
-        if (j != c) {
-          d = fmaf(q[j], G[c] - G[j], d);
-          e = fmaf(q[j], lam[c] - lam[j], e);
-        }
-      o[c] = q[c] * (d - e);
-    }
+    for (int c = 0; c < N; ++c) o[c] *= q[c];
     nxn_row_st<N>(row + N * k, o);
   }
+}
+
+// Copy a tile of `nel` floats between global memory and the padded token
+// layout in shared memory (token t at t * STRIDE).  With a 16-byte aligned
+// global tile the copy moves float4s: for odd n the layouts coincide
+// (STRIDE = n^2) and the float4 goes straight across; for even n (n^2 a
+// multiple of 4) each float4 lies inside one token and is scattered into its
+// padded row.  The last nel % 4 floats, or all of them when the tile is not
+// aligned, go one by one.  Measured on GB300 (1 GiB of X per n): the float4
+// copy lifts the n = 3 ... 8 forward and the n = 3, 5 ... 8 backward by 2-22
+// points of HBM bandwidth, but the scatter's bank conflicts cost the
+// bandwidth-bound n = 2 and n = 4 backward 6-8 points, so those keep the
+// one-by-one copy (as does the n = 2 forward, where it made no difference).
+template <int N, bool FWD>
+struct NxnVecCopy {
+  static constexpr bool value = FWD ? N >= 3 : ((N % 2 == 1) || N >= 6);
+};
+
+template <int N, int TILE, bool FWD>
+__device__ __forceinline__ void nxn_tile_in(float* s, const float* g, int nel) {
+  using S = NxnShape<N>;
+  int done = 0;
+  if (NxnVecCopy<N, FWD>::value && (reinterpret_cast<uintptr_t>(g) & 15u) == 0u) {
+    const int n4 = nel >> 2;
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    for (int i = threadIdx.x; i < n4; i += TILE) {
+      const float4 v = __ldg(g4 + i);
+      if constexpr (S::STRIDE == S::NN) {
+        *reinterpret_cast<float4*>(s + 4 * i) = v;
+      } else {
+        static_assert(S::NN % 4 == 0, "a float4 stays inside one token");
+        const int t = (4 * i) / S::NN;
+        float* d = s + t * S::STRIDE + (4 * i - t * S::NN);
+        d[0] = v.x;
+        d[1] = v.y;
+        d[2] = v.z;
+        d[3] = v.w;
+      }
+    }
+    done = n4 << 2;
+  }
+  for (int i = done + threadIdx.x; i < nel; i += TILE) s[(i / S::NN) * S::STRIDE + i % S::NN] = __ldg(g + i);
+}
+
+template <int N, int TILE, bool FWD>
+__device__ __forceinline__ void nxn_tile_out(float* g, const float* s, int nel) {
+  using S = NxnShape<N>;
+  int done = 0;
+  if (NxnVecCopy<N, FWD>::value && (reinterpret_cast<uintptr_t>(g) & 15u) == 0u) {
+    const int n4 = nel >> 2;
+    float4* g4 = reinterpret_cast<float4*>(g);
+    for (int i = threadIdx.x; i < n4; i += TILE) {
+      float4 v;
+      if constexpr (S::STRIDE == S::NN) {
+        v = *reinterpret_cast<const float4*>(s + 4 * i);
+      } else {
+        const int t = (4 * i) / S::NN;
+        const float* d = s + t * S::STRIDE + (4 * i - t * S::NN);
+        v = make_float4(d[0], d[1], d[2], d[3]);
+      }
+      g4[i] = v;
+    }
+    done = n4 << 2;
+  }
+  for (int i = done + threadIdx.x; i < nel; i += TILE) g[i] = s[(i / S::NN) * S::STRIDE + i % S::NN];
 }
 
 struct NxnParams {
@@ -592,7 +685,7 @@ constexpr int nxn_minb() {
 template <int N, int TILE, bool FWD>
 __global__ void __launch_bounds__(TILE, (nxn_minb<N, FWD>())) nxn_kernel(const NxnParams a) {
   using S = NxnShape<N>;
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* s0 = sm;                     // X or P tile, reused for the output
   float* s1 = sm + TILE * S::STRIDE;  // dP tile (backward)
   const int tid = threadIdx.x;
@@ -614,12 +707,8 @@ __global__ void __launch_bounds__(TILE, (nxn_minb<N, FWD>())) nxn_kernel(const N
         if (bytes != 0u && (reinterpret_cast<uintptr_t>(n1) & 15u) == 0u) prefetch_l2_bulk(n1, bytes);
       }
     }
-    const float* g0 = a.in0 + base * S::NN;
-    for (int i = tid; i < nel; i += TILE) s0[(i / S::NN) * S::STRIDE + i % S::NN] = __ldg(g0 + i);
-    if constexpr (!FWD) {
-      const float* g1 = a.in1 + base * S::NN;
-      for (int i = tid; i < nel; i += TILE) s1[(i / S::NN) * S::STRIDE + i % S::NN] = __ldg(g1 + i);
-    }
+    nxn_tile_in<N, TILE, FWD>(s0, a.in0 + base * S::NN, nel);
+    if constexpr (!FWD) nxn_tile_in<N, TILE, FWD>(s1, a.in1 + base * S::NN, nel);
     __syncthreads();
     float out[(FWD && N < kNxnSmemFrom) ? S::NN : 1];
     const bool valid = tid < ntok;
@@ -640,7 +729,7 @@ __global__ void __launch_bounds__(TILE, (nxn_minb<N, FWD>())) nxn_kernel(const N
       } else {
         // P is read from the token's own row of s0 and dX written back
         // there (each thread touches only its own rows)
-        if constexpr (N >= kNxnSmemFrom)
+        if constexpr (NxnBwdSmem<N>::value)
           nxn_backward_smem<N>(s0 + tid * S::STRIDE, s1 + tid * S::STRIDE);
         else
           nxn_backward<N>(s0 + tid * S::STRIDE, s1 + tid * S::STRIDE, s0 + tid * S::STRIDE);
@@ -654,8 +743,7 @@ __global__ void __launch_bounds__(TILE, (nxn_minb<N, FWD>())) nxn_kernel(const N
       }
     }
     __syncthreads();
-    float* go = a.out + base * S::NN;
-    for (int i = tid; i < nel; i += TILE) go[i] = s0[(i / S::NN) * S::STRIDE + i % S::NN];
+    nxn_tile_out<N, TILE, FWD>(a.out + base * S::NN, s0, nel);
     __syncthreads();  // the tile is free for the next load
   }
 }
