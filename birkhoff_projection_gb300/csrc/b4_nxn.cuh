@@ -108,29 +108,41 @@ __device__ __forceinline__ void nxn_weights(const float p[N * N], float w[N][N],
 // positive terms.  w is overwritten.
 template <int N>
 __device__ __forceinline__ void nxn_solve(float w[N][N], const float g[N - 1], float x[N - 1]) {
-  float gg[N - 1], inv[N - 1];
+  if constexpr (N == 3) {
+    // the same elimination written out for two unknowns (the general loops
+    // left w in a 40-byte local-memory frame at n = 3); same operations,
+    // same order
+    const float i0 = rcp(fmaxf(w[0][1] + w[0][2], 1e-30f));
+    const float t = w[0][1] * i0;
+    const float w12 = fmaf(t, w[0][2], w[1][2]);
+    const float g1 = fmaf(t, g[0], g[1]);
+    x[1] = g1 * rcp(fmaxf(w12, 1e-30f));
+    x[0] = fmaf(w[0][1], x[1], g[0]) * i0;
+  } else {
+    float gg[N - 1], inv[N - 1];
 #pragma unroll
-  for (int j = 0; j < N - 1; ++j) gg[j] = g[j];
+    for (int j = 0; j < N - 1; ++j) gg[j] = g[j];
 #pragma unroll
-  for (int a = 0; a < N - 1; ++a) {
-    float d = 0.0f;
+    for (int a = 0; a < N - 1; ++a) {
+      float d = 0.0f;
 #pragma unroll
-    for (int k = a + 1; k < N; ++k) d += w[a][k];
-    inv[a] = rcp(fmaxf(d, 1e-30f));
+      for (int k = a + 1; k < N; ++k) d += w[a][k];
+      inv[a] = rcp(fmaxf(d, 1e-30f));
 #pragma unroll
-    for (int j = a + 1; j < N; ++j) {
-      const float t = w[a][j] * inv[a];
-      if (j < N - 1) gg[j] = fmaf(t, gg[a], gg[j]);
+      for (int j = a + 1; j < N; ++j) {
+        const float t = w[a][j] * inv[a];
+        if (j < N - 1) gg[j] = fmaf(t, gg[a], gg[j]);
 #pragma unroll
-      for (int k = j + 1; k < N; ++k) w[j][k] = fmaf(t, w[a][k], w[j][k]);
+        for (int k = j + 1; k < N; ++k) w[j][k] = fmaf(t, w[a][k], w[j][k]);
+      }
     }
-  }
 #pragma unroll
-  for (int a = N - 2; a >= 0; --a) {
-    float s = gg[a];
+    for (int a = N - 2; a >= 0; --a) {
+      float s = gg[a];
 #pragma unroll
-    for (int j = a + 1; j < N - 1; ++j) s = fmaf(w[a][j], x[j], s);
-    x[a] = s * inv[a];
+      for (int j = a + 1; j < N - 1; ++j) s = fmaf(w[a][j], x[j], s);
+      x[a] = s * inv[a];
+    }
   }
 }
 
