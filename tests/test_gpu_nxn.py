@@ -137,3 +137,31 @@ def test_large_magnitude_nxn(n):
     assert max_abs_err(Pg, Pst) <= 1e-4
     assert residual(Pg).max() <= 1e-4
     assert rel_fro(dX.double().cpu().numpy(), dXst) <= TOL_DX_REL
+
+
+@pytest.mark.parametrize("n", [3, 4, 6, 8])
+def test_unaligned_arrays_match_aligned(n):
+    """Arrays whose base is 4 bytes past a 16-byte boundary take the
+    one-float-at-a-time tile copies; the arithmetic is the same as with the
+    float4 copies, so P and dX must be equal bit for bit.  1000 tokens:
+    several tiles and a ragged last one."""
+    T = 1000
+    X = tokens(n, T, 1.0, seed=500 + n)
+    G = tokens(n, T, 1.0, seed=600 + n)
+    P = b4.forward_nxn(X)
+    dX = b4.backward_nxn(G, P=P)
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 1, device=DEV)
+        v = buf[1:].view(t.shape)
+        v.copy_(t)
+        return v
+
+    Xu, Gu = shifted(X), shifted(G)
+    Pu = shifted(torch.zeros_like(X))
+    dXu = shifted(torch.zeros_like(X))
+    assert Xu.data_ptr() % 16 == 4
+    b4.forward_nxn(Xu, out=Pu)
+    b4.backward_nxn(Gu, P=Pu, out=dXu)
+    assert torch.equal(Pu, P)
+    assert torch.equal(dXu, dX)
