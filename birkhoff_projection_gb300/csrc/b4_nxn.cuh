@@ -7,9 +7,10 @@
 // a log-domain refresh every 8 steps, Laplacian-form Hessian and elimination,
 // step clamp 3 with Newton-decrement damping from the fifth step), written
 // for any n; for n = 2 the single free dual variable has a closed form,
-// which the forward uses instead.  Tokens are staged through shared memory with plain coalesced
-// loads: n x n rows of n^2 * 4 bytes are not all multiples of 16 bytes, which
-// TMA tiles need.
+// which the forward uses instead.  Tokens are staged through shared memory
+// with plain coalesced loads (float4 where the tile allows, see
+// nxn_tile_in): n x n rows of n^2 * 4 bytes are not all multiples of 16
+// bytes, which TMA tiles need.
 #pragma once
 
 #include "b4_device.cuh"
