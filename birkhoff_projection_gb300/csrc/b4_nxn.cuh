@@ -22,8 +22,12 @@ template <int N>
 struct NxnShape {
   static constexpr int NN = N * N;
   // row stride of a token in shared memory: odd, so that lanes reading the
-  // same element of consecutive tokens hit different banks
-  static constexpr int STRIDE = (NN % 2 == 0) ? NN + 1 : NN;
+  // same element of consecutive tokens hit different banks.  For n = 8 it is
+  // 68 instead: every 32-byte row then starts on a 16-byte boundary and moves
+  // as two 128-bit accesses, and for eight consecutive tokens the 16-byte
+  // slots (272 t + 32 r) mod 128 are distinct, so those accesses are free of
+  // bank conflicts.
+  static constexpr int STRIDE = (N == 8) ? NN + 4 : (NN % 2 == 0) ? NN + 1 : NN;
 };
 
 constexpr float kNxnRidge = 1e-7f;
@@ -257,13 +261,29 @@ __device__ __forceinline__ bool nxn_newton(const float* xs, float p[N * N], floa
 // the results are the same bit for bit.
 template <int N>
 __device__ __forceinline__ void nxn_row_ld(const float* r, float v[N]) {
+  if constexpr (N == 8) {  // rows 16-byte aligned (stride 68)
 #pragma unroll
-  for (int j = 0; j < N; ++j) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[j]) : "r"(smem_addr(r + j)));
+    for (int j = 0; j < N; j += 4)
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(v[j]), "=f"(v[j + 1]), "=f"(v[j + 2]), "=f"(v[j + 3])
+                   : "r"(smem_addr(r + j)));
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[j]) : "r"(smem_addr(r + j)));
+  }
 }
 template <int N>
 __device__ __forceinline__ void nxn_row_st(float* r, const float v[N]) {
+  if constexpr (N == 8) {
 #pragma unroll
-  for (int j = 0; j < N; ++j) asm volatile("st.shared.f32 [%0], %1;" ::"r"(smem_addr(r + j)), "f"(v[j]) : "memory");
+    for (int j = 0; j < N; j += 4)
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(r + j)), "f"(v[j]),
+                   "f"(v[j + 1]), "f"(v[j + 2]), "f"(v[j + 3])
+                   : "memory");
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) asm volatile("st.shared.f32 [%0], %1;" ::"r"(smem_addr(r + j)), "f"(v[j]) : "memory");
+  }
 }
 
 // Column sums and edge weights (+ base) accumulated over rows.
@@ -622,10 +642,14 @@ __device__ __forceinline__ void nxn_tile_in(float* s, const float* g, int nel) {
         static_assert(S::NN % 4 == 0, "a float4 stays inside one token");
         const int t = (4 * i) / S::NN;
         float* d = s + t * S::STRIDE + (4 * i - t * S::NN);
-        d[0] = v.x;
-        d[1] = v.y;
-        d[2] = v.z;
-        d[3] = v.w;
+        if constexpr (S::STRIDE % 4 == 0) {
+          *reinterpret_cast<float4*>(d) = v;
+        } else {
+          d[0] = v.x;
+          d[1] = v.y;
+          d[2] = v.z;
+          d[3] = v.w;
+        }
       }
     }
     done = n4 << 2;
@@ -647,7 +671,10 @@ __device__ __forceinline__ void nxn_tile_out(float* g, const float* s, int nel) 
       } else {
         const int t = (4 * i) / S::NN;
         const float* d = s + t * S::STRIDE + (4 * i - t * S::NN);
-        v = make_float4(d[0], d[1], d[2], d[3]);
+        if constexpr (S::STRIDE % 4 == 0)
+          v = *reinterpret_cast<const float4*>(d);
+        else
+          v = make_float4(d[0], d[1], d[2], d[3]);
       }
       g4[i] = v;
     }
@@ -670,9 +697,11 @@ struct NxnParams {
 // Resident CTAs per SM the register allocation aims at (launch-bounds
 // minimum), swept on GB300.  Forward (128-thread CTAs): 3 / 4 for n = 5 / 6,
 // where P, the Hessian and the solve live in registers (128-255 of them
-// uncapped; n = 7 went 1.63 -> 1.00 ms with a cap); 7 / 6 for n = 7 / 8,
-// where P lives in shared memory (nxn_newton_smem: 72 / 80 registers, no
-// spill; n = 8 went 0.72 -> 0.36 ms at 512 MiB).  Backward (64-thread CTAs,
+// uncapped; n = 7 went 1.63 -> 1.00 ms with a cap); 7 / 5 for n = 7 / 8,
+// where P lives in shared memory (nxn_newton_smem: 72 / 96 registers, no
+// spill; n = 8 went 0.72 -> 0.36 ms at 512 MiB; with its 128-bit row
+// accesses a cap of 6 spilled 32 bytes and took 0.599 against 0.579 ms at
+// 1 GiB).  Backward (64-thread CTAs,
 // P and dP tiles in shared memory): the most CTAs that both the shared
 // memory and a spill-free register allocation allow, 11 / 10 / 9 / 6 (the
 // backward forms D row by row, so it needs far fewer registers than it
@@ -687,7 +716,7 @@ struct NxnParams {
 #define B4_NXN_F7 7
 #endif
 #ifndef B4_NXN_F8
-#define B4_NXN_F8 6
+#define B4_NXN_F8 5
 #endif
 template <int N, bool FWD>
 constexpr int nxn_minb() {
