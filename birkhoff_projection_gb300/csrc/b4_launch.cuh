@@ -62,8 +62,18 @@ namespace b4 {
 #ifndef B4_Q_QC
 #define B4_Q_QC 64
 #endif
-#ifndef B4_Q_K1
-#define B4_Q_K1 6
+// Fresh-round length per pass, swept on GB300 at 2^26 N(0,10^2) tokens
+// (K1 = 6 / 7 / 8 / 9 / 10): forward 2.928 / 2.840 / 2.911 / 3.079 /
+// 3.279 ms; fused 4.529 / 4.143 / 3.971 / 4.006 / 4.149 ms; recompute
+// 4.088 / 3.790 / 3.738 / 3.854 / 4.031 ms; N(0,1) unchanged (every token is
+// solved within 5 evaluations).  A resume re-reads X (and, for the passes
+// with a backward, dP) after it may have left L2, so the passes with a
+// backward prefer the longer round.
+#ifndef B4_Q_K1_FWD
+#define B4_Q_K1_FWD 7
+#endif
+#ifndef B4_Q_K1_BWD
+#define B4_Q_K1_BWD 8
 #endif
 #ifndef B4_Q_K2
 #define B4_Q_K2 2
@@ -161,7 +171,8 @@ cudaError_t launch_queue(const LaunchArgs& la, cudaStream_t stream, int dev, int
                        : BF16             ? B4_Q_MINB_BF16
                        : M == Mode::Fused ? B4_Q_MINB_FUSED
                                           : B4_Q_MINB_RECOMPUTE;
-  auto kern = queue_kernel<M, TIn, TOut, B4_Q_WARPS, B4_Q_NSTAGE, B4_Q_QC, B4_Q_K1, B4_Q_K2, MINB>;
+  constexpr int K1 = M == Mode::Forward ? B4_Q_K1_FWD : B4_Q_K1_BWD;
+  auto kern = queue_kernel<M, TIn, TOut, B4_Q_WARPS, B4_Q_NSTAGE, B4_Q_QC, K1, B4_Q_K2, MINB>;
   static std::atomic<int> cap_cache[64];
   int grid_cap = dev < 64 ? cap_cache[dev].load(std::memory_order_acquire) : 0;
   cudaError_t err;

@@ -2,9 +2,9 @@
 through the C ABI.
 
 B4_SCHED_QUEUE (the default) solves each warp's tokens in a fresh round of
-at most 6 evaluations, parks the unsolved ones in shared memory and finishes
-them in resume rounds of 2 evaluations, re-evaluating P in the log domain on
-each resume.  B4_SCHED_LANE keeps one token per thread to the end.
+at most 7 evaluations (8 in the passes with a backward), parks the unsolved
+ones in shared memory and finishes them in resume rounds of 2 evaluations,
+re-evaluating P in the log domain on each resume.  B4_SCHED_LANE keeps one token per thread to the end.
   * N(0,1) tokens all finish within their fresh round (at most 5
     evaluations), so both schedules run the same arithmetic: bit-identical
     results for every pass and dtype.
@@ -68,8 +68,8 @@ def test_queue_parks_and_resumes(kind, T):
     P, b, ev, nc = b4.forward(X, return_dual=True, return_stats=True, schedule="queue")
     _, evl, _ = b4.forward(X, return_stats=True, schedule="lane")
     e = ev.cpu().numpy()
-    # most tokens needed more than the fresh round's 6 evaluations
-    assert (e > 6).mean() > (0.3 if kind == "sigma10" else 0.5)
+    # many tokens needed more than the forward's fresh round of 7 evaluations
+    assert (e > 7).mean() > (0.25 if kind == "sigma10" else 0.5)
     assert e.max() <= 48 and int(nc.item()) == 0
     # the same iteration: evaluation counts within a step or two of the
     # single-round schedule's on average (resumes re-evaluate P in the log domain)
@@ -84,9 +84,13 @@ def test_queue_parks_and_resumes(kind, T):
         z = np64(X) + bb[:, None, :]
         s = np.exp(z - z.max(axis=2, keepdims=True))
         assert max_abs_err(s / s.sum(axis=2, keepdims=True), Pg) <= 1e-4
-    # fused: the same P, and dX against the oracle; recompute: the same dX
+    # fused: P and dX against the oracle (its fresh round is 8 evaluations
+    # against the forward's 7, so a token parked by one is re-evaluated in
+    # the log domain at another step than in the other: P agrees within the
+    # tolerance, not bit for bit); recompute: the same dX as the fused pass
     Pf, dXf = b4.forward_backward(X, G)
-    assert torch.equal(Pf, P)
+    assert max_abs_err(np64(Pf), Pst) <= TOL_P_LARGE
+    assert max_abs_err(np64(Pf), Pg) <= TOL_P_LARGE
     assert rel_fro(np64(dXf), oracle.backward64(Pst, np64(G))) <= TOL_DX_REL
     _, dXr = b4.forward_backward(X, G, want_P=False)
     assert torch.equal(dXr, dXf)
@@ -97,17 +101,17 @@ def test_queue_parks_and_resumes(kind, T):
     assert np.abs(np64(Pb) - Pbst).max() <= 2.0 ** -8 + TOL_P_LARGE
 
 
-@pytest.mark.parametrize("cap", [3, 7, 9])
+@pytest.mark.parametrize("cap", [3, 7, 10])
 def test_queue_caps(cap):
-    """max_evals within every fresh round (3: no token is parked, so the
-    schedules agree bit for bit) and beyond it (7, 9: the cap falls in a
-    resume round)."""
+    """max_evals within every fresh round of the forward (3, 7: no token is
+    parked, so the schedules agree bit for bit) and beyond it (10: the cap
+    falls in a resume round)."""
     X = workloads.normal(20000, 10.0, seed=44, device=DEV)
     Pq, eq, nq = b4.forward(X, max_evals=cap, return_stats=True, schedule="queue")
     Pl, el, nl = b4.forward(X, max_evals=cap, return_stats=True, schedule="lane")
     e = eq.cpu().numpy()
     assert e.max() == cap and e.min() >= 1
-    if cap < 6:
+    if cap <= 7:
         assert torch.equal(Pq, Pl) and torch.equal(eq, el)
         assert int(nq.item()) == int(nl.item())
     res = residual(np64(Pq))
