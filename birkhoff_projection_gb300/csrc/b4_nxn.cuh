@@ -22,13 +22,63 @@ template <int N>
 struct NxnShape {
   static constexpr int NN = N * N;
   // row stride of a token in shared memory: odd, so that lanes reading the
-  // same element of consecutive tokens hit different banks.  For n = 8 it is
-  // 68 instead: every 32-byte row then starts on a 16-byte boundary and moves
-  // as two 128-bit accesses, and for eight consecutive tokens the 16-byte
-  // slots (272 t + 32 r) mod 128 are distinct, so those accesses are free of
-  // bank conflicts.
-  static constexpr int STRIDE = (N == 8) ? NN + 4 : (NN % 2 == 0) ? NN + 1 : NN;
+  // same element of consecutive tokens hit different banks.  For n = 6 and 8
+  // it is 38 and 68 instead, so that every row is 8- or 16-byte aligned and
+  // moves as 64- or 128-bit accesses (NxnRowVec), free of bank conflicts:
+  // for 128-bit accesses the 16-byte slots of eight consecutive tokens,
+  // (272 t + 32 r) mod 128, are distinct, and for 64-bit accesses the
+  // 8-byte slots of sixteen consecutive tokens, (152 t + 24 r) / 8 mod 16 =
+  // (3 t + 3 r) mod 16, are.  (At n = 4 a stride of 20 sped the forward up
+  // by 4% but slowed the bandwidth-bound backward by 5-8%: the float4 tile
+  // stores of neighbouring tokens collide two ways there.)
+  static constexpr int STRIDE = (N == 8) ? 68 : (N == 6) ? 38 : (NN % 2 == 0) ? NN + 1 : NN;
 };
+
+// Width (floats) of the shared-memory accesses that move one row of a token.
+template <int N>
+struct NxnRowVec {
+  static constexpr int value = (N == 8) ? 4 : (N == 6) ? 2 : 1;
+};
+
+// One row of a token in shared memory, loaded or stored in order (each
+// row is fetched where it is used), NxnRowVec<N> floats per access.
+template <int N>
+__device__ __forceinline__ void nxn_row_ld(const float* r, float v[N]) {
+  constexpr int W = NxnRowVec<N>::value;
+  if constexpr (W == 4) {  // rows 16-byte aligned
+#pragma unroll
+    for (int j = 0; j < N; j += 4)
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(v[j]), "=f"(v[j + 1]), "=f"(v[j + 2]), "=f"(v[j + 3])
+                   : "r"(smem_addr(r + j)));
+  } else if constexpr (W == 2) {  // rows 8-byte aligned
+#pragma unroll
+    for (int j = 0; j < N; j += 2)
+      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v[j]), "=f"(v[j + 1]) : "r"(smem_addr(r + j)));
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[j]) : "r"(smem_addr(r + j)));
+  }
+}
+template <int N>
+__device__ __forceinline__ void nxn_row_st(float* r, const float v[N]) {
+  constexpr int W = NxnRowVec<N>::value;
+  if constexpr (W == 4) {
+#pragma unroll
+    for (int j = 0; j < N; j += 4)
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(r + j)), "f"(v[j]),
+                   "f"(v[j + 1]), "f"(v[j + 2]), "f"(v[j + 3])
+                   : "memory");
+  } else if constexpr (W == 2) {
+#pragma unroll
+    for (int j = 0; j < N; j += 2)
+      asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(smem_addr(r + j)), "f"(v[j]), "f"(v[j + 1])
+                   : "memory");
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) asm volatile("st.shared.f32 [%0], %1;" ::"r"(smem_addr(r + j)), "f"(v[j]) : "memory");
+  }
+}
 
 constexpr float kNxnRidge = 1e-7f;
 constexpr float kNxnClamp = 3.0f;
@@ -53,11 +103,12 @@ template <int N>
 __device__ __forceinline__ void nxn_eval_log(const float* xs, const float beta[N], float p[N * N]) {
 #pragma unroll
   for (int i = 0; i < N; ++i) {
-    float z[N];
+    float z[N], x[N];
+    nxn_row_ld<N>(xs + N * i, x);
     float m = -3.0e38f;
 #pragma unroll
     for (int j = 0; j < N; ++j) {
-      z[j] = fmaf(xs[N * i + j], LOG2E, beta[j]);
+      z[j] = fmaf(x[j], LOG2E, beta[j]);
       m = fmaxf(m, z[j]);
     }
     float s = 0.0f;
@@ -186,13 +237,16 @@ __device__ __forceinline__ bool nxn_newton(const float* xs, float p[N * N], floa
   float cs[N];
   float all = 0.0f;
 #pragma unroll
-  for (int j = 0; j < N; ++j) {
-    float s = 0.0f;
+  for (int j = 0; j < N; ++j) cs[j] = 0.0f;
 #pragma unroll
-    for (int i = 0; i < N; ++i) s += xs[N * i + j];
-    cs[j] = s;
-    all += s;
+  for (int i = 0; i < N; ++i) {
+    float x[N];
+    nxn_row_ld<N>(xs + N * i, x);
+#pragma unroll
+    for (int j = 0; j < N; ++j) cs[j] += x[j];
   }
+#pragma unroll
+  for (int j = 0; j < N; ++j) all += cs[j];
   if (!isfinite(all)) {
     const float nan = __int_as_float(0x7fffffff);
 #pragma unroll
@@ -259,33 +313,6 @@ __device__ __forceinline__ bool nxn_newton(const float* xs, float p[N * N], floa
 // Hessian edge weights of the new P on the way, so only those, the dual and
 // one row are live.  The operations and their order are those of nxn_newton:
 // the results are the same bit for bit.
-template <int N>
-__device__ __forceinline__ void nxn_row_ld(const float* r, float v[N]) {
-  if constexpr (N == 8) {  // rows 16-byte aligned (stride 68)
-#pragma unroll
-    for (int j = 0; j < N; j += 4)
-      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                   : "=f"(v[j]), "=f"(v[j + 1]), "=f"(v[j + 2]), "=f"(v[j + 3])
-                   : "r"(smem_addr(r + j)));
-  } else {
-#pragma unroll
-    for (int j = 0; j < N; ++j) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[j]) : "r"(smem_addr(r + j)));
-  }
-}
-template <int N>
-__device__ __forceinline__ void nxn_row_st(float* r, const float v[N]) {
-  if constexpr (N == 8) {
-#pragma unroll
-    for (int j = 0; j < N; j += 4)
-      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(r + j)), "f"(v[j]),
-                   "f"(v[j + 1]), "f"(v[j + 2]), "f"(v[j + 3])
-                   : "memory");
-  } else {
-#pragma unroll
-    for (int j = 0; j < N; ++j) asm volatile("st.shared.f32 [%0], %1;" ::"r"(smem_addr(r + j)), "f"(v[j]) : "memory");
-  }
-}
-
 // Column sums and edge weights (+ base) accumulated over rows.
 template <int N>
 struct NxnAccum {
@@ -447,9 +474,7 @@ __device__ __forceinline__ bool nxn_newton_smem(float* row, const float* xg, flo
 // p, the Hessian and one row are live (holding D or G whole spills at n = 8).
 template <int N>
 __device__ __forceinline__ void nxn_load_row(const float* g, float G[N]) {
-  // ordered shared loads: each row is fetched where it is used
-#pragma unroll
-  for (int j = 0; j < N; ++j) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(G[j]) : "r"(smem_addr(g + j)));
+  nxn_row_ld<N>(g, G);  // ordered shared loads: each row is fetched where it is used
 }
 
 // out_c = sum_{j != c} q_j (h_c - h_j) for every c of one row.  From n = 5
@@ -546,7 +571,8 @@ __device__ __forceinline__ void nxn_backward(const float* Ps, const float* Gs, f
     for (int q = 0; q < N; ++q) H[q] -= lam[q];
     nxn_excl_diff<N>(p + N * k, H, E);
 #pragma unroll
-    for (int q = 0; q < N; ++q) out[N * k + q] = p[N * k + q] * E[q];
+    for (int q = 0; q < N; ++q) E[q] *= p[N * k + q];
+    nxn_row_st<N>(out + N * k, E);
   }
 }
 
@@ -615,13 +641,15 @@ __device__ __forceinline__ void nxn_backward_smem(float* row, const float* Gs) {
 // layout in shared memory (token t at t * STRIDE).  With a 16-byte aligned
 // global tile the copy moves float4s: for odd n the layouts coincide
 // (STRIDE = n^2) and the float4 goes straight across; for even n (n^2 a
-// multiple of 4) each float4 lies inside one token and is scattered into its
-// padded row.  The last nel % 4 floats, or all of them when the tile is not
-// aligned, go one by one.  Measured on GB300 (1 GiB of X per n): the float4
-// copy lifts the n = 3 ... 8 forward and the n = 3, 5 ... 8 backward by 2-22
-// points of HBM bandwidth, but the scatter's bank conflicts cost the
-// bandwidth-bound n = 2 and n = 4 backward 6-8 points, so those keep the
-// one-by-one copy (as does the n = 2 forward, where it made no difference).
+// multiple of 4) each float4 lies inside one token and goes into its row
+// as one float4 or two float2s where the stride aligns the row (n = 8, 6),
+// else as four floats.  The last nel % 4 floats, or all of them when the
+// tile is not aligned, go one by one.  Measured on GB300 (1 GiB of X per
+// n): the float4 copy lifts the n = 3 ... 8 forward and the n = 3, 5 ... 8
+// backward by 2-22 points of HBM bandwidth, but the four-float scatter's
+// bank conflicts cost the bandwidth-bound n = 2 and n = 4 backward 6-8
+// points, so those keep the one-by-one copy (as does the n = 2 forward,
+// where it made no difference).
 template <int N, bool FWD>
 struct NxnVecCopy {
   static constexpr bool value = FWD ? N >= 3 : ((N % 2 == 1) || N >= 6);
@@ -644,6 +672,9 @@ __device__ __forceinline__ void nxn_tile_in(float* s, const float* g, int nel) {
         float* d = s + t * S::STRIDE + (4 * i - t * S::NN);
         if constexpr (S::STRIDE % 4 == 0) {
           *reinterpret_cast<float4*>(d) = v;
+        } else if constexpr (S::STRIDE % 2 == 0) {
+          reinterpret_cast<float2*>(d)[0] = make_float2(v.x, v.y);
+          reinterpret_cast<float2*>(d)[1] = make_float2(v.z, v.w);
         } else {
           d[0] = v.x;
           d[1] = v.y;
@@ -671,10 +702,14 @@ __device__ __forceinline__ void nxn_tile_out(float* g, const float* s, int nel) 
       } else {
         const int t = (4 * i) / S::NN;
         const float* d = s + t * S::STRIDE + (4 * i - t * S::NN);
-        if constexpr (S::STRIDE % 4 == 0)
+        if constexpr (S::STRIDE % 4 == 0) {
           v = *reinterpret_cast<const float4*>(d);
-        else
+        } else if constexpr (S::STRIDE % 2 == 0) {
+          const float2 lo = reinterpret_cast<const float2*>(d)[0], hi = reinterpret_cast<const float2*>(d)[1];
+          v = make_float4(lo.x, lo.y, hi.x, hi.y);
+        } else {
           v = make_float4(d[0], d[1], d[2], d[3]);
+        }
       }
       g4[i] = v;
     }
@@ -781,7 +816,7 @@ __global__ void __launch_bounds__(TILE, (nxn_minb<N, FWD>())) nxn_kernel(const N
       __syncthreads();  // every token's inputs have been read
       if (valid) {
 #pragma unroll
-        for (int e = 0; e < S::NN; ++e) s0[tid * S::STRIDE + e] = out[e];
+        for (int i = 0; i < N; ++i) nxn_row_st<N>(s0 + tid * S::STRIDE + N * i, out + N * i);
       }
     }
     __syncthreads();
