@@ -86,8 +86,9 @@ enum birkhoff4_dtype {
 /* rounding of sums taken in another order.                                */
 enum birkhoff4_schedule {
     B4_SCHED_DEFAULT = 0, /* the measured fastest: B4_SCHED_QUEUE          */
-    /* One thread per token; a warp solves its 32 tokens for at most 6     */
-    /* evaluations, parks the unsolved ones (dual, residual, index, count) */
+    /* One thread per token; a warp solves its 32 tokens for at most 7     */
+    /* evaluations (8 in the passes with a backward), parks the unsolved   */
+    /* ones (dual, residual, index, count)                                 */
     /* in shared memory and solves them later in full warps of parked      */
     /* tokens, 2 evaluations per round, re-evaluating P in the log domain  */
     /* from X and the dual on each resume (which replaces the periodic     */
