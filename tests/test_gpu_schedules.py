@@ -94,11 +94,18 @@ def test_queue_parks_and_resumes(kind, T):
     assert rel_fro(np64(dXf), oracle.backward64(Pst, np64(G))) <= TOL_DX_REL
     _, dXr = b4.forward_backward(X, G, want_P=False)
     assert torch.equal(dXr, dXf)
-    # bf16 in and out, parked tokens included
+    # bf16 in and out, parked tokens included: the forward, and the fused
+    # pass (its own, longer fresh round, parking and resuming with a
+    # backward): P within bf16 rounding of the oracle, dX within bf16
+    # rounding in the relative Frobenius norm
     Xb = X.bfloat16()
+    Gb = G.bfloat16()
     Pb = b4.forward(Xb)
     Pbst = oracle.project64(np64(Xb))
     assert np.abs(np64(Pb) - Pbst).max() <= 2.0 ** -8 + TOL_P_LARGE
+    Pbf, dXbf = b4.forward_backward(Xb, Gb)
+    assert np.abs(np64(Pbf) - Pbst).max() <= 2.0 ** -8 + TOL_P_LARGE
+    assert rel_fro(np64(dXbf), oracle.backward64(Pbst, np64(Gb))) <= 2.0 ** -8 + TOL_DX_REL
 
 
 @pytest.mark.parametrize("cap", [3, 7, 10])
